@@ -1,0 +1,205 @@
+"""Pins of the oracle's group quantizer against what the definition fixes.
+
+Definition ("Strata" MoE tuning notes, lpnh.cn/news/2730718, §2.1 group_quantize
+sketch): per 128-wide group along the input dimension, scale = absmax / 7 and
+q = clamp(round(w / scale), -8, 7). None of the checks below re-types the
+oracle's formula: they use exact rational arithmetic and exhaustive search.
+"""
+import bisect
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import strata_oracle as so
+from workloads import gen
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "quantize_cases.json")
+
+
+# ---------------------------------------------------------------- exact references
+
+def _all_fp16_positive():
+    bits = np.arange(1, 0x7C00, dtype=np.uint16)          # every positive finite fp16
+    vals = bits.view(np.float16)
+    return [Fraction(float(v)) for v in vals], bits
+
+
+_POS16, _POS16_BITS = _all_fp16_positive()
+
+
+def nearest_fp16_exact(x: Fraction) -> Fraction:
+    """Nearest fp16 to a non-negative rational by exhaustive table, ties to even bits."""
+    if x == 0:
+        return Fraction(0)
+    i = bisect.bisect_left(_POS16, x)
+    cands = []
+    if i < len(_POS16):
+        cands.append(i)
+    if i > 0:
+        cands.append(i - 1)
+    else:
+        cands.append(None)                                  # zero is the lower neighbour
+    best = None
+    for c in cands:
+        v = Fraction(0) if c is None else _POS16[c]
+        even = True if c is None else int(_POS16_BITS[c]) % 2 == 0
+        d = abs(v - x)
+        key = (d, not even)
+        if best is None or key < best[0]:
+            best = (key, v)
+    return best[1]
+
+
+def brute_quantize_group(ws):
+    """Exact: scale = fp16-nearest(absmax/7); q = argmin |w - q s| over [-8,7], ties even."""
+    fr = [Fraction(float(w)) for w in ws]
+    a = max(abs(v) for v in fr)
+    s = nearest_fp16_exact(a / 7)
+    qs = []
+    for v in fr:
+        if s == 0:
+            qs.append(0)
+            continue
+        best = None
+        for q in range(-8, 8):
+            key = (abs(v - q * s), q % 2)                    # prefer the even code on a tie
+            if best is None or key < best[0]:
+                best = (key, q)
+        qs.append(best[1])
+    return s, qs
+
+
+def _groups_from(w16, n_groups, rng):
+    rows = rng.integers(0, w16.shape[0], n_groups)
+    gs = rng.integers(0, w16.shape[1] // 128, n_groups)
+    return [(int(r), int(g)) for r, g in zip(rows, gs)]
+
+
+# ---------------------------------------------------------------- tests
+
+def test_golden_hand_built_groups():
+    cases = json.load(open(GOLDEN))
+    for g in cases["groups"]:
+        w = np.zeros((1, 128), dtype=np.float16)
+        for i, v in g["nonzero"]:
+            w[0, i] = v
+        codes, scales = oracle.quantize_groups(w)
+        assert float(scales[0, 0]) == g["scale"], g["why"]
+        q = oracle.unpack_codes(codes)[0]
+        expect = np.zeros(128, dtype=np.int8)
+        for i, c in g["codes_nonzero"]:
+            expect[i] = c
+        np.testing.assert_array_equal(q, expect, err_msg=g["why"])
+
+
+def test_golden_packing():
+    cases = json.load(open(GOLDEN))["packing"]
+    for (a, b), byte in cases["pairs"]:
+        q = np.array([[a, b]], dtype=np.int8)
+        assert int(oracle.pack_codes(q)[0, 0]) == byte
+        np.testing.assert_array_equal(oracle.unpack_codes(np.array([[byte]], np.uint8))[0], [a, b])
+
+
+@pytest.mark.parametrize("scale_exp", [0, -6, -14, -20])
+def test_exact_brute_force_random_groups(scale_exp):
+    """Random N(0,0.02) groups, also rescaled into fp16's subnormal range."""
+    rng = np.random.default_rng(100 + scale_exp)
+    w = gen.expert_weight(0, 0, 0, "gate", 16, 1024)
+    w = (w.astype(np.float32) * np.float32(2.0 ** scale_exp)).astype(np.float16)
+    codes, scales = oracle.quantize_groups(w)
+    q = oracle.unpack_codes(codes)
+    for r, g in _groups_from(w, 12, rng):
+        s, qs = brute_quantize_group(w[r, g * 128:(g + 1) * 128])
+        assert Fraction(float(scales[r, g])) == s
+        np.testing.assert_array_equal(q[r, g * 128:(g + 1) * 128], qs)
+
+
+def test_round_trip_bound_and_absmax():
+    w = gen.expert_weight(0, 0, 1, "up", 64, 2048)
+    codes, scales = oracle.quantize_groups(w)
+    q = oracle.unpack_codes(codes).astype(np.int64)
+    s = scales.astype(np.float64)
+    wg = w.astype(np.float64).reshape(64, 16, 128)
+    qg = q.reshape(64, 16, 128)
+    # |w - q s| <= s/2 holds exactly: check with rationals on a sample, fp64 (exact here) on all
+    err = np.abs(wg - qg * s[..., None])
+    assert np.all(err <= s[..., None] / 2)
+    for r, g in [(0, 0), (13, 7), (63, 15)]:
+        sf = Fraction(float(s[r, g]))
+        for i in range(128):
+            assert abs(Fraction(float(wg[r, g, i])) - qg[r, g, i] * sf) <= sf / 2
+    # the group's absmax element maps to +-7, and -8 never occurs
+    am = np.abs(wg).argmax(axis=-1)
+    top = np.take_along_axis(qg, am[..., None], axis=-1)[..., 0]
+    topw = np.take_along_axis(wg, am[..., None], axis=-1)[..., 0]
+    np.testing.assert_array_equal(np.abs(top), 7)
+    np.testing.assert_array_equal(np.sign(top), np.sign(topw))
+    assert q.min() >= -7
+
+
+def test_idempotent():
+    """Quantizing w = q0*s0 (exact in fp16, one +-7 per group) returns (q0, s0)."""
+    rng = np.random.default_rng(11)
+    n, kdim = 32, 1024
+    q0 = rng.integers(-7, 8, (n, kdim)).astype(np.int8)
+    q0[:, ::128] = rng.choice([-7, 7], (n, kdim // 128))
+    # scales with <= 8 significant bits so that every q*s (q <= 7, 3 bits) is exact in fp16
+    mant = rng.integers(128, 256, (n, kdim // 128))
+    s0 = (mant * 2.0 ** rng.integers(-20, -8, (n, kdim // 128))).astype(np.float16)
+    assert np.all(s0.astype(np.float64) == mant * 2.0 ** np.log2(s0.astype(np.float64) / mant))
+    w64 = q0.reshape(n, -1, 128) * s0.astype(np.float64)[..., None]
+    w = w64.reshape(n, kdim).astype(np.float16)
+    assert np.array_equal(w.astype(np.float64), w64.reshape(n, kdim))
+    codes, scales = oracle.quantize_groups(w)
+    np.testing.assert_array_equal(scales, s0)
+    np.testing.assert_array_equal(oracle.unpack_codes(codes), q0)
+
+
+def test_dequantize_layout_by_hand():
+    # 2 rows x 256: row 0 group 0 codes 1, group 1 codes -2; row 1 group 0 codes 7, group 1 codes -7
+    q = np.zeros((2, 256), dtype=np.int8)
+    q[0, :128], q[0, 128:] = 1, -2
+    q[1, :128], q[1, 128:] = 7, -7
+    sc = np.array([[0.5, 0.25], [2.0, 1.0]], dtype=np.float16)
+    d = oracle.dequantize(oracle.pack_codes(q), sc)
+    assert d[0, 0] == 0.5 and d[0, 200] == -0.5 and d[1, 5] == 14.0 and d[1, 255] == -7.0
+
+
+def test_shape_and_finiteness_errors():
+    with pytest.raises(ValueError):
+        oracle.quantize_groups(np.zeros((2, 100), dtype=np.float16))
+    bad = np.zeros((1, 128), dtype=np.float16)
+    bad[0, 3] = np.inf
+    with pytest.raises(ValueError):
+        oracle.quantize_groups(bad)
+    with pytest.raises(ValueError):
+        oracle.quantize_groups(np.zeros((1, 128), dtype=np.float16), group=64)
+
+
+def test_fp16_quotient_reading_differs_rarely():
+    """The literal fp16 quotient reading: count where it differs from the exact one."""
+    w = gen.expert_weight(0, 0, 3, "gate", 256, 4096)
+    c_exact, s_exact = oracle.quantize_groups(w)
+    c_f16, s_f16 = oracle.quantize_groups_f16_quotient(w)
+    np.testing.assert_array_equal(s_exact, s_f16)
+    diff = np.count_nonzero(oracle.unpack_codes(c_exact) != oracle.unpack_codes(c_f16))
+    assert diff / w.size < 1e-3      # rare; reported, not a failure of either reading
+
+
+def test_planted_rounding_mistake_is_caught(monkeypatch):
+    """Round-half-away (a plausible slip) must fail the hand-built tie group."""
+    monkeypatch.setattr(so.np, "rint", lambda a: np.trunc(a + np.copysign(0.5, a)))
+    cases = json.load(open(GOLDEN))
+    g = cases["groups"][0]
+    w = np.zeros((1, 128), dtype=np.float16)
+    for i, v in g["nonzero"]:
+        w[0, i] = v
+    q = so.unpack_codes(so.quantize_groups(w)[0])[0]
+    expect = np.zeros(128, dtype=np.int8)
+    for i, c in g["codes_nonzero"]:
+        expect[i] = c
+    assert not np.array_equal(q, expect)
