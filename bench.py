@@ -1,0 +1,465 @@
+"""Throughput of the GB300 routed int4-g128 MoE layer (one JSON line on stdout).
+
+Default workload: the decode MoE layer — hidden 4096, expert inter 1536, 288 routed experts
+top-8 + 1 shared expert, int4 g128 experts quantized on the device, bf16 activations, Zipf(1.1)
+router bias — at a batch of 16 tokens (the largest batch of its sweep; the other batches are
+reported under "sweep"). A step is one strata_moe_forward: router + softmax + top-k, grouping,
+gate/up grouped GEMM with SiLU, down grouped GEMM, weighted combine.
+
+Cold L2: every step uses another of 8 copies of the layer's quantized experts (identical
+values, distinct addresses: 8 x 2.8 GB, far above the 129 MB L2) and another of 8 token
+batches, so no step finds its weights in L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl strata|reference] [--batch T]
+
+Under torchrun (N > 1) each rank runs its own replica of the layer on its own GPU (the layer is
+data-parallel over tokens: no exchange step); the time is the max over ranks and the value the
+tokens all ranks processed per second.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import CONFIGS, gen  # noqa: E402
+
+WORKLOAD = "c2"
+METRIC = "MoE-layer tokens/s (decode)"
+N_LAYER_COPIES = 8
+N_TOKEN_BATCHES = 8
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(backend):
+    import torch.distributed as dist
+    ws, rank, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return ws, rank
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(value: float) -> float:
+    """Max of a per-rank float over all ranks (the value itself on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(tokens_per_rank: int, elapsed_s: float, world: int) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world / max_over_ranks(elapsed_s)
+
+
+# ----------------------------------------------------------------------------- clocks
+
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"strata_clocks_{os.getpid()}.csv")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={CLOCK_QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            p = [c.strip() for c in line.split(",")]
+            if len(p) >= 9:
+                rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.nanmedian(sm)), "sm_max_mhz": num(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": float(np.nanmax([num(r[3]) for r in rows]))}
+
+
+# ----------------------------------------------------------------------------- workload
+
+def build_layer(wl, threads=0):
+    """One device layer quantized from the seeded fp16 experts (strata_quantize_groups)."""
+    import torch
+    from int4_grouped_expert_gb300 import MoELayer
+    L = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared)
+    L.set_router(gen.router_weight(wl), gen.router_bias(wl))
+    n = wl.E + wl.shared
+    for s in range(0, n, 16):
+        es = list(range(s, min(n, s + 16)))
+        for e, m in zip(es, gen.expert_weights_many(wl, es, 0, threads)):
+            L.load_expert_fp16(e, *m)
+    torch.cuda.synchronize()
+    L.check_status()
+    return L
+
+
+def layer_copies(L0, n):
+    """n layers sharing L0's router and values but with their own expert storage."""
+    from int4_grouped_expert_gb300 import MoELayer
+    out = [L0]
+    for _ in range(n - 1):
+        L = MoELayer(L0.H, L0.I, L0.E, L0.k, L0.shared)
+        L.w_router.copy_(L0.w_router)
+        L.bias = L0.bias
+        L.copy_expert_from(L0)
+        out.append(L)
+    return out
+
+
+def token_batches(wl, T, n):
+    import torch
+    xs = [gen.activations(T, wl.H, wl.seed, name=f"bench/{T}/{i}") for i in range(n)]
+    return xs, [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda() for x in xs]
+
+
+def routed_experts(L, x_dev, T):
+    """Distinct experts (incl. shared) the batch activates, read back from the GPU routing."""
+    import torch
+    import int4_grouped_expert_gb300 as st
+    ws = torch.empty(L.workspace_size(T), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(x_dev)
+    counts = torch.zeros(L.E, dtype=torch.int32, device="cuda")
+    st.check(st.strata_moe_forward_ex(L.struct(), x_dev, T, out, counts=counts, workspace=ws,
+                                      ws_bytes=ws.numel()), "forward_ex")
+    c = counts.cpu().numpy()
+    return int((c > 0).sum()) + L.shared
+
+
+# ----------------------------------------------------------------------------- strata arm
+
+def time_steps(layers, xs_dev, T, steps, warmup, stream, ws, ws_bytes, out, profiled=False):
+    import torch
+    import int4_grouped_expert_gb300 as st
+    structs = [L.struct() for L in layers]
+    nL, nX = len(structs), len(xs_dev)
+
+    def one(i, evs=None):
+        s = structs[i % nL]
+        x = xs_dev[i % nX]
+        if evs is None:
+            rc = st.strata_moe_forward(s, x, T, out, ws, ws_bytes, stream)
+        else:
+            rc = st.strata_moe_forward_profiled(s, x, T, out, ws, ws_bytes, evs, stream)
+        if rc:
+            st.check(rc, "strata_moe_forward")
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            one(i)
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        stage_ev = None
+        if profiled:
+            stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(steps):
+            one(warmup + i, stage_ev[i] if profiled else None)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    stages = None
+    if profiled:
+        names = ["router", "grouping", "gate_up_gemm", "down_gemm", "combine"]
+        acc = np.zeros(5)
+        for ev in stage_ev:
+            acc += [ev[j].elapsed_time(ev[j + 1]) for j in range(5)]
+        stages = {n: float(a / steps) for n, a in zip(names, acc)}
+    return elapsed_ms, stages
+
+
+def time_e2e(L, xs_host, T, steps, warmup, stream):
+    """Through the C ABI with host buffers: H2D of x and D2H of out inside every call."""
+    import torch
+    import int4_grouped_expert_gb300 as st
+    s = L.struct()
+    need = st.strata_moe_workspace_size(s, T) + st.strata_moe_host_staging_size(s, T)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    xh = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs_host]
+    oh = torch.empty_like(xh[0]).pin_memory()
+    for i in range(warmup):
+        st.check(st.strata_moe_forward_host(s, xh[i % len(xh)], T, oh, ws, need, stream), "host")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        st.check(st.strata_moe_forward_host(s, xh[i % len(xh)], T, oh, ws, need, stream), "host")
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    nbytes = xh[0].numel() * 2
+    return dt, nbytes
+
+
+def cpu_baseline(wl, xs_host, T, budget_s=20.0):
+    """The fp64 oracle on the host cores, on a bounded sample of the batch's tokens."""
+    import oracle
+    from workloads.gen import router_bias, router_weight
+    wr, b = router_weight(wl), router_bias(wl)
+    x = xs_host[0]
+    cache = {}
+
+    def experts(e):
+        if e not in cache:
+            cache[e] = tuple(oracle.quantize_groups(m) for m in gen.expert_weights(wl, e))
+        return cache[e]
+    r = oracle.route_topk(x, wr, b, wl.k)
+    # quantization is part of loading, as on the GPU: pre-quantize the sampled tokens' experts
+    n_tok = 1
+    for e in sorted(set(r["ids"][:n_tok].reshape(-1).tolist()) | ({wl.E} if wl.shared else set())):
+        experts(e)
+    tokens = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.moe_forward(x, wr, b, wl.k, experts, wl.E, wl.shared, tokens=np.arange(n_tok))
+        tokens += n_tok
+        if time.perf_counter() - t0 > budget_s / 4 or tokens >= 4:
+            break
+    dt = time.perf_counter() - t0
+    threads = os.environ.get("OMP_NUM_THREADS") or os.environ.get("OPENBLAS_NUM_THREADS")
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": int(threads) if threads else
+            (os.cpu_count() or 1), "kind": "oracle",
+            "sample": f"{n_tok} token of the T={T} batch per pass ({tokens} tokens, {dt:.1f} s): "
+                      f"fp64 routing over all {wl.E} experts, dequant + FFN of its "
+                      f"{wl.k} routed experts and the shared one; experts pre-quantized"}
+
+
+def peak_numbers():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def run_strata(args):
+    import torch
+    ws_n, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    import int4_grouped_expert_gb300 as st
+    st.lib()
+    wl = CONFIGS[WORKLOAD]
+    T = args.batch
+    L0 = build_layer(wl)
+    layers = layer_copies(L0, max(1, args.copies))
+    stream = torch.cuda.Stream()
+    xs_host, xs_dev = token_batches(wl, T, N_TOKEN_BATCHES)
+    ws_bytes = L0.workspace_size(T)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty(T, wl.H, dtype=torch.bfloat16, device="cuda")
+
+    # distinct activated experts per step (all batches): bytes the layer must stream
+    experts = [routed_experts(L0, x, T) for x in xs_dev]
+    n_exp = float(np.mean(experts))
+    eb = wl.expert_bytes()
+    gu_bytes = n_exp * (2 * wl.H * wl.I) * (0.5 + 2 / 128)
+
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    torch.cuda.nvtx.range_push("timed")
+    elapsed_ms, _ = time_steps(layers, xs_dev, T, args.steps, args.warmup, stream, ws, ws_bytes, out)
+    torch.cuda.nvtx.range_pop()
+    clk = clocks.stop()
+    # per-stage times from a second, profiled pass (events between the kernels)
+    _, stages = time_steps(layers, xs_dev, T, min(args.steps, 2000), args.warmup, stream, ws,
+                           ws_bytes, out, profiled=True)
+    elapsed_s = elapsed_ms / 1e3
+    value = aggregate_throughput(T * args.steps, elapsed_s, ws_n)
+    ms_step = max_over_ranks(elapsed_ms) / args.steps
+
+    sweep = {}
+    for Tb in (() if args.quick else (1, 4, 8, 16)):
+        if Tb == T:
+            continue
+        xh_b, xd_b = token_batches(wl, Tb, N_TOKEN_BATCHES)
+        wsb = torch.empty(L0.workspace_size(Tb), dtype=torch.uint8, device="cuda")
+        ob = torch.empty(Tb, wl.H, dtype=torch.bfloat16, device="cuda")
+        eb_n = float(np.mean([routed_experts(L0, x, Tb) for x in xd_b]))
+        ms, _ = time_steps(layers, xd_b, Tb, min(args.steps, 2000), args.warmup, stream, wsb,
+                           wsb.numel(), ob)
+        per = ms / min(args.steps, 2000)
+        sweep[str(Tb)] = {"tokens_per_s": Tb / (per / 1e3), "us_per_layer": per * 1e3,
+                          "experts": eb_n, "layer_hbm_gbs": eb_n * eb / (per / 1e3) / 1e9}
+    per = ms_step
+    sweep[str(T)] = {"tokens_per_s": T / (per / 1e3), "us_per_layer": per * 1e3, "experts": n_exp,
+                     "layer_hbm_gbs": n_exp * eb / (per / 1e3) / 1e9}
+
+    e2e = None
+    if not args.quick:
+        e2e_steps = max(10, min(args.steps, 500))
+        e2e_dt, xbytes = time_e2e(L0, xs_host, T, e2e_steps, args.warmup, stream)
+        e2e = {"value": aggregate_throughput(T * e2e_steps, e2e_dt, ws_n), "unit": "tokens/s",
+               "h2d_bytes_per_step": xbytes, "d2h_bytes_per_step": xbytes}
+
+    peak, peak_kind = peak_numbers()
+    gu_ms = stages["gate_up_gemm"]
+    achieved = gu_bytes / (gu_ms / 1e3) / 1e9
+    layer_gbs = n_exp * eb / (ms_step / 1e3) / 1e9
+    rec = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "tokens_per_step": T, "H": wl.H, "I": wl.I, "E": wl.E,
+                   "k": wl.k, "shared": wl.shared, "router": "zipf(s=1.1), top-20% take 80%",
+                   "weights": "int4 g128 codes + fp16 scales, quantized on device",
+                   "l2": f"inputs larger than L2: {N_LAYER_COPIES} expert-storage copies x "
+                         f"{N_TOKEN_BATCHES} token batches rotated per step",
+                   "parallelism": f"replicas x{ws_n}"},
+        "roofline": {"kernel": "gate_up_gemm (grouped W4A16 GEMM + SiLU)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": gu_bytes, "traffic": None},
+        "layer_hbm": {"achieved_gbs": layer_gbs, "frac": layer_gbs / peak,
+                      "bytes_per_step": n_exp * eb, "experts_per_step": n_exp},
+        "stages_us": {k: v * 1e3 for k, v in stages.items()},
+        "sweep": sweep,
+        "e2e": e2e,
+        "gpu_launches": 6 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        if ws_n == 1 and not args.quick:
+            rec["cpu_baseline"] = cpu_baseline(wl, xs_host, T)
+        print(json.dumps(rec), flush=True)
+
+
+def run_reference(args):
+    """The oracle on the host cores, same metric and workload, each step a bounded sample."""
+    ws_n, rank = init_dist("gloo")
+    if rank != 0:
+        return
+    import oracle
+    wl = CONFIGS[WORKLOAD]
+    T = args.batch
+    x = gen.activations(T, wl.H, wl.seed, name=f"bench/{T}/0")
+    wr, b = gen.router_weight(wl), gen.router_bias(wl)
+    cache = {}
+
+    def experts(e):
+        if e not in cache:
+            cache[e] = tuple(oracle.quantize_groups(m) for m in gen.expert_weights(wl, e))
+        return cache[e]
+    r = oracle.route_topk(x, wr, b, wl.k)
+    sample = max(1, min(T, int(args.ref_tokens)))
+    order = [t % T for t in range(args.warmup + args.steps)]
+    need = set()
+    for t in order:
+        need |= set(r["ids"][t].tolist())
+    for e in sorted(need | ({wl.E} if wl.shared else set())):
+        experts(e)
+    for i in range(args.warmup):
+        oracle.moe_forward(x, wr, b, wl.k, experts, wl.E, wl.shared, tokens=[order[i]])
+    t0 = time.perf_counter()
+    done = 0
+    for i in range(args.steps):
+        t = order[args.warmup + i]
+        oracle.moe_forward(x, wr, b, wl.k, experts, wl.E, wl.shared,
+                           tokens=[(t + j) % T for j in range(sample)])
+        done += 1
+        if time.perf_counter() - t0 > args.ref_budget_s:
+            break                                   # a bounded run: steps_timed says how many
+    dt = time.perf_counter() - t0
+    val = sample * done / dt
+    cores = os.cpu_count() or 1
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": ws_n,
+        "steps": args.steps, "steps_timed": done, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / done,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "tokens_per_step": sample, "H": wl.H, "I": wl.I,
+                   "E": wl.E, "k": wl.k, "shared": wl.shared},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{sample} token(s) of the T={T} batch per step: fp64 routing, "
+                                   "dequant + FFN of its experts; experts pre-quantized"},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None,
+                   help="timed steps (default 5000; 10 for --impl reference)")
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--copies", type=int, default=N_LAYER_COPIES,
+                   help="expert-storage copies rotated per step (cold L2)")
+    p.add_argument("--quick", action="store_true",
+                   help="headline only: no batch sweep, no host-buffer run, no CPU baseline")
+    p.add_argument("--batch", type=int, default=16)
+    p.add_argument("--impl", choices=["strata", "reference"], default="strata")
+    p.add_argument("--ref-tokens", type=int, default=1)
+    p.add_argument("--ref-budget-s", type=float, default=240.0)
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.steps is None:
+        args.steps = 10 if args.impl == "reference" else 5000
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_strata(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+/*
+ * strata.h — C ABI of the GB300 routed MoE FFN layer with int4 group-quantized experts.
+ *
+ * The operations follow the problem statement of five write-ups about the
+ * "Strata" MoE engine (the pages have no titles; each is named by its address):
+ *   [tuning-3090] xdnf.cn/news/329730            §3.2 tokens routed to one expert are
+ *                                                gathered into one group of a single
+ *                                                grouped-GEMM launch; §5.2 fixed,
+ *                                                pre-allocated buffers
+ *   [tuning-moe]  lpnh.cn/news/2730718           §2.1 group_quantize(weight, 128, 4):
+ *                                                scale = absmax/7, clamp(-8, 7);
+ *                                                §2.3 point 1: router softmax + top-k
+ *                                                fused in one kernel
+ *   [tok-102]     zwxr.cn/news/276292            §3.2 routing engine: logits in,
+ *                                                softmax, partial sort, expert ids out
+ *   [glm-4090]    haowenji.com/articles/x-2109226022155796480
+ *                                                §01 experts are Gate/Up + Down
+ *                                                projections; 8 routed + 1 shared
+ *                                                expert per token
+ *
+ * Conventions for every call below.
+ *  - All tensor pointers are DEVICE pointers owned by the caller, unless a
+ *    parameter says "host". The library never allocates or frees memory and keeps
+ *    no state between calls; scratch memory is a caller-owned workspace whose size
+ *    the *_workspace_size queries return.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) unless documented as blocking.
+ *  - Arguments are validated on the host before anything is launched; a failed
+ *    check returns its status and has no side effects.
+ *  - Launch failures return STRATA_ERR_CUDA (from cudaGetLastError).
+ *  - Kernels never trap. Faults they detect in the data (a non-finite weight, an
+ *    expert id out of range) set bits in a device status word, read back with
+ *    strata_workspace_status / strata_read_status (these synchronize the stream).
+ *  - Dtypes: bf16/fp16 tensors are passed as void* to raw 16-bit storage.
+ *  - Layouts are row-major and contiguous unless stated.
+ */
+#ifndef STRATA_H_
+#define STRATA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* strata_stream; /* identical to cudaStream_t */
+
+typedef enum {
+  STRATA_OK = 0,
+  STRATA_ERR_INVALID_ARG = 1,   /* null pointer, bad flag, k > E, ... */
+  STRATA_ERR_SHAPE = 2,         /* a dimension is not a multiple of 128, or out of range */
+  STRATA_ERR_UNSUPPORTED = 3,   /* group size other than 128, or a size above a limit */
+  STRATA_ERR_WORKSPACE = 4,     /* workspace null, misaligned or smaller than required */
+  STRATA_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
+  STRATA_ERR_DEVICE_STATUS = 6, /* the device status word reported a data fault */
+  STRATA_ERR_TIMEOUT = 7        /* a bounded device-side wait gave up */
+} strata_status;
+
+/* Flags of strata_route_topk / strata_moe_layer.flags. */
+#define STRATA_RENORM 0x1u       /* renormalise the k gates of a token to sum to 1 (off by default:
+                                    the pages never renormalise) */
+#define STRATA_ADD_RESIDUAL 0x2u /* moe_forward only: out = bf16(x + MoE(x)), one rounding */
+
+/* Bits of the device status word. */
+#define STRATA_DEV_NONFINITE 0x1u /* a quantized group held inf/nan (its scale is written as NaN,
+                                     its codes as 0) */
+#define STRATA_DEV_BAD_ID 0x2u    /* an expert id outside [0, E) reached the permutation */
+#define STRATA_DEV_TIMEOUT 0x4u   /* a bounded device wait gave up */
+
+#define STRATA_GROUP 128     /* [tuning-moe] §2.1: 128 weights share one scale */
+#define STRATA_MAX_EXPERTS 1024
+#define STRATA_MAX_TOPK 32
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* strata_status_string(int status);
+
+/* ABI version: major*10000 + minor*100 + patch. */
+int strata_version(void);
+
+/*
+ * strata_quantize_groups — symmetric int4 group quantization, [tuning-moe] §2.1.
+ *
+ * For each row i of w and each group g of 128 consecutive columns:
+ *   scale[i,g] = fp16_round_nearest_even(absmax(w[i, 128g : 128g+128]) / 7)
+ *   q[i,c]     = clamp(round_half_even(w[i,c] / scale[i,g]), -8, 7)   (exact quotient)
+ *   a group whose stored scale is 0 gets q = 0.
+ * w_fp16      [n, k] fp16, row-major (device).
+ * codes       [n, k/2] uint8 (device, written): byte c of row i holds q[i,2c] in bits 0-3 and
+ *             q[i,2c+1] in bits 4-7, as 4-bit two's complement.
+ * scales_fp16 [n, k/128] fp16 (device, written).
+ * group_size  must be 128 (STRATA_ERR_UNSUPPORTED otherwise); k % 128 != 0 -> STRATA_ERR_SHAPE;
+ *             n == 0 is a no-op.
+ * dev_status  optional device uint32 (NULL to skip): STRATA_DEV_NONFINITE is OR-ed in when a
+ *             group holds inf/nan; such a group gets scale NaN and codes 0.
+ * Buffers must be 16-byte aligned (STRATA_ERR_INVALID_ARG otherwise).
+ */
+strata_status strata_quantize_groups(const void* w_fp16, int64_t n, int64_t k, int32_t group_size,
+                                     uint8_t* codes, void* scales_fp16, uint32_t* dev_status,
+                                     strata_stream stream);
+
+/*
+ * strata_route_topk — router GEMV + softmax + top-k + token grouping,
+ * [tuning-moe] §2.3 point 1 and [tok-102] §3.2; grouping per [tuning-3090] §3.2.
+ *
+ *   logits[t,e] = sum_h x[t,h] * w_router[e,h] + bias[e]     (fp32 accumulation)
+ *   p[t,:]      = softmax(logits[t,:])                        (fp32)
+ *   ids[t,:]    = the k experts of largest logit, in descending order, ties to the lower id
+ *   gates[t,j]  = p[t, ids[t,j]]   (divided by sum_j of them when flags & STRATA_RENORM)
+ * and, when the pointers are non-NULL, the grouping of the T*k routed rows by expert, rows
+ * ordered by (expert, token):
+ *   counts[e]   rows routed to expert e;  offsets[e] = sum_{e'<e} counts[e'], offsets[E] = T*k
+ *   perm[r]     token of row r;           inv[t,j] = row of (t, ids[t,j])
+ * x_bf16 [T,H] bf16; w_router [E,H] fp32; bias [E] fp32 or NULL.
+ * ids [T,k] int32, gates [T,k] fp32 (required); counts [E], offsets [E+1], perm [T*k],
+ * inv [T,k] int32 (optional as a group: all four or none).
+ * Limits: H % 128 == 0, 1 <= k <= min(E, 32), E <= 1024, T >= 0 (T == 0 writes counts/offsets
+ * as zeros only). workspace >= strata_route_workspace_size(T, E, k) bytes, 256-byte aligned.
+ */
+size_t strata_route_workspace_size(int64_t T, int32_t E, int32_t k);
+strata_status strata_route_topk(const void* x_bf16, const float* w_router, const float* bias,
+                                int64_t T, int64_t H, int32_t E, int32_t k, uint32_t flags,
+                                int32_t* ids, float* gates, int32_t* counts, int32_t* offsets,
+                                int32_t* perm, int32_t* inv, void* workspace, size_t ws_bytes,
+                                strata_stream stream);
+
+/*
+ * One routed MoE FFN layer. Expert weights are the outputs of strata_quantize_groups, stacked
+ * over experts; the shared expert, when has_shared != 0, is index E of each stack.
+ * Expert e computes y = (silu(x Wg_e^T) * (x Wu_e^T)) Wd_e^T   ([glm-4090] §01: Gate/Up, Down).
+ */
+typedef struct {
+  int64_t H;             /* hidden size, % 128 == 0 */
+  int64_t I;             /* expert intermediate size, % 128 == 0 */
+  int32_t E;             /* routed experts, 1..1024 */
+  int32_t k;             /* experts per token, 1..min(E, 32) */
+  int32_t has_shared;    /* 0 or 1: expert E is always on, gate 1 */
+  uint32_t flags;        /* STRATA_RENORM | STRATA_ADD_RESIDUAL */
+  const float* w_router; /* [E, H] fp32 */
+  const float* bias;     /* [E] fp32 or NULL */
+  const uint8_t* gate_codes; const void* gate_scales; /* [E+S, I, H/2] u8, [E+S, I, H/128] fp16 */
+  const uint8_t* up_codes;   const void* up_scales;   /* same shapes */
+  const uint8_t* down_codes; const void* down_scales; /* [E+S, H, I/2] u8, [E+S, H, I/128] fp16 */
+} strata_moe_layer;
+
+/* Workspace bytes strata_moe_forward needs for up to T_max tokens (0 if the layer is invalid). */
+size_t strata_moe_workspace_size(const strata_moe_layer* layer, int64_t T_max);
+
+/*
+ * strata_moe_forward — out[t] = sum_j gates[t,j] * y_{ids[t,j]}(x_t) + has_shared * y_E(x_t)
+ * (+ x_t with STRATA_ADD_RESIDUAL), summed in fp32 and rounded once to bf16.
+ * x_bf16 [T,H], out_bf16 [T,H] bf16 (device; out may not alias x). T == 0 is a no-op.
+ * workspace: >= strata_moe_workspace_size(layer, T) bytes, 256-byte aligned, device. The
+ * workspace needs no initialisation; one workspace serves one stream at a time.
+ */
+strata_status strata_moe_forward(const strata_moe_layer* layer, const void* x_bf16, int64_t T,
+                                 void* out_bf16, void* workspace, size_t ws_bytes,
+                                 strata_stream stream);
+
+/*
+ * strata_moe_forward_ex — strata_moe_forward that also copies the routing out (each pointer
+ * optional, device): ids [T,k], gates [T,k], counts [E], offsets [E+1], perm [T*k], inv [T,k],
+ * with the meanings of strata_route_topk.
+ */
+strata_status strata_moe_forward_ex(const strata_moe_layer* layer, const void* x_bf16, int64_t T,
+                                    void* out_bf16, int32_t* ids, float* gates, int32_t* counts,
+                                    int32_t* offsets, int32_t* perm, int32_t* inv,
+                                    void* workspace, size_t ws_bytes, strata_stream stream);
+
+/*
+ * strata_moe_forward_profiled — strata_moe_forward that also records caller-created CUDA events
+ * (cudaEvent_t, passed as void*) on `stream` at the stage boundaries, for per-kernel timing:
+ *   events[0] before the router, [1] after the router (logits + top-k), [2] after the grouping,
+ *   [3] after the gate/up grouped GEMM, [4] after the down grouped GEMM, [5] after the combine.
+ * n_events must be 6; any NULL event is skipped. Results are identical to strata_moe_forward.
+ */
+#define STRATA_PROFILE_EVENTS 6
+strata_status strata_moe_forward_profiled(const strata_moe_layer* layer, const void* x_bf16,
+                                          int64_t T, void* out_bf16, void* workspace,
+                                          size_t ws_bytes, strata_stream stream,
+                                          void* const* events, int32_t n_events);
+
+/*
+ * strata_moe_forward_host — the same layer with HOST activations: copies x_host (bf16 [T,H],
+ * host memory, best pinned) to the workspace, runs the layer, copies the result to out_host
+ * (bf16 [T,H], host). BLOCKING: returns after out_host is written (synchronizes `stream`).
+ * workspace >= strata_moe_workspace_size(layer, T) + strata_moe_host_staging_size(layer, T).
+ */
+size_t strata_moe_host_staging_size(const strata_moe_layer* layer, int64_t T_max);
+strata_status strata_moe_forward_host(const strata_moe_layer* layer, const void* x_host,
+                                      int64_t T, void* out_host, void* workspace, size_t ws_bytes,
+                                      strata_stream stream);
+
+/*
+ * Device status of a route/forward workspace: synchronizes `stream`, returns the status word in
+ * *status_out (host) and clears it. Returns STRATA_ERR_DEVICE_STATUS when any bit was set.
+ */
+strata_status strata_workspace_status(void* workspace, strata_stream stream, uint32_t* status_out);
+
+/* Same for a caller-owned device status word (e.g. the one given to strata_quantize_groups). */
+strata_status strata_read_status(uint32_t* dev_status, strata_stream stream, uint32_t* status_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* STRATA_H_ */

@@ -1,0 +1,56 @@
+// K5: weighted un-permute / combine of the expert outputs. Each token's output is the sum of its k
+// routed expert outputs weighted by their gates, plus the always-on shared expert with gate 1
+// ("GLM-5.3-Flash on one 4090", haowenji.com/articles/x-2109226022155796480, §01: 8 routed + 1
+// shared expert per token), summed in fp32 in a fixed order (j = 0..k-1, shared, residual) and
+// rounded once to bf16.
+#include "kernels.cuh"
+
+namespace strata {
+
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y,
+                                                      const float* __restrict__ gates,
+                                                      const int* __restrict__ inv,
+                                                      const __nv_bfloat16* __restrict__ x, int T,
+                                                      int H, int k, int has_shared, int R,
+                                                      int residual, __nv_bfloat16* __restrict__ out) {
+  const int t = blockIdx.x;
+  const int64_t H4 = H / 4;
+  for (int64_t c = threadIdx.x; c < H4; c += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const float g = gates[static_cast<int64_t>(t) * k + j];
+      const int row = inv[static_cast<int64_t>(t) * k + j];
+      const float4 v = reinterpret_cast<const float4*>(y + static_cast<int64_t>(row) * H)[c];
+      acc.x = fmaf(g, v.x, acc.x); acc.y = fmaf(g, v.y, acc.y);
+      acc.z = fmaf(g, v.z, acc.z); acc.w = fmaf(g, v.w, acc.w);
+    }
+    if (has_shared) {
+      const float4 v = reinterpret_cast<const float4*>(y + static_cast<int64_t>(R + t) * H)[c];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    if (residual) {
+      const uint2 raw = reinterpret_cast<const uint2*>(x + static_cast<int64_t>(t) * H)[c];
+      const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      const float2 a = __bfloat1622float2(p[0]), b = __bfloat1622float2(p[1]);
+      acc.x += a.x; acc.y += a.y; acc.z += b.x; acc.w += b.y;
+    }
+    uint2 o;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+    o.x = *reinterpret_cast<uint32_t*>(&lo);
+    o.y = *reinterpret_cast<uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(out + static_cast<int64_t>(t) * H)[c] = o;
+  }
+}
+
+cudaError_t launch_combine(const float* y, const float* gates, const int* inv, const void* x,
+                           int64_t T, int64_t H, int k, int has_shared, int64_t R, int residual,
+                           void* out, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  combine_kernel<<<static_cast<unsigned>(T), 256, 0, stream>>>(
+      y, gates, inv, static_cast<const __nv_bfloat16*>(x), static_cast<int>(T),
+      static_cast<int>(H), k, has_shared, static_cast<int>(R), residual,
+      static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace strata

@@ -1,0 +1,84 @@
+// Shared device helpers of the strata kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/strata.h"
+
+namespace strata {
+
+constexpr int kGroup = STRATA_GROUP;  // weights per scale group
+
+// Workspace header (first 256 bytes of every route/forward workspace).
+struct WsHeader {
+  uint32_t status;      // STRATA_DEV_* bits
+  int32_t nseg;         // active expert segments (routed experts with rows, then the shared one)
+  int32_t n_items_gu;   // gate/up work items
+  int32_t n_items_dn;   // down work items
+  int32_t n_tiles_gu;   // (tcgen05 path) gate/up tiles
+  int32_t n_tiles_dn;   // (tcgen05 path) down tiles
+  int32_t pad[58];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+__device__ __forceinline__ void set_status(uint32_t* st, uint32_t bits) {
+  if (st) atomicOr(st, bits);
+}
+
+__device__ __forceinline__ uint32_t lane_id() {
+  uint32_t l;
+  asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
+  return l;
+}
+
+// ---------------------------------------------------------------------------- mma.sync bf16
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + C (fp32).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1, const float (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%11,%12,%13};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+        "f"(c[2]), "f"(c[3]));
+}
+
+// ---------------------------------------------------------------------------- int4 -> bf16
+// A 32-bit word holds 8 codes, nibble i = element i (4-bit two's complement). After flipping the
+// sign bit of every nibble (w ^ 0x88888888 turns q into q + 8 in [0, 15]), OR-ing a nibble into the
+// low mantissa bits of bf16 128.0 (0x4300) gives exactly 128 + q + 8; subtracting 136 leaves q.
+// pair(w, i) returns bf16x2 {element i, element i + 4} (low half first).
+__device__ __forceinline__ uint32_t int4pair_to_bf16x2(uint32_t w_offset_binary, int i) {
+  uint32_t v = (w_offset_binary >> (4 * i)) & 0x000F000Fu;
+  v |= 0x43004300u;
+  __nv_bfloat162 r = *reinterpret_cast<__nv_bfloat162*>(&v);
+  const __nv_bfloat162 bias = __floats2bfloat162_rn(136.0f, 136.0f);
+  r = __hsub2(r, bias);  // exact: small integers
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Byte permute: result bytes selected from {a (bytes 0-3), b (bytes 4-7)}.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// ---------------------------------------------------------------------------- cp.async
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool pred) {
+  uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  int sz = pred ? 16 : 0;  // zero-fill when the source row does not exist
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(sz));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ float silu_f(float u) { return u / (1.0f + expf(-u)); }
+
+}  // namespace strata

@@ -1,0 +1,57 @@
+// Launchers and argument blocks shared between the kernels and the C ABI layer.
+#pragma once
+
+#include "common.cuh"
+
+namespace strata {
+
+struct PermuteArgs {
+  const int* ids;
+  int T, k, E, has_shared;
+  int* counts;   // [E]
+  int* offsets;  // [E+1]
+  int* perm;     // [T*k + T]: rows of the shared segment follow the routed rows
+  int* inv;      // [T*k]
+  // grouped-GEMM work lists (optional: seg_expert == nullptr skips them)
+  int* seg_expert;
+  int* seg_row0;
+  int* seg_rows;
+  int* seg_item_gu;  // [nseg + 1] exclusive prefix of gate/up items
+  int* seg_item_dn;  // [nseg + 1]
+  int tokc;          // rows per work item along the token dimension
+  int mtiles_gu;     // I / 16
+  int mtiles_dn;     // H / 16
+  WsHeader* hdr;
+  uint32_t* status;
+};
+
+struct GemmArgs {
+  const uint8_t* codes0;     // gate (gate/up mode) or down codes, [experts, N, K/2]
+  const __half* scales0;     // [experts, N, K/128]
+  const uint8_t* codes1;     // up codes (gate/up mode)
+  const __half* scales1;
+  const __nv_bfloat16* act;  // gate/up: x [T, K]; down: h [rows, K]
+  const int* perm;           // gate/up: token of each row; down: unused (row indexes h)
+  void* out;                 // gate/up: h bf16 [rows, N]; down: y fp32 [rows, N]
+  int K;                     // contraction length (H for gate/up, I for down)
+  int N;                     // weight rows per expert (I for gate/up, H for down)
+  const WsHeader* hdr;
+  const int* seg_expert;
+  const int* seg_row0;
+  const int* seg_rows;
+  const int* seg_item;       // exclusive prefix of work items per segment, [nseg + 1]
+};
+
+cudaError_t launch_quantize(const void* w, int64_t n, int64_t k, uint8_t* codes, void* scales,
+                            uint32_t* status, cudaStream_t stream, int num_sms);
+int router_num_splits(int64_t T, int64_t H, int E, int num_sms);
+cudaError_t launch_router(const void* x, const float* wr, const float* bias, int64_t T, int64_t H,
+                          int E, int k, uint32_t flags, int nsplit, float* partial, int* ids,
+                          float* gates, cudaStream_t stream);
+cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t stream);
+cudaError_t launch_gemm_warp(const GemmArgs& a, bool gate_up, int num_sms, cudaStream_t stream);
+cudaError_t launch_combine(const float* y, const float* gates, const int* inv, const void* x,
+                           int64_t T, int64_t H, int k, int has_shared, int64_t R, int residual,
+                           void* out, cudaStream_t stream);
+
+}  // namespace strata

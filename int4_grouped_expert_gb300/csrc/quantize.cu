@@ -1,0 +1,79 @@
+// K1: symmetric int4 group quantization ("Strata" MoE tuning notes, lpnh.cn/news/2730718, §2.1
+// group_quantize sketch: scale = absmax / (2^(bits-1) - 1), codes = round(w / scale) clamped to
+// [-8, 7], 128 weights per group).
+//
+// HBM-streaming pass: 16 threads own one 128-wide group (8 fp16 = one 16-byte load each), find
+// the group's absmax with four butterfly shuffles, and write 4 bytes of packed codes each (the
+// half-warp's 64 bytes are contiguous) plus one fp16 scale. Each thread walks several groups with
+// a grid-stride loop so loads of the next group are in flight while the current one is packed.
+//
+// Exactness: absmax / 7.0f is an IEEE fp32 division rounded once more to fp16 (no double-rounding
+// hazard: a/7 has a period-3 binary expansion, never 12 equal bits in a row), and w / s is an IEEE
+// fp32 division of two fp16 values, so rintf() decides every half-way case like the exact
+// quotient (a spurious tie would need the 11-bit ratio to sit within 2^-21 of x.5).
+#include "kernels.cuh"
+
+namespace strata {
+
+__global__ void __launch_bounds__(256) quantize_groups_kernel(const uint4* __restrict__ w,
+                                                              int64_t n_groups,
+                                                              uint32_t* __restrict__ codes,
+                                                              __half* __restrict__ scales,
+                                                              uint32_t* status) {
+  const int sub = threadIdx.x & 15;  // position in the group
+  // the two half-warps may leave the loop at different times: shuffle within the half only
+  const unsigned half_mask = (threadIdx.x & 16) ? 0xFFFF0000u : 0x0000FFFFu;
+  const int64_t first = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+  const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4;
+  for (int64_t g = first; g < n_groups; g += stride) {
+    uint4 v = __ldcs(w + g * 16 + sub);  // streaming read: every weight is touched once
+    const __half* h = reinterpret_cast<const __half*>(&v);
+    float f[8];
+    float amax = 0.0f;
+    bool finite = true;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      f[i] = __half2float(h[i]);
+      finite &= isfinite(f[i]);
+      amax = fmaxf(amax, fabsf(f[i]));
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+      amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, o));
+      finite = __shfl_xor_sync(half_mask, finite ? 1 : 0, o) != 0 && finite;
+    }
+    __half s_h = __float2half_rn(amax / 7.0f);
+    const float s = __half2float(s_h);
+    uint32_t packed = 0;
+    if (finite && s > 0.0f) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float q = rintf(f[i] / s);
+        q = fminf(fmaxf(q, -8.0f), 7.0f);
+        packed |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xFu) << (4 * i);
+      }
+    }
+    if (!finite) {
+      s_h = __ushort_as_half(0x7E00);  // NaN scale marks the group
+      if (sub == 0) set_status(status, STRATA_DEV_NONFINITE);
+    }
+    __stcs(codes + g * 16 + sub, packed);
+    if (sub == 0) scales[g] = s_h;
+  }
+}
+
+cudaError_t launch_quantize(const void* w, int64_t n, int64_t k, uint8_t* codes, void* scales,
+                            uint32_t* status, cudaStream_t stream, int num_sms) {
+  const int64_t n_groups = n * (k / kGroup);
+  if (n_groups == 0) return cudaSuccess;
+  const int threads = 256;                       // 16 groups per block and pass
+  int64_t blocks = (n_groups + 15) / 16;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;  // ~8 resident blocks/SM, grid-stride
+  if (blocks > cap) blocks = cap;
+  quantize_groups_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      static_cast<const uint4*>(w), n_groups, reinterpret_cast<uint32_t*>(codes),
+      static_cast<__half*>(scales), status);
+  return cudaGetLastError();
+}
+
+}  // namespace strata

@@ -1,0 +1,193 @@
+// K2: router logits + softmax + top-k ("Strata" MoE tuning notes, lpnh.cn/news/2730718, §2.3,
+// point 1: softmax and top-k selection fused into one kernel; routing engine of the 102.7 tok/s
+// write-up, zwxr.cn/news/276292, §3.2: softmax over the logits, partial sort, expert ids out).
+//
+// Two launches:
+//  router_logits_kernel  fp32 x*Wr^T tile GEMM (SIMT, fp32 accumulation in 32-term chunks joined by
+//                        compensated addition), split along H so that a
+//                        decode batch of a few tokens still spreads the router matrix over the SMs.
+//                        Partial sums go to the workspace as [split][T][E].
+//  router_topk_kernel    one warp per token: sums the partials in split order (deterministic), adds
+//                        the bias, softmax in fp32, then k rounds of a warp arg-max (largest logit,
+//                        lower expert id on ties), gates = p of the chosen experts.
+#include "kernels.cuh"
+
+namespace strata {
+
+constexpr int kRouterBT = 32;  // tokens per CTA tile
+constexpr int kRouterBE = 64;  // experts per CTA tile
+constexpr int kRouterKC = 32;  // H chunk staged in shared memory
+
+__global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16* __restrict__ x,
+                                                            const float* __restrict__ wr, int T,
+                                                            int H, int E, int h_per_split,
+                                                            float* __restrict__ partial) {
+  __shared__ float xs[kRouterKC][kRouterBT + 1];
+  __shared__ float ws[kRouterKC][kRouterBE + 4];
+  const int tid = threadIdx.x;
+  const int e0 = blockIdx.x * kRouterBE;
+  const int t0 = blockIdx.y * kRouterBT;
+  const int split = blockIdx.z;
+  const int hbeg = split * h_per_split;
+  const int hend = min(H, hbeg + h_per_split);
+  const int tx = tid & 15;  // experts tx*4 .. tx*4+3
+  const int ty = tid >> 4;  // tokens ty*2, ty*2+1
+  float acc[2][4] = {}, comp[2][4] = {};
+
+  for (int hc = hbeg; hc < hend; hc += kRouterKC) {
+    {  // x tile: 32 tokens x 32 h, 4 bf16 per thread
+      const int tok = tid >> 3, kq = (tid & 7) * 4;
+      const int t = t0 + tok;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (t < T) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(x + static_cast<int64_t>(t) * H + hc + kq);
+        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        float2 a = __bfloat1622float2(p[0]), b = __bfloat1622float2(p[1]);
+        v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) xs[kq + c][tok] = v[c];
+    }
+    {  // router tile: 64 experts x 32 h fp32, 8 floats per thread
+      const int er = tid >> 2, kq = (tid & 3) * 8;
+      const int e = e0 + er;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+      if (e < E) {
+        const float4* p = reinterpret_cast<const float4*>(wr + static_cast<int64_t>(e) * H + hc + kq);
+        a = __ldg(p);
+        b = __ldg(p + 1);
+      }
+      ws[kq + 0][er] = a.x; ws[kq + 1][er] = a.y; ws[kq + 2][er] = a.z; ws[kq + 3][er] = a.w;
+      ws[kq + 4][er] = b.x; ws[kq + 5][er] = b.y; ws[kq + 6][er] = b.z; ws[kq + 7][er] = b.w;
+    }
+    __syncthreads();
+    float part[2][4] = {};
+#pragma unroll 8
+    for (int kk = 0; kk < kRouterKC; ++kk) {
+      const float a0 = xs[kk][ty * 2], a1 = xs[kk][ty * 2 + 1];
+      const float4 b = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
+      part[0][0] = fmaf(a0, b.x, part[0][0]); part[0][1] = fmaf(a0, b.y, part[0][1]);
+      part[0][2] = fmaf(a0, b.z, part[0][2]); part[0][3] = fmaf(a0, b.w, part[0][3]);
+      part[1][0] = fmaf(a1, b.x, part[1][0]); part[1][1] = fmaf(a1, b.y, part[1][1]);
+      part[1][2] = fmaf(a1, b.z, part[1][2]); part[1][3] = fmaf(a1, b.w, part[1][3]);
+    }
+    // chunk sums enter the running total with compensated (Kahan) addition, so the rounding
+    // error stays at the level of one 32-term chunk instead of growing with H
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float y = part[i][j] - comp[i][j];
+        const float t = acc[i][j] + y;
+        comp[i][j] = (t - acc[i][j]) - y;
+        acc[i][j] = t;
+      }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int t = t0 + ty * 2 + i;
+    if (t >= T) continue;
+    float* out = partial + (static_cast<int64_t>(split) * T + t) * E;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) out[e] = acc[i][j];
+    }
+  }
+}
+
+// One warp per token. Logits of the token live in shared memory (E <= 1024).
+__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ partial,
+                                                          int nsplit, const float* __restrict__ bias,
+                                                          int T, int E, int k, uint32_t flags,
+                                                          int* __restrict__ ids,
+                                                          float* __restrict__ gates) {
+  extern __shared__ float lg_all[];  // [8 warps][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  float* lg = lg_all + warp * E;
+  float mx = -INFINITY;
+  for (int e = lane; e < E; e += 32) {
+    float v = 0.f;
+    for (int s = 0; s < nsplit; ++s) v += partial[(static_cast<int64_t>(s) * T + t) * E + e];
+    if (bias) v += bias[e];
+    lg[e] = v;
+    mx = fmaxf(mx, v);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float sum = 0.f;
+  for (int e = lane; e < E; e += 32) sum += expf(lg[e] - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  __syncwarp();
+
+  uint32_t taken = 0;  // bit i: expert lane + 32*i already chosen
+  float gsel[STRATA_MAX_TOPK > 32 ? 32 : STRATA_MAX_TOPK];
+  int isel[STRATA_MAX_TOPK > 32 ? 32 : STRATA_MAX_TOPK];
+  float gsum = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float best = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int e = lane, i = 0; e < E; e += 32, ++i) {
+      if (taken & (1u << i)) continue;
+      const float v = lg[e];
+      if (v > best || (v == best && e < bi) || bi == 0x7fffffff) { best = v; bi = e; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > best || (ov == best && oi < bi))) {
+        best = ov; bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    const float g = expf(best - mx) / sum;
+    if (j < 32) { gsel[j] = g; isel[j] = bi; }
+    gsum += g;
+  }
+  if (lane == 0) {
+    const bool renorm = (flags & STRATA_RENORM) != 0;
+    for (int j = 0; j < k; ++j) {
+      ids[static_cast<int64_t>(t) * k + j] = isel[j];
+      gates[static_cast<int64_t>(t) * k + j] = renorm ? gsel[j] / gsum : gsel[j];
+    }
+  }
+}
+
+int router_num_splits(int64_t T, int64_t H, int E, int num_sms) {
+  const int64_t tiles = ((E + kRouterBE - 1) / kRouterBE) * ((T + kRouterBT - 1) / kRouterBT);
+  int64_t want = (2 * num_sms + tiles - 1) / tiles;  // ~2 CTAs per SM
+  const int64_t max_split = H / 128;
+  if (want > max_split) want = max_split;
+  if (want > 16) want = 16;
+  if (want < 1) want = 1;
+  return static_cast<int>(want);
+}
+
+cudaError_t launch_router(const void* x, const float* wr, const float* bias, int64_t T, int64_t H,
+                          int E, int k, uint32_t flags, int nsplit, float* partial, int* ids,
+                          float* gates, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  // splits cover whole 128-column groups (a multiple of the 32-wide chunk)
+  const int64_t groups = H / 128;
+  const int64_t gps = (groups + nsplit - 1) / nsplit;
+  const int h_per_split = static_cast<int>(gps * 128);
+  const int used = static_cast<int>((groups + gps - 1) / gps);
+  dim3 grid((E + kRouterBE - 1) / kRouterBE, static_cast<unsigned>((T + kRouterBT - 1) / kRouterBT),
+            used);
+  router_logits_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), wr,
+                                                 static_cast<int>(T), static_cast<int>(H), E,
+                                                 h_per_split, partial);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const size_t smem = static_cast<size_t>(8) * E * sizeof(float);
+  router_topk_kernel<<<static_cast<unsigned>((T + 7) / 8), 256, smem, stream>>>(
+      partial, used, bias, static_cast<int>(T), E, k, flags, ids, gates);
+  return cudaGetLastError();
+}
+
+}  // namespace strata

@@ -1,0 +1,385 @@
+// The C ABI (include/strata.h): host-side argument checks, workspace layout and the launch
+// sequence of one MoE layer. Nothing here allocates device memory; every check runs before the
+// first CUDA call of an entry point.
+#include <cstdint>
+#include <cstring>
+
+#include "kernels.cuh"
+
+namespace strata {
+
+constexpr int64_t kMaxTokens = int64_t(1) << 22;
+constexpr int64_t kMaxDim = int64_t(1) << 16;
+constexpr int kRouterSplitsForSizing = 256;  // SM count bound used to size the router scratch
+constexpr size_t kAlign = 256;
+
+static size_t up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct RouteLayout {
+  size_t hdr, partial, ids, gates, counts, offsets, perm, inv, total;
+};
+static RouteLayout route_layout(int64_t T, int64_t H, int E, int k, int shared, size_t base = 0) {
+  RouteLayout L{};
+  size_t o = base;
+  const int ns = router_num_splits(T, H, E, kRouterSplitsForSizing);
+  const int64_t R = T * k;
+  L.hdr = o; o = up(o + sizeof(WsHeader));
+  L.partial = o; o = up(o + sizeof(float) * ns * T * E);
+  L.ids = o; o = up(o + sizeof(int) * R);
+  L.gates = o; o = up(o + sizeof(float) * R);
+  L.counts = o; o = up(o + sizeof(int) * (E + 1));
+  L.offsets = o; o = up(o + sizeof(int) * (E + 2));
+  L.perm = o; o = up(o + sizeof(int) * (R + shared * T));
+  L.inv = o; o = up(o + sizeof(int) * R);
+  L.total = o;
+  return L;
+}
+
+struct FwdLayout {
+  RouteLayout r;
+  size_t seg_expert, seg_row0, seg_rows, seg_item_gu, seg_item_dn, h, y, total;
+};
+static FwdLayout fwd_layout(const strata_moe_layer* L, int64_t T) {
+  FwdLayout F{};
+  F.r = route_layout(T, L->H, L->E, L->k, L->has_shared);
+  size_t o = F.r.total;
+  const int nseg = L->E + 2;
+  const int64_t rows = T * L->k + (L->has_shared ? T : 0);
+  F.seg_expert = o; o = up(o + sizeof(int) * nseg);
+  F.seg_row0 = o; o = up(o + sizeof(int) * nseg);
+  F.seg_rows = o; o = up(o + sizeof(int) * nseg);
+  F.seg_item_gu = o; o = up(o + sizeof(int) * nseg);
+  F.seg_item_dn = o; o = up(o + sizeof(int) * nseg);
+  F.h = o; o = up(o + sizeof(uint16_t) * rows * L->I);
+  F.y = o; o = up(o + sizeof(float) * rows * L->H);
+  F.total = o;
+  return F;
+}
+
+static strata_status cuda_fail(cudaError_t e) {
+  return e == cudaSuccess ? STRATA_OK : STRATA_ERR_CUDA;
+}
+
+static int device_sms(int* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  return 0;
+}
+
+static strata_status check_layer(const strata_moe_layer* L) {
+  if (!L) return STRATA_ERR_INVALID_ARG;
+  if (L->H <= 0 || L->I <= 0 || L->H > kMaxDim || L->I > kMaxDim) return STRATA_ERR_SHAPE;
+  if (L->H % STRATA_GROUP || L->I % STRATA_GROUP) return STRATA_ERR_SHAPE;
+  if (L->has_shared != 0 && L->has_shared != 1) return STRATA_ERR_INVALID_ARG;
+  if (L->E < 1 || L->E + L->has_shared > STRATA_MAX_EXPERTS) return STRATA_ERR_UNSUPPORTED;
+  if (L->k < 1 || L->k > L->E || L->k > STRATA_MAX_TOPK) return STRATA_ERR_INVALID_ARG;
+  if (L->flags & ~(STRATA_RENORM | STRATA_ADD_RESIDUAL)) return STRATA_ERR_INVALID_ARG;
+  if (!L->w_router || !L->gate_codes || !L->gate_scales || !L->up_codes || !L->up_scales ||
+      !L->down_codes || !L->down_scales)
+    return STRATA_ERR_INVALID_ARG;
+  if (!aligned(L->w_router, 16) || !aligned(L->gate_codes, 16) || !aligned(L->up_codes, 16) ||
+      !aligned(L->down_codes, 16) || !aligned(L->gate_scales, 2) || !aligned(L->up_scales, 2) ||
+      !aligned(L->down_scales, 2) || (L->bias && !aligned(L->bias, 4)))
+    return STRATA_ERR_INVALID_ARG;
+  return STRATA_OK;
+}
+
+struct Taps {
+  int32_t* ids;
+  float* gates;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv;
+};
+
+static strata_status run_forward(const strata_moe_layer* L, const void* x, int64_t T, void* out,
+                                 const Taps* taps, void* ws, size_t ws_bytes, cudaStream_t st,
+                                 void* const* events = nullptr) {
+  auto mark = [&](int i) -> bool {
+    if (!events || !events[i]) return true;
+    return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
+  };
+  strata_status s = check_layer(L);
+  if (s != STRATA_OK) return s;
+  if (T < 0 || T > kMaxTokens) return STRATA_ERR_SHAPE;
+  if (T == 0) return STRATA_OK;
+  if (!x || !out) return STRATA_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16)) return STRATA_ERR_INVALID_ARG;
+  if (x == out) return STRATA_ERR_INVALID_ARG;
+  const FwdLayout F = fwd_layout(L, T);
+  if (!ws || !aligned(ws, kAlign)) return STRATA_ERR_WORKSPACE;
+  if (ws_bytes < F.total) return STRATA_ERR_WORKSPACE;
+
+  int sms = 0;
+  if (device_sms(&sms) != 0) return STRATA_ERR_CUDA;
+  char* base = static_cast<char*>(ws);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(base + F.r.hdr);
+  const int E = L->E, k = L->k, S = L->has_shared;
+  const int64_t R = T * k;
+  int* ids = reinterpret_cast<int*>(base + F.r.ids);
+  float* gates = reinterpret_cast<float*>(base + F.r.gates);
+  int* counts = reinterpret_cast<int*>(base + F.r.counts);
+  int* offsets = reinterpret_cast<int*>(base + F.r.offsets);
+  int* perm = reinterpret_cast<int*>(base + F.r.perm);
+  int* inv = reinterpret_cast<int*>(base + F.r.inv);
+
+  if (!mark(0)) return STRATA_ERR_CUDA;
+  cudaError_t e = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st);
+  if (e != cudaSuccess) return STRATA_ERR_CUDA;
+  const int nsplit = router_num_splits(T, L->H, E, sms);
+  e = launch_router(x, L->w_router, L->bias, T, L->H, E, k, L->flags & STRATA_RENORM, nsplit,
+                    reinterpret_cast<float*>(base + F.r.partial), ids, gates, st);
+  if (e != cudaSuccess || !mark(1)) return STRATA_ERR_CUDA;
+
+  PermuteArgs pa{};
+  pa.ids = ids;
+  pa.T = static_cast<int>(T);
+  pa.k = k;
+  pa.E = E;
+  pa.has_shared = S;
+  pa.counts = counts;
+  pa.offsets = offsets;
+  pa.perm = perm;
+  pa.inv = inv;
+  pa.seg_expert = reinterpret_cast<int*>(base + F.seg_expert);
+  pa.seg_row0 = reinterpret_cast<int*>(base + F.seg_row0);
+  pa.seg_rows = reinterpret_cast<int*>(base + F.seg_rows);
+  pa.seg_item_gu = reinterpret_cast<int*>(base + F.seg_item_gu);
+  pa.seg_item_dn = reinterpret_cast<int*>(base + F.seg_item_dn);
+  pa.tokc = 8;
+  pa.mtiles_gu = static_cast<int>(L->I / 16);
+  pa.mtiles_dn = static_cast<int>(L->H / 16);
+  pa.hdr = hdr;
+  pa.status = &hdr->status;
+  e = launch_permute(pa, st);
+  if (e != cudaSuccess || !mark(2)) return STRATA_ERR_CUDA;
+
+  GemmArgs g{};
+  g.codes0 = L->gate_codes;
+  g.scales0 = static_cast<const __half*>(L->gate_scales);
+  g.codes1 = L->up_codes;
+  g.scales1 = static_cast<const __half*>(L->up_scales);
+  g.act = static_cast<const __nv_bfloat16*>(x);
+  g.perm = perm;
+  g.out = base + F.h;
+  g.K = static_cast<int>(L->H);
+  g.N = static_cast<int>(L->I);
+  g.hdr = hdr;
+  g.seg_expert = pa.seg_expert;
+  g.seg_row0 = pa.seg_row0;
+  g.seg_rows = pa.seg_rows;
+  g.seg_item = pa.seg_item_gu;
+  e = launch_gemm_warp(g, true, sms, st);
+  if (e != cudaSuccess || !mark(3)) return STRATA_ERR_CUDA;
+
+  GemmArgs d = g;
+  d.codes0 = L->down_codes;
+  d.scales0 = static_cast<const __half*>(L->down_scales);
+  d.codes1 = nullptr;
+  d.scales1 = nullptr;
+  d.act = reinterpret_cast<const __nv_bfloat16*>(base + F.h);
+  d.perm = nullptr;
+  d.out = base + F.y;
+  d.K = static_cast<int>(L->I);
+  d.N = static_cast<int>(L->H);
+  d.seg_item = pa.seg_item_dn;
+  e = launch_gemm_warp(d, false, sms, st);
+  if (e != cudaSuccess || !mark(4)) return STRATA_ERR_CUDA;
+
+  e = launch_combine(reinterpret_cast<const float*>(base + F.y), gates, inv, x, T, L->H, k, S, R,
+                     (L->flags & STRATA_ADD_RESIDUAL) ? 1 : 0, out, st);
+  if (e != cudaSuccess || !mark(5)) return STRATA_ERR_CUDA;
+
+  if (taps) {
+    struct { void* dst; const void* src; size_t n; } cp[] = {
+        {taps->ids, ids, sizeof(int) * R},           {taps->gates, gates, sizeof(float) * R},
+        {taps->counts, counts, sizeof(int) * E},     {taps->offsets, offsets, sizeof(int) * (E + 1)},
+        {taps->perm, perm, sizeof(int) * R},         {taps->inv, inv, sizeof(int) * R}};
+    for (auto& c : cp)
+      if (c.dst && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return STRATA_ERR_CUDA;
+  }
+  return STRATA_OK;
+}
+
+}  // namespace strata
+
+using namespace strata;
+
+extern "C" {
+
+const char* strata_status_string(int status) {
+  switch (status) {
+    case STRATA_OK: return "STRATA_OK";
+    case STRATA_ERR_INVALID_ARG: return "STRATA_ERR_INVALID_ARG";
+    case STRATA_ERR_SHAPE: return "STRATA_ERR_SHAPE";
+    case STRATA_ERR_UNSUPPORTED: return "STRATA_ERR_UNSUPPORTED";
+    case STRATA_ERR_WORKSPACE: return "STRATA_ERR_WORKSPACE";
+    case STRATA_ERR_CUDA: return "STRATA_ERR_CUDA";
+    case STRATA_ERR_DEVICE_STATUS: return "STRATA_ERR_DEVICE_STATUS";
+    case STRATA_ERR_TIMEOUT: return "STRATA_ERR_TIMEOUT";
+    default: return "STRATA_ERR_UNKNOWN";
+  }
+}
+
+int strata_version(void) { return 100; }
+
+strata_status strata_quantize_groups(const void* w_fp16, int64_t n, int64_t k, int32_t group_size,
+                                     uint8_t* codes, void* scales_fp16, uint32_t* dev_status,
+                                     strata_stream stream) {
+  if (group_size != STRATA_GROUP) return STRATA_ERR_UNSUPPORTED;
+  if (n < 0 || k <= 0 || k % STRATA_GROUP) return STRATA_ERR_SHAPE;
+  if (n > (int64_t(1) << 40) / k) return STRATA_ERR_SHAPE;
+  if (n == 0) return STRATA_OK;
+  if (!w_fp16 || !codes || !scales_fp16) return STRATA_ERR_INVALID_ARG;
+  if (!aligned(w_fp16, 16) || !aligned(codes, 16) || !aligned(scales_fp16, 2) ||
+      (dev_status && !aligned(dev_status, 4)))
+    return STRATA_ERR_INVALID_ARG;
+  int sms = 0;
+  if (device_sms(&sms) != 0) return STRATA_ERR_CUDA;
+  return cuda_fail(launch_quantize(w_fp16, n, k, codes, scales_fp16, dev_status,
+                                   reinterpret_cast<cudaStream_t>(stream), sms));
+}
+
+size_t strata_route_workspace_size(int64_t T, int32_t E, int32_t k) {
+  if (T < 0 || E < 1 || k < 1) return 0;
+  // the router scratch depends on H only through the split count; size for the largest split
+  return route_layout(T, int64_t(16) * 128, E, k, 0).total;
+}
+
+strata_status strata_route_topk(const void* x_bf16, const float* w_router, const float* bias,
+                                int64_t T, int64_t H, int32_t E, int32_t k, uint32_t flags,
+                                int32_t* ids, float* gates, int32_t* counts, int32_t* offsets,
+                                int32_t* perm, int32_t* inv, void* workspace, size_t ws_bytes,
+                                strata_stream stream) {
+  if (T < 0 || T > kMaxTokens || H <= 0 || H > kMaxDim || H % STRATA_GROUP) return STRATA_ERR_SHAPE;
+  if (E < 1 || E > STRATA_MAX_EXPERTS) return STRATA_ERR_UNSUPPORTED;
+  if (k < 1 || k > E || k > STRATA_MAX_TOPK) return STRATA_ERR_INVALID_ARG;
+  if (flags & ~STRATA_RENORM) return STRATA_ERR_INVALID_ARG;
+  const bool any_group = counts || offsets || perm || inv;
+  const bool all_group = counts && offsets && perm && inv;
+  if (any_group && !all_group) return STRATA_ERR_INVALID_ARG;
+  if (T > 0 && (!x_bf16 || !w_router || !ids || !gates)) return STRATA_ERR_INVALID_ARG;
+  if ((x_bf16 && !aligned(x_bf16, 16)) || (w_router && !aligned(w_router, 16)))
+    return STRATA_ERR_INVALID_ARG;
+  const RouteLayout L = route_layout(T, int64_t(16) * 128, E, k, 0);
+  if (!workspace || !aligned(workspace, kAlign)) return STRATA_ERR_WORKSPACE;
+  if (ws_bytes < L.total) return STRATA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(base + L.hdr);
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return STRATA_ERR_CUDA;
+  if (T == 0) {
+    if (all_group) {
+      if (cudaMemsetAsync(counts, 0, sizeof(int) * E, st) != cudaSuccess ||
+          cudaMemsetAsync(offsets, 0, sizeof(int) * (E + 1), st) != cudaSuccess)
+        return STRATA_ERR_CUDA;
+    }
+    return STRATA_OK;
+  }
+  int sms = 0;
+  if (device_sms(&sms) != 0) return STRATA_ERR_CUDA;
+  int nsplit = router_num_splits(T, H, E, sms);
+  const int cap = router_num_splits(T, int64_t(16) * 128, E, kRouterSplitsForSizing);
+  if (nsplit > cap) nsplit = cap;
+  cudaError_t e = launch_router(x_bf16, w_router, bias, T, H, E, k, flags, nsplit,
+                                reinterpret_cast<float*>(base + L.partial), ids, gates, st);
+  if (e != cudaSuccess) return STRATA_ERR_CUDA;
+  if (!all_group) return STRATA_OK;
+  PermuteArgs pa{};
+  pa.ids = ids;
+  pa.T = static_cast<int>(T);
+  pa.k = k;
+  pa.E = E;
+  pa.has_shared = 0;
+  pa.counts = counts;
+  pa.offsets = offsets;
+  pa.perm = perm;
+  pa.inv = inv;
+  pa.hdr = hdr;
+  pa.status = &hdr->status;
+  return cuda_fail(launch_permute(pa, st));
+}
+
+size_t strata_moe_workspace_size(const strata_moe_layer* layer, int64_t T_max) {
+  if (check_layer(layer) != STRATA_OK || T_max < 0 || T_max > kMaxTokens) return 0;
+  return fwd_layout(layer, T_max).total;
+}
+
+strata_status strata_moe_forward(const strata_moe_layer* layer, const void* x_bf16, int64_t T,
+                                 void* out_bf16, void* workspace, size_t ws_bytes,
+                                 strata_stream stream) {
+  return run_forward(layer, x_bf16, T, out_bf16, nullptr, workspace, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+strata_status strata_moe_forward_ex(const strata_moe_layer* layer, const void* x_bf16, int64_t T,
+                                    void* out_bf16, int32_t* ids, float* gates, int32_t* counts,
+                                    int32_t* offsets, int32_t* perm, int32_t* inv,
+                                    void* workspace, size_t ws_bytes, strata_stream stream) {
+  Taps t{ids, gates, counts, offsets, perm, inv};
+  return run_forward(layer, x_bf16, T, out_bf16, &t, workspace, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+strata_status strata_moe_forward_profiled(const strata_moe_layer* layer, const void* x_bf16,
+                                          int64_t T, void* out_bf16, void* workspace,
+                                          size_t ws_bytes, strata_stream stream,
+                                          void* const* events, int32_t n_events) {
+  if (!events || n_events != STRATA_PROFILE_EVENTS) return STRATA_ERR_INVALID_ARG;
+  return run_forward(layer, x_bf16, T, out_bf16, nullptr, workspace, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream), events);
+}
+
+size_t strata_moe_host_staging_size(const strata_moe_layer* layer, int64_t T_max) {
+  if (check_layer(layer) != STRATA_OK || T_max < 0 || T_max > kMaxTokens) return 0;
+  return 2 * up(sizeof(uint16_t) * T_max * layer->H);
+}
+
+strata_status strata_moe_forward_host(const strata_moe_layer* layer, const void* x_host,
+                                      int64_t T, void* out_host, void* workspace, size_t ws_bytes,
+                                      strata_stream stream) {
+  strata_status s = check_layer(layer);
+  if (s != STRATA_OK) return s;
+  if (T < 0 || T > kMaxTokens) return STRATA_ERR_SHAPE;
+  if (T == 0) return STRATA_OK;
+  if (!x_host || !out_host) return STRATA_ERR_INVALID_ARG;
+  const size_t need = strata_moe_workspace_size(layer, T);
+  const size_t stage = strata_moe_host_staging_size(layer, T);
+  if (!workspace || !aligned(workspace, kAlign)) return STRATA_ERR_WORKSPACE;
+  if (ws_bytes < need + stage) return STRATA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(workspace);
+  void* xd = base + need;
+  void* od = base + need + stage / 2;
+  const size_t bytes = sizeof(uint16_t) * T * layer->H;
+  if (cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return STRATA_ERR_CUDA;
+  s = run_forward(layer, xd, T, od, nullptr, workspace, need, st);
+  if (s != STRATA_OK) return s;
+  if (cudaMemcpyAsync(out_host, od, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return STRATA_ERR_CUDA;
+  return cuda_fail(cudaStreamSynchronize(st));
+}
+
+strata_status strata_read_status(uint32_t* dev_status, strata_stream stream, uint32_t* status_out) {
+  if (!dev_status || !status_out) return STRATA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, dev_status, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return STRATA_ERR_CUDA;
+  if (cudaMemsetAsync(dev_status, 0, sizeof(uint32_t), st) != cudaSuccess) return STRATA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return STRATA_ERR_CUDA;
+  *status_out = v;
+  return v ? STRATA_ERR_DEVICE_STATUS : STRATA_OK;
+}
+
+strata_status strata_workspace_status(void* workspace, strata_stream stream, uint32_t* status_out) {
+  if (!workspace || !aligned(workspace, kAlign)) return STRATA_ERR_WORKSPACE;
+  return strata_read_status(&reinterpret_cast<WsHeader*>(workspace)->status, stream, status_out);
+}
+
+}  // extern "C"

@@ -1,0 +1,142 @@
+"""The whole layer (strata_moe_forward) vs the oracle on decode / small workloads.
+
+Output tolerance: relative L2 <= 5e-3 and max-abs <= 3e-2 over the compared
+tokens (bf16 activations, fp32 accumulation); tokens whose top-k boundary is a
+near tie (gap <= 1e-6) may route differently and are then excluded, counted.
+Expert form: Gate/Up + Down ("GLM-5.3-Flash on one 4090",
+haowenji.com/articles/x-2109226022155796480, §01), SiLU gate, weighted combine
+plus a shared expert with gate 1.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import (OracleExperts, bf16_tensor, build_gpu_layer, compare_output, compare_routing,
+                     run_forward)
+from workloads import CONFIGS, Workload, gen
+
+pytestmark = pytest.mark.gpu
+
+_CACHE = {}
+
+
+def layer_for(key, layer=0, router_kind=None, flags=0):
+    ck = (key, layer, router_kind, flags)
+    if ck not in _CACHE:
+        _CACHE.clear()
+        wl = CONFIGS[key]
+        _CACHE[ck] = (wl,) + build_gpu_layer(wl, layer, router_kind, flags)
+    return _CACHE[ck]
+
+
+def check_layer(wl, L, wr, b, x, layer=0, residual=False, renorm=False, rows=None,
+                overrides=None):
+    g = run_forward(L, x)
+    tokens = np.arange(x.shape[0]) if rows is None else np.asarray(rows)
+    ref = oracle.moe_forward(x, wr, b, wl.k, OracleExperts(wl, layer, overrides), wl.E, wl.shared,
+                             renorm=renorm, residual=residual, tokens=tokens)
+    full_ref = oracle.route_topk(x, wr, b, wl.k, renorm=renorm)
+    diff, _ = compare_routing(g, full_ref, wl.E)
+    keep = ~diff[tokens]
+    compare_output(g["out"][tokens][keep], ref["out"][keep])
+    return int(diff.sum())
+
+
+def test_c1_single_layer_64_tokens():
+    wl, L, wr, b = layer_for("c1")
+    check_layer(wl, L, wr, b, gen.activations(64, wl.H, wl.seed))
+
+
+@pytest.mark.parametrize("T", [1, 7, 63, 200])
+def test_c1_ragged_batches(T):
+    wl, L, wr, b = layer_for("c1")
+    check_layer(wl, L, wr, b, gen.activations(T, wl.H, wl.seed, name=f"ragged{T}"))
+
+
+@pytest.mark.parametrize("T", [1, 4, 8, 16])
+def test_c2_decode_batches(T):
+    wl, L, wr, b = layer_for("c2")
+    check_layer(wl, L, wr, b, gen.activations(T, wl.H, wl.seed, name=f"decode{T}"))
+
+
+def test_c4_layer_decode_32():
+    wl, L, wr, b = layer_for("c4", layer=3)
+    check_layer(wl, L, wr, b, gen.activations(32, wl.H, wl.seed, name="c4l3"), layer=3)
+
+
+def test_residual_and_renorm_flags():
+    import int4_grouped_expert_gb300 as st
+    wl, L, wr, b = layer_for("c1", flags=st.STRATA_ADD_RESIDUAL | st.STRATA_RENORM)
+    check_layer(wl, L, wr, b, gen.activations(40, wl.H, wl.seed, name="flags"), residual=True,
+                renorm=True)
+
+
+SMALL = Workload("t", "edge", H=256, I=384, E=20, k=20, shared=1, batches=(5,), router="uniform")
+
+
+def test_k_equals_e_with_shared_and_odd_expert_count():
+    wl = SMALL
+    L, wr, b = build_gpu_layer(wl)
+    check_layer(wl, L, wr, b, gen.activations(5, wl.H, 3))
+
+
+def test_dense_equivalence_on_gpu():
+    """k = E, zero router: out = mean of the experts' FFNs + shared (checked via the oracle)."""
+    wl = SMALL
+    wr = np.zeros((wl.E, wl.H), np.float32)
+    L, wr, b = build_gpu_layer(wl, w_router=wr)
+    check_layer(wl, L, wr, b, gen.activations(9, wl.H, 4))
+
+
+def test_all_tokens_one_expert():
+    wl = Workload("t1", "one", H=512, I=256, E=12, k=1, shared=0, batches=(70,), router="uniform")
+    bias = np.zeros(wl.E, np.float32)
+    bias[5] = 40.0
+    L, wr, b = build_gpu_layer(wl, bias=bias)
+    x = gen.activations(70, wl.H, 5)
+    g = run_forward(L, x)
+    assert (g["ids"] == 5).all() and g["counts"][5] == 70
+    check_layer(wl, L, wr, b, x)
+
+
+def test_host_entry_point_matches_device_entry_point():
+    import torch
+    import int4_grouped_expert_gb300 as st
+    wl, L, wr, b = layer_for("c1")
+    x = gen.activations(33, wl.H, 9)
+    g = run_forward(L, x, taps=False)
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    s = L.struct()
+    need = st.strata_moe_workspace_size(s, 33) + st.strata_moe_host_staging_size(s, 33)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    st.check(st.strata_moe_forward_host(s, xh, 33, oh, ws, need), "forward_host")
+    np.testing.assert_array_equal(oh.numpy().view(np.uint16), g["out"])
+
+
+def test_workspace_reuse_and_determinism():
+    import torch
+    wl, L, wr, b = layer_for("c1")
+    x = gen.activations(64, wl.H, 11)
+    ws = torch.full((L.workspace_size(64),), 0x5A, dtype=torch.uint8, device="cuda")
+    a = run_forward(L, x, workspace=ws)
+    c = run_forward(L, gen.activations(3, wl.H, 12), workspace=ws)
+    d = run_forward(L, x, workspace=ws)
+    np.testing.assert_array_equal(a["out"], d["out"])
+    assert c["out"].shape == (3, wl.H)
+
+
+def test_forward_argument_errors():
+    import torch
+    import int4_grouped_expert_gb300 as st
+    wl, L, wr, b = layer_for("c1")
+    s = L.struct()
+    x = bf16_tensor(gen.activations(4, wl.H, 0))
+    out = torch.empty_like(x)
+    need = L.workspace_size(4)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    assert st.strata_moe_forward(s, x, 4, out, ws, need - 1) == 4          # WORKSPACE
+    assert st.strata_moe_forward(s, x, 4, x, ws, need) == 1                # out aliases x
+    assert st.strata_moe_forward(s, x, 0, out, ws, need) == 0              # empty batch
+    s.k = 17
+    assert st.strata_moe_forward(s, x, 4, out, ws, need) == 1              # k > E
