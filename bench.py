@@ -209,6 +209,10 @@ def time_steps(layers, xs_dev, T, steps, warmup, stream, ws, ws_bytes, out, prof
         stage_ev = None
         if profiled:
             stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+            for evs in stage_ev:          # torch creates the CUDA event on its first record
+                for ev in evs:
+                    ev.record(stream)
+            torch.cuda.synchronize()
         start = torch.cuda.Event(enable_timing=True)
         stop = torch.cuda.Event(enable_timing=True)
         start.record(stream)
