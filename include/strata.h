@@ -61,6 +61,10 @@ typedef enum {
 #define STRATA_RENORM 0x1u       /* renormalise the k gates of a token to sum to 1 (off by default:
                                     the pages never renormalise) */
 #define STRATA_ADD_RESIDUAL 0x2u /* moe_forward only: out = bf16(x + MoE(x)), one rounding */
+/* Kernel-path selection of moe_forward (results agree within the layer tolerance; default: the
+   tensor-core path from 128 tokens up, the warp path below). For tests and tuning. */
+#define STRATA_FORCE_WARP_PATH 0x100u /* mma.sync warp GEMMs, B from registers */
+#define STRATA_FORCE_TC_PATH 0x200u   /* tcgen05 / TMEM GEMMs fed by TMA */
 
 /* Bits of the device status word. */
 #define STRATA_DEV_NONFINITE 0x1u /* a quantized group held inf/nan (its scale is written as NaN,
@@ -135,7 +139,7 @@ typedef struct {
   int32_t E;             /* routed experts, 1..1024 */
   int32_t k;             /* experts per token, 1..min(E, 32) */
   int32_t has_shared;    /* 0 or 1: expert E is always on, gate 1 */
-  uint32_t flags;        /* STRATA_RENORM | STRATA_ADD_RESIDUAL */
+  uint32_t flags;        /* STRATA_RENORM | STRATA_ADD_RESIDUAL | STRATA_FORCE_*_PATH */
   const float* w_router; /* [E, H] fp32 */
   const float* bias;     /* [E] fp32 or NULL */
   const uint8_t* gate_codes; const void* gate_scales; /* [E+S, I, H/2] u8, [E+S, I, H/128] fp16 */

@@ -15,12 +15,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       int residual, __nv_bfloat16* __restrict__ out) {
   const int t = blockIdx.x;
   const int64_t H4 = H / 4;
-  for (int64_t c = threadIdx.x; c < H4; c += blockDim.x) {
+  for (int64_t c = blockIdx.y * blockDim.x + threadIdx.x; c < H4; c += gridDim.y * blockDim.x) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int64_t tk = static_cast<int64_t>(t) * k;
+    // rows and gates first, then all row loads: the k loads are independent
+#pragma unroll 8
     for (int j = 0; j < k; ++j) {
-      const float g = gates[static_cast<int64_t>(t) * k + j];
-      const int row = inv[static_cast<int64_t>(t) * k + j];
-      const float4 v = reinterpret_cast<const float4*>(y + static_cast<int64_t>(row) * H)[c];
+      const float g = gates[tk + j];
+      const int row = inv[tk + j];
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(y + static_cast<int64_t>(row) * H) + c);
       acc.x = fmaf(g, v.x, acc.x); acc.y = fmaf(g, v.y, acc.y);
       acc.z = fmaf(g, v.z, acc.z); acc.w = fmaf(g, v.w, acc.w);
     }
@@ -46,7 +49,9 @@ cudaError_t launch_combine(const float* y, const float* gates, const int* inv, c
                            int64_t T, int64_t H, int k, int has_shared, int64_t R, int residual,
                            void* out, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<static_cast<unsigned>(T), 256, 0, stream>>>(
+  // one float4 of one token per thread: T x ceil(H / 1024) CTAs
+  dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((H / 4 + 255) / 256));
+  combine_kernel<<<grid, 256, 0, stream>>>(
       y, gates, inv, static_cast<const __nv_bfloat16*>(x), static_cast<int>(T),
       static_cast<int>(H), k, has_shared, static_cast<int>(R), residual,
       static_cast<__nv_bfloat16*>(out));

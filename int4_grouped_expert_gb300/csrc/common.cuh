@@ -15,12 +15,14 @@ constexpr int kGroup = STRATA_GROUP;  // weights per scale group
 // Workspace header (first 256 bytes of every route/forward workspace).
 struct WsHeader {
   uint32_t status;      // STRATA_DEV_* bits
-  int32_t nseg;         // active expert segments (routed experts with rows, then the shared one)
+  int32_t nseg;         // active expert segments (the shared one first, then routed experts with rows)
   int32_t n_items_gu;   // gate/up work items
   int32_t n_items_dn;   // down work items
-  int32_t n_tiles_gu;   // (tcgen05 path) gate/up tiles
-  int32_t n_tiles_dn;   // (tcgen05 path) down tiles
-  int32_t pad[58];
+  int32_t next_gu;      // dynamic scheduler: next gate/up item
+  int32_t next_dn;      // dynamic scheduler: next down item
+  uint32_t route_done;  // CTAs of the fused router that finished their logits
+  int32_t n_chunks;     // warp path: 8-row chunks in the chunk list
+  int32_t pad[56];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

@@ -1,0 +1,389 @@
+// K4 (tensor-core path): W4A16 grouped GEMM on tcgen05 for segments with many rows (prefill),
+// where the expert FFN is a dense contraction. One persistent launch covers every expert's group
+// ("Strata" 3090 tuning, xdnf.cn/news/329730, §3.2: one grouped GEMM for all experts); the int4
+// weights are dequantized on chip ("Strata" MoE tuning notes, lpnh.cn/news/2730718, §2.1 format:
+// 128 codes share one fp16 scale).
+//
+// Tile = (segment, 128 weight rows, up to 256 token rows), contraction in 64-wide stages.
+//   warp 0       TMA producer: the stage's token rows (bf16, 128-byte swizzle) -> shared memory
+//   warp 1       MMA issuer: one thread issues tcgen05.mma (M=128, N=rows, K=16) into TMEM
+//   warp 2       owns the TMEM allocation
+//   warps 4..11  dequant producers: int4 codes (global) -> bf16(q*s) written in the same swizzled
+//                K-major layout (the A operand), then the epilogue: TMEM -> registers -> global
+// D[weight row][token] accumulates in TMEM (gate at column 0, up at column 256). Gate/up writes
+// h = silu(gate) * up as bf16; down writes y in fp32 for the combine.
+//
+// Contraction order: inside every 8-wide chunk the K order is (0,4,1,5,2,6,3,7). That is the
+// order in which one LOP3 per pair unpacks the codes, so the activations are stored in it too (by
+// the gather kernel for x, by the gate/up epilogue for h); a dot product is order-independent.
+//
+// Scale: w = bf16(q * s) computed as fma(q, s_hi, q * s_lo) in bf16 with s = s_hi + s_lo, so the
+// product is rounded once (to within 2^-17 relative).
+//
+// Every mbarrier wait is bounded in time; on time-out the kernel sets STRATA_DEV_TIMEOUT, every
+// role leaves its loop, in-flight copies and MMAs are drained (bounded) and TMEM is freed.
+#include <cudaTypedefs.h>
+
+#include "kernels.cuh"
+#include "tc_ptx.cuh"
+
+namespace strata {
+
+constexpr int kTcBM = 128;       // weight rows per tile (MMA M)
+constexpr int kTcBK = 64;        // contraction per stage: one 128-byte swizzle row of bf16
+constexpr int kTcNMax = 256;     // token rows per tile (MMA N)
+constexpr int kTcThreads = 384;  // 12 warps
+
+template <bool kGateUp>
+struct TcCfg {
+  static constexpr int STAGES = kGateUp ? 3 : 4;
+  static constexpr int A_BYTES = kTcBM * kTcBK * 2;    // 16 KB per weight matrix
+  static constexpr int B_BYTES = kTcNMax * kTcBK * 2;  // 32 KB
+  static constexpr int NMAT = kGateUp ? 2 : 1;
+  static constexpr int STAGE_BYTES = NMAT * A_BYTES + B_BYTES;
+  static constexpr uint32_t TMEM_COLS = kGateUp ? 512 : 256;
+  static constexpr size_t SMEM = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + 256;
+};
+
+struct TcTile {
+  int e, mt, row0, nvalid, nmma;
+};
+
+__device__ __forceinline__ bool tc_decode(const TcArgs& a, int item, int nseg, int mtiles,
+                                          TcTile& t) {
+  int lo = 0, hi = nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.seg_item[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  const int local = item - a.seg_item[lo];
+  const int chunk = local / mtiles;
+  t.mt = local - chunk * mtiles;
+  t.e = a.seg_expert[lo];
+  t.row0 = a.seg_row0[lo] + chunk * kTcNMax;
+  t.nvalid = min(kTcNMax, a.seg_rows[lo] - chunk * kTcNMax);
+  t.nmma = (t.nvalid + 15) & ~15;
+  return true;
+}
+
+// bf16x2 {q_i, q_{i+4}} of an 8-code word (two's complement nibbles), exact
+__device__ __forceinline__ uint32_t codes_pair_bf16(uint32_t w, int i) {
+  const uint32_t v = w >> (4 * i);
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(v), "n"(0x000F000F), "n"(0x43084308));
+  __nv_bfloat162 r = *reinterpret_cast<__nv_bfloat162*>(&d);
+  r = __hsub2(r, __floats2bfloat162_rn(136.0f, 136.0f));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t scale_pair(uint32_t q, __nv_bfloat162 hi, __nv_bfloat162 lo) {
+  const __nv_bfloat162 qq = *reinterpret_cast<__nv_bfloat162*>(&q);
+  const __nv_bfloat162 r = __hfma2(qq, hi, __hmul2(qq, lo));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Position of natural index i (0..7) inside a chunk stored in (0,4,1,5,2,6,3,7) order.
+__device__ __forceinline__ int pair_pos(int i) { return i < 4 ? 2 * i : 2 * (i - 4) + 1; }
+
+template <bool kGateUp>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, TcArgs a) {
+  using C = TcCfg<kGateUp>;
+  constexpr int ST = C::STAGES;
+  extern __shared__ uint8_t tc_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ST * C::STAGE_BYTES);
+  uint64_t* full_a = bars;
+  uint64_t* full_b = bars + ST;
+  uint64_t* empty = bars + 2 * ST;
+  uint64_t* acc_full = bars + 3 * ST;
+  uint64_t* acc_empty = bars + 3 * ST + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * ST + 2);
+  __shared__ int abort_flag_s;
+  volatile int* abort_flag = &abort_flag_s;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ST; ++s) {
+      tc::mbar_init(full_a + s, 8);
+      tc::mbar_init(full_b + s, 1);
+      tc::mbar_init(empty + s, 1);
+    }
+    tc::mbar_init(acc_full, 1);
+    tc::mbar_init(acc_empty, 8);
+    tc::fence_barrier_init();
+    abort_flag_s = 0;
+  }
+  if (warp == 2) {
+    tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) tc::prefetch_tmap(&tmap_b);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int n_items = kGateUp ? a.hdr->n_items_gu : a.hdr->n_items_dn;
+  const int nseg = a.hdr->nseg;
+  const int nk = a.K / kTcBK;
+  const int mtiles = a.Nw / kTcBM;
+  auto A_of = [&](int s, int m) { return smem + s * C::STAGE_BYTES + m * C::A_BYTES; };
+  auto B_of = [&](int s) { return smem + s * C::STAGE_BYTES + C::NMAT * C::A_BYTES; };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        TcTile t;
+        tc_decode(a, item, nseg, mtiles, t);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % ST;
+          const uint32_t ph = (it / ST) & 1;
+          if (!tc::mbar_wait(empty + s, ph ^ 1, abort_flag, a.status)) { ok = false; break; }
+          tc::mbar_arrive_expect_tx(full_b + s, C::B_BYTES);
+          tc::tma_load_2d(B_of(s), &tmap_b, kb * kTcBK, t.row0, full_b + s);
+        }
+      }
+      if (!ok)  // drain the copies that may still be in flight
+        for (int j = (it > ST ? it - ST : 0); j < it; ++j)
+          tc::mbar_wait_drain(full_b + (j % ST), (j / ST) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int it = 0, tcount = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++tcount) {
+        TcTile t;
+        tc_decode(a, item, nseg, mtiles, t);
+        const uint32_t idesc = tc::idesc_bf16(kTcBM, t.nmma);
+        if (tcount > 0 && !tc::mbar_wait(acc_empty, (tcount - 1) & 1, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % ST;
+          const uint32_t ph = (it / ST) & 1;
+          if (!tc::mbar_wait(full_a + s, ph, abort_flag, a.status) ||
+              !tc::mbar_wait(full_b + s, ph, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint64_t da0 = tc::sw128_desc(tc::smem_u32(A_of(s, 0)));
+          const uint64_t da1 = kGateUp ? tc::sw128_desc(tc::smem_u32(A_of(s, 1))) : 0;
+          const uint64_t db = tc::sw128_desc(tc::smem_u32(B_of(s)));
+#pragma unroll
+          for (int kk = 0; kk < kTcBK / 16; ++kk) {
+            const uint32_t acc = (kb | kk) ? 1u : 0u;
+            // +32 bytes per 16-wide K step inside the swizzle row (address field is in 16 B)
+            tc::mma_bf16_ss(tmem, da0 + 2 * kk, db + 2 * kk, idesc, acc);
+            if (kGateUp) tc::mma_bf16_ss(tmem + 256, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+          }
+          tc::mma_commit(empty + s);
+        }
+        if (!ok) break;
+        tc::mma_commit(acc_full);
+      }
+      if (!ok) {  // drain every MMA issued so far before TMEM is released
+        tc::mma_commit(acc_empty);
+        tc::mbar_wait_drain(acc_empty, tcount & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ dequant + epilogue
+    const int pt = threadIdx.x - 128;  // 0..255
+    const int mat = kGateUp ? (pt >> 7) : 0;
+    const int half = kGateUp ? 0 : (pt >> 7);
+    const int r = pt & 127;
+    const uint8_t* codes = mat ? a.codes1 : a.codes0;
+    const __half* scales = mat ? a.scales1 : a.scales0;
+    const int64_t row_bytes = a.K / 2;
+    const int64_t srow = a.K / kGroup;
+    const int q4 = warp & 3;       // TMEM lane quarter of this warp
+    const int wg = (warp - 4) >> 2;  // epilogue: warpgroup 0 / 1 take alternating column blocks
+    int it = 0, tcount = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++tcount) {
+      TcTile t;
+      tc_decode(a, item, nseg, mtiles, t);
+      const int64_t wrow = static_cast<int64_t>(t.e) * a.Nw + t.mt * kTcBM + r;
+      const uint8_t* cp = codes + wrow * row_bytes + half * 16;
+      const __half* sp = scales + wrow * srow;
+      const uint32_t soff = (r >> 3) * 1024 + (r & 7) * 128;
+      // codes of the next stages stay in flight in registers (3 deep)
+      uint4 c0a, c0b, c1a, c1b, c2a, c2b;
+      auto ld = [&](int kb, uint4& x0, uint4& x1) {
+        if (kb < nk) {
+          x0 = __ldg(reinterpret_cast<const uint4*>(cp + static_cast<int64_t>(kb) * 32));
+          if (kGateUp) x1 = __ldg(reinterpret_cast<const uint4*>(cp + static_cast<int64_t>(kb) * 32 + 16));
+        }
+      };
+      ld(0, c0a, c0b);
+      ld(1, c1a, c1b);
+      ld(2, c2a, c2b);
+      __nv_bfloat162 s_hi, s_lo;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = it % ST;
+        const uint32_t ph = (it / ST) & 1;
+        if ((kb & 1) == 0) {
+          const float sf = __half2float(sp[kb >> 1]);
+          const __nv_bfloat16 h = __float2bfloat16_rn(sf);
+          const __nv_bfloat16 l = __float2bfloat16_rn(sf - __bfloat162float(h));
+          s_hi = __halves2bfloat162(h, h);
+          s_lo = __halves2bfloat162(l, l);
+        }
+        const uint4 x0 = c0a, x1 = c0b;
+        c0a = c1a; c0b = c1b; c1a = c2a; c1b = c2b;
+        ld(kb + 3, c2a, c2b);
+        if (!tc::mbar_wait(empty + s, ph ^ 1, abort_flag, a.status)) { ok = false; break; }
+        uint8_t* dst = A_of(s, mat) + soff;
+        const uint32_t wds[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+        for (int j = 0; j < (kGateUp ? 8 : 4); ++j) {
+          const uint32_t w = wds[j];
+          uint4 o;
+          o.x = scale_pair(codes_pair_bf16(w, 0), s_hi, s_lo);
+          o.y = scale_pair(codes_pair_bf16(w, 1), s_hi, s_lo);
+          o.z = scale_pair(codes_pair_bf16(w, 2), s_hi, s_lo);
+          o.w = scale_pair(codes_pair_bf16(w, 3), s_hi, s_lo);
+          const int chunk = kGateUp ? j : (half * 4 + j);
+          *reinterpret_cast<uint4*>(dst + ((chunk ^ (r & 7)) << 4)) = o;
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(full_a + s);
+      }
+      if (!ok) break;
+      // epilogue
+      if (!tc::mbar_wait(acc_full, tcount & 1, abort_flag, a.status)) { ok = false; break; }
+      tc::tc_fence_after();
+      const int irow = t.mt * kTcBM + q4 * 32 + lane;  // weight row = output column
+      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+      for (int c = wg * 32; c < t.nmma; c += 64) {
+        uint32_t g[32];
+        tc::tmem_ld32(lane_addr + c, g);
+        if (kGateUp) {
+          uint32_t u[32];
+          tc::tmem_ld32(lane_addr + 256 + c, u);
+          tc::tmem_ld_wait();
+          __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.out);
+          const int col = (irow & ~7) | pair_pos(irow & 7);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int n = c + j;
+            if (n < t.nvalid) {
+              const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
+              h[static_cast<int64_t>(t.row0 + n) * a.Nw + col] = __float2bfloat16_rn(silu_f(gv) * uv);
+            }
+          }
+        } else {
+          tc::tmem_ld_wait();
+          float* y = static_cast<float*>(a.out);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int n = c + j;
+            if (n < t.nvalid) y[static_cast<int64_t>(t.row0 + n) * a.Nw + irow] = __uint_as_float(g[j]);
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(acc_empty);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ----------------------------------------------------------------------------- gather
+
+// xp[r] = x[perm[r]] with every 8-wide chunk stored in (0,4,1,5,2,6,3,7) order.
+__global__ void __launch_bounds__(128) gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
+                                                          const int* __restrict__ perm, int H,
+                                                          __nv_bfloat16* __restrict__ xp) {
+  const int row = blockIdx.x;
+  const int tok = perm[row];
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tok) * H);
+  uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<int64_t>(row) * H);
+  for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
+    const uint4 v = __ldg(src + c);
+    uint4 o;
+    o.x = prmt(v.x, v.z, 0x5410);  // x0, x4
+    o.y = prmt(v.x, v.z, 0x7632);  // x1, x5
+    o.z = prmt(v.y, v.w, 0x5410);  // x2, x6
+    o.w = prmt(v.y, v.w, 0x7632);  // x3, x7
+    dst[c] = o;
+  }
+}
+
+cudaError_t launch_gather_rows(const void* x, const int* perm, int64_t rows, int64_t H, void* xp,
+                               cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  gather_rows_kernel<<<static_cast<unsigned>(rows), 128, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(x), perm, static_cast<int>(H),
+      static_cast<__nv_bfloat16*>(xp));
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- host
+
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Row-major bf16 [rows, cols]: boxes of 256 rows x 64 columns, 128-byte swizzle, zero fill.
+static bool make_row_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {kTcBK, kTcNMax};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kGateUp>
+cudaError_t launch_gemm_tc_t(const TcArgs& a, const void* b_rows, int64_t rows, int num_sms,
+                             cudaStream_t stream) {
+  using C = TcCfg<kGateUp>;
+  CUtensorMap map;
+  if (!make_row_tmap(&map, b_rows, rows, a.K)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<kGateUp>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(C::SMEM));
+  if (e != cudaSuccess) return e;
+  grouped_gemm_tc_kernel<kGateUp><<<num_sms, kTcThreads, C::SMEM, stream>>>(map, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tc(const TcArgs& a, bool gate_up, const void* b_rows, int64_t rows,
+                           int num_sms, cudaStream_t stream) {
+  return gate_up ? launch_gemm_tc_t<true>(a, b_rows, rows, num_sms, stream)
+                 : launch_gemm_tc_t<false>(a, b_rows, rows, num_sms, stream);
+}
+
+}  // namespace strata

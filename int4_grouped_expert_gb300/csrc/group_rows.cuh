@@ -1,0 +1,194 @@
+// Stable counting sort of the routed rows by expert, shared by the stand-alone grouping kernel and
+// the last CTA of the fused decode router. Tokens routed to the same expert become one contiguous
+// segment of the grouped GEMM ("Strata" 3090 tuning, xdnf.cn/news/329730, §3.2).
+//
+// Rows r = t*k + j of the flattened [T, k] id array are ordered by (expert, token): each warp owns a
+// contiguous range of r, counts it into its own histogram row (equal ids inside a 32-row step are
+// grouped with __match_any_sync), the histograms are scanned per expert in warp order, and the same
+// walk then hands out positions. The result does not depend on thread timing.
+#pragma once
+
+#include "kernels.cuh"
+
+namespace strata {
+
+// Exclusive scan of one int per thread over the whole block (blockDim.x = 32 * NW);
+// scratch holds NW + 1 ints. Every thread of the block must call it.
+template <int NW>
+__device__ __forceinline__ int block_scan_excl(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) scratch[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < NW ? scratch[lane] : 0;
+    int winc = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, winc, o);
+      if (lane >= o) winc += n;
+    }
+    if (lane < NW) scratch[lane] = winc - w;
+    if (lane == 31) scratch[NW] = winc;
+  }
+  __syncthreads();
+  const int res = scratch[warp] + inc - v;
+  *total = scratch[NW];
+  __syncthreads();
+  return res;
+}
+
+// Group rows. hist: NW*E ints of shared memory; scratch: NW+1 ints of shared memory.
+// Per-thread expert ownership: thread i owns experts [i*EPT, i*EPT + EPT) with EPT = ceil(E / NT).
+template <int NW>
+__device__ void group_rows(const PermuteArgs& a, int* hist, int* scratch) {
+  constexpr int NT = NW * 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = a.E;
+  const int R = a.T * a.k;
+  for (int i = tid; i < NW * E; i += NT) hist[i] = 0;
+  __syncthreads();
+
+  const int per_warp = (R + NW - 1) / NW;
+  const int rbeg = min(R, warp * per_warp), rend = min(R, rbeg + per_warp);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = rbeg; base < rend; base += 32) {
+    const int r = base + lane;
+    const unsigned active = __ballot_sync(0xffffffffu, r < rend);
+    if (r < rend) {
+      int e = a.ids[r];
+      if (e < 0 || e >= E) {
+        set_status(a.status, STRATA_DEV_BAD_ID);
+        e = -1;
+      }
+      const unsigned m = __match_any_sync(active, e);
+      if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
+      __syncwarp(active);
+    }
+  }
+  __syncthreads();
+
+  const int ept = (E + NT - 1) / NT;
+  const int e0 = min(E, tid * ept), e1 = min(E, e0 + ept);
+  int my = 0;
+  for (int e = e0; e < e1; ++e)
+    for (int w = 0; w < NW; ++w) my += hist[w * E + e];
+  int total;
+  int run = block_scan_excl<NW>(my, scratch, &total);
+  for (int e = e0; e < e1; ++e) {
+    int c = 0;
+    for (int w = 0; w < NW; ++w) {
+      const int h = hist[w * E + e];
+      hist[w * E + e] = run + c;
+      c += h;
+    }
+    a.counts[e] = c;
+    a.offsets[e] = run;
+    run += c;
+  }
+  if (tid == 0) a.offsets[E] = total;
+  __syncthreads();
+
+  for (int base = rbeg; base < rend; base += 32) {
+    const int r = base + lane;
+    const unsigned active = __ballot_sync(0xffffffffu, r < rend);
+    if (r < rend) {
+      int e = a.ids[r];
+      if (e < 0 || e >= E) e = -1;
+      const unsigned m = __match_any_sync(active, e);
+      if (e >= 0) {
+        const int pos = hist[warp * E + e] + __popc(m & lt_mask);
+        a.perm[pos] = r / a.k;
+        a.inv[r] = pos;
+      }
+      __syncwarp(active);
+      if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
+      __syncwarp(active);
+    }
+  }
+  if (a.has_shared)
+    for (int t = tid; t < a.T; t += NT) a.perm[R + t] = t;
+  __syncthreads();
+
+  if (a.seg_expert == nullptr) return;
+  // Active segments: the shared expert first (the largest), then routed experts with rows, by id.
+  const int sh = (a.has_shared && a.T > 0) ? 1 : 0;
+  int nz = 0;
+  for (int e = e0; e < e1; ++e) nz += (a.counts[e] > 0);
+  int nseg_routed;
+  int sidx = block_scan_excl<NW>(nz, scratch, &nseg_routed) + sh;
+  for (int e = e0; e < e1; ++e) {
+    const int c = a.counts[e];
+    if (c > 0) {
+      a.seg_expert[sidx] = e;
+      a.seg_row0[sidx] = a.offsets[e];
+      a.seg_rows[sidx] = c;
+      ++sidx;
+    }
+  }
+  const int nseg = nseg_routed + sh;
+  if (sh && tid == 0) {
+    a.seg_expert[0] = E;
+    a.seg_row0[0] = R;
+    a.seg_rows[0] = a.T;
+  }
+  __syncthreads();
+  const int spt = (nseg + NT - 1) / NT;
+  const int s0 = min(nseg, tid * spt), s1 = min(nseg, s0 + spt);
+  if (a.chunk_list) {
+    // Warp path: a flat list of tokc-row chunks; items = chunk x row tile (x contraction split).
+    int my = 0;
+    for (int s = s0; s < s1; ++s) my += (a.seg_rows[s] + a.tokc - 1) / a.tokc;
+    int nchunks;
+    int off = block_scan_excl<NW>(my, scratch, &nchunks);
+    for (int s = s0; s < s1; ++s) {
+      const int e = a.seg_expert[s], row0 = a.seg_row0[s], rows = a.seg_rows[s];
+      for (int c = 0; c * a.tokc < rows; ++c)
+        a.chunk_list[off++] = make_int4(e, row0 + c * a.tokc, min(a.tokc, rows - c * a.tokc), 0);
+    }
+    if (tid == 0) {
+      a.hdr->nseg = nseg;
+      a.hdr->n_chunks = nchunks;
+      a.hdr->n_items_gu = nchunks * a.mtiles_gu * a.ksplit_gu;
+      a.hdr->n_items_dn = nchunks * a.mtiles_dn;
+      a.hdr->next_gu = 0;
+      a.hdr->next_dn = 0;
+    }
+    if (a.split_cnt && a.ksplit_gu > 1)
+      for (int i = tid; i < nchunks * a.mtiles_gu; i += NT) a.split_cnt[i] = 0;
+    return;
+  }
+  // Tensor-core path: tiles per segment = (token chunks) x (row tiles); prefix over segments.
+  int my_gu = 0, my_dn = 0;
+  for (int s = s0; s < s1; ++s) {
+    const int chunks = (a.seg_rows[s] + a.tokc - 1) / a.tokc;
+    my_gu += chunks * a.mtiles_gu;
+    my_dn += chunks * a.mtiles_dn;
+  }
+  int tot_gu, tot_dn;
+  int pg = block_scan_excl<NW>(my_gu, scratch, &tot_gu);
+  int pd = block_scan_excl<NW>(my_dn, scratch, &tot_dn);
+  for (int s = s0; s < s1; ++s) {
+    const int chunks = (a.seg_rows[s] + a.tokc - 1) / a.tokc;
+    a.seg_item_gu[s] = pg;
+    a.seg_item_dn[s] = pd;
+    pg += chunks * a.mtiles_gu;
+    pd += chunks * a.mtiles_dn;
+  }
+  if (tid == 0) {
+    a.seg_item_gu[nseg] = tot_gu;
+    a.seg_item_dn[nseg] = tot_dn;
+    a.hdr->nseg = nseg;
+    a.hdr->n_items_gu = tot_gu;
+    a.hdr->n_items_dn = tot_dn;
+    a.hdr->next_gu = 0;
+    a.hdr->next_dn = 0;
+  }
+}
+
+}  // namespace strata

@@ -19,8 +19,11 @@ struct PermuteArgs {
   int* seg_item_gu;  // [nseg + 1] exclusive prefix of gate/up items
   int* seg_item_dn;  // [nseg + 1]
   int tokc;          // rows per work item along the token dimension
-  int mtiles_gu;     // I / 16
-  int mtiles_dn;     // H / 16
+  int mtiles_gu;     // gate/up row tiles per expert
+  int mtiles_dn;     // down row tiles per expert
+  int ksplit_gu;     // gate/up contraction splits per tile (1 = none)
+  int* split_cnt;    // [gate/up tiles] arrival counters of the split-K reduction, zeroed here
+  int4* chunk_list;  // warp path: {expert, first row, rows, 0} per tokc-row chunk (else null)
   WsHeader* hdr;
   uint32_t* status;
 };
@@ -35,11 +38,47 @@ struct GemmArgs {
   void* out;                 // gate/up: h bf16 [rows, N]; down: y fp32 [rows, N]
   int K;                     // contraction length (H for gate/up, I for down)
   int N;                     // weight rows per expert (I for gate/up, H for down)
-  const WsHeader* hdr;
+  WsHeader* hdr;
   const int* seg_expert;
   const int* seg_row0;
   const int* seg_rows;
   const int* seg_item;       // exclusive prefix of work items per segment, [nseg + 1]
+  const int4* chunk_list;    // {expert, first row, rows, 0} per 8-row chunk
+  int ksplit;                // contraction splits per tile (gate/up only)
+  float* split_part;         // [tiles * ksplit * 256] partial sums of split tiles
+  int* split_cnt;            // [tiles] arrival counters (zero on entry)
+};
+
+// Tensor-core grouped GEMM (gemm_tc.cu).
+struct TcArgs {
+  const uint8_t* codes0;  // gate or down codes [experts, Nw, K/2]
+  const __half* scales0;
+  const uint8_t* codes1;  // up codes (gate/up)
+  const __half* scales1;
+  void* out;              // gate/up: h bf16 [rows, Nw] (pair-interleaved columns); down: y fp32
+  int K, Nw;              // contraction; weight rows per expert
+  WsHeader* hdr;
+  const int* seg_expert;
+  const int* seg_row0;
+  const int* seg_rows;
+  const int* seg_item;    // exclusive prefix of tiles per segment
+  uint32_t* status;
+};
+
+// Fused decode router: logits (split along H over the grid), then the last CTA does softmax +
+// top-k for every token and groups the rows.
+struct RouteSmallArgs {
+  const __nv_bfloat16* x;  // [T, H]
+  const float* wr;         // [E, H]
+  const float* bias;       // [E] or null
+  int T, H, E, k;
+  uint32_t flags;
+  int epc;                 // experts per CTA (each split over 8 / epc warps along H)
+  float* logits;           // [T][E] scratch
+  int* ids;
+  float* gates;
+  PermuteArgs grp;         // grouping of the rows (ids = this->ids)
+  bool do_group;
 };
 
 cudaError_t launch_quantize(const void* w, int64_t n, int64_t k, uint8_t* codes, void* scales,
@@ -49,7 +88,16 @@ cudaError_t launch_router(const void* x, const float* wr, const float* bias, int
                           int E, int k, uint32_t flags, int nsplit, float* partial, int* ids,
                           float* gates, cudaStream_t stream);
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t stream);
+constexpr int kRouteSmallMaxT = 64;  // tokens handled by the fused decode router
+int route_small_epc(int E, int num_sms);
+cudaError_t launch_route_small(const RouteSmallArgs& a, cudaStream_t stream);
 cudaError_t launch_gemm_warp(const GemmArgs& a, bool gate_up, int num_sms, cudaStream_t stream);
+int warp_ksplit(int64_t T, int E, int k, int shared, int64_t I);
+constexpr int kTcRows = 256;  // token rows per tensor-core tile
+cudaError_t launch_gemm_tc(const TcArgs& a, bool gate_up, const void* b_rows, int64_t rows,
+                           int num_sms, cudaStream_t stream);
+cudaError_t launch_gather_rows(const void* x, const int* perm, int64_t rows, int64_t H, void* xp,
+                               cudaStream_t stream);
 cudaError_t launch_combine(const float* y, const float* gates, const int* inv, const void* x,
                            int64_t T, int64_t H, int k, int has_shared, int64_t R, int residual,
                            void* out, cudaStream_t stream);

@@ -2,17 +2,178 @@
 // point 1: softmax and top-k selection fused into one kernel; routing engine of the 102.7 tok/s
 // write-up, zwxr.cn/news/276292, §3.2: softmax over the logits, partial sort, expert ids out).
 //
-// Two launches:
-//  router_logits_kernel  fp32 x*Wr^T tile GEMM (SIMT, fp32 accumulation in 32-term chunks joined by
-//                        compensated addition), split along H so that a
-//                        decode batch of a few tokens still spreads the router matrix over the SMs.
-//                        Partial sums go to the workspace as [split][T][E].
-//  router_topk_kernel    one warp per token: sums the partials in split order (deterministic), adds
-//                        the bias, softmax in fp32, then k rounds of a warp arg-max (largest logit,
-//                        lower expert id on ties), gates = p of the chosen experts.
-#include "kernels.cuh"
+// Decode batches (T <= 64): ONE launch, route_small_kernel. Each CTA owns 1-8 router rows (about
+// one CTA per SM); the 8 warps split each row along H, dot their slice with every token and the
+// slices are summed in shared memory in a fixed order. The last CTA to finish (a device-scope
+// counter) runs softmax and top-k for every token and then groups the routed rows
+// (group_rows.cuh).
+//
+// Large batches: router_logits_kernel (fp32 tile GEMM, 32-term chunks joined by compensated
+// addition), router_topk_kernel (one warp per token), then the permute kernel.
+//
+// Top-k order: descending logit, ties to the lower expert id; gates = softmax probabilities of the
+// chosen experts (fp32, expf), renormalised over the k only with STRATA_RENORM.
+#include "group_rows.cuh"
 
 namespace strata {
+
+// ----------------------------------------------------------------------------- shared pieces
+
+// Softmax + top-k of one token whose E logits sit in shared memory (one warp).
+__device__ void warp_softmax_topk(const float* lg, int E, int k, uint32_t flags, int* ids,
+                                  float* gates) {
+  const int lane = threadIdx.x & 31;
+  float mx = -INFINITY;
+  for (int e = lane; e < E; e += 32) mx = fmaxf(mx, lg[e]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float sum = 0.f;
+  for (int e = lane; e < E; e += 32) sum += expf(lg[e] - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+
+  uint32_t taken = 0;  // bit i: expert lane + 32*i already chosen
+  float gsum = 0.f;
+  float my_g = 0.f;    // lane j keeps the j-th gate
+  int my_i = 0;
+  for (int j = 0; j < k; ++j) {
+    float best = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int e = lane, i = 0; e < E; e += 32, ++i) {
+      if (taken & (1u << i)) continue;
+      const float v = lg[e];
+      if (bi == 0x7fffffff || v > best) { best = v; bi = e; }  // e ascends: ties keep the lower id
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > best || (ov == best && oi < bi))) {
+        best = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    const float g = expf(best - mx) / sum;
+    gsum += g;
+    if (lane == j) { my_g = g; my_i = bi; }
+  }
+  if (lane < k) {
+    ids[lane] = my_i;
+    gates[lane] = (flags & STRATA_RENORM) ? my_g / gsum : my_g;
+  }
+}
+
+// ----------------------------------------------------------------------------- decode: fused
+
+constexpr int kRsWarps = 8;
+
+int route_small_epc(int E, int num_sms) {
+  int epc = 1;  // experts per CTA: about one CTA per SM
+  while (epc < 8 && (E + epc - 1) / epc > num_sms) epc *= 2;
+  return epc;
+}
+
+__global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
+  extern __shared__ __align__(16) unsigned char rs_smem[];  // [8][E] floats / ints (last CTA)
+  __shared__ float red[kRsWarps][kRouteSmallMaxT];
+  __shared__ int is_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = a.T, H = a.H, E = a.E;
+  const int wpe = kRsWarps / a.epc;  // warps per expert
+  const int slot = warp / wpe, part = warp - slot * wpe;
+  const int e = blockIdx.x * a.epc + slot;
+
+  // logits: each warp dots its H slice of one router row with every token (8 tokens at a time)
+  const int nvec = H / 8;
+  const int vb = part * nvec / wpe, ve = (part + 1) * nvec / wpe;
+  for (int t0 = 0; t0 < T; t0 += 8) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (e < E) {
+      for (int v = vb + lane; v < ve; v += 32) {
+        const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.wr + static_cast<int64_t>(e) * H) + 2 * v);
+        const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.wr + static_cast<int64_t>(e) * H) + 2 * v + 1);
+        const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+        for (int tt = 0; tt < 8; ++tt) {
+          if (t0 + tt < T) {
+            const uint4 raw = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t0 + tt) * H) + v);
+            const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float2 f = __bfloat1622float2(p[q]);
+              acc[tt] = fmaf(f.x, w[2 * q], acc[tt]);
+              acc[tt] = fmaf(f.y, w[2 * q + 1], acc[tt]);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int tt = 0; tt < 8; ++tt) {
+      float v = acc[tt];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0 && t0 + tt < T) red[warp][t0 + tt] = v;
+    }
+  }
+  __syncthreads();
+  // the H slices of one expert, summed in slice order
+  for (int i = threadIdx.x; i < a.epc * T; i += blockDim.x) {
+    const int sl = i / T, t = i - sl * T;
+    const int ee = blockIdx.x * a.epc + sl;
+    if (ee >= E) continue;
+    float v = 0.f;
+    for (int p = 0; p < wpe; ++p) v += red[sl * wpe + p][t];
+    if (a.bias) v += a.bias[ee];
+    a.logits[static_cast<int64_t>(t) * E + ee] = v;
+  }
+
+  // last CTA: softmax + top-k of every token, then the grouping
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(&a.grp.hdr->route_done, 1u);
+    is_last = (prev == gridDim.x - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+
+  float* lg = reinterpret_cast<float*>(rs_smem);  // [8 warps][E]
+  for (int t = warp; t < T; t += kRsWarps) {
+    float* l = lg + warp * E;
+#pragma unroll 4
+    for (int e2 = lane; e2 < E; e2 += 32) l[e2] = __ldcg(a.logits + static_cast<int64_t>(t) * E + e2);
+    __syncwarp();
+    warp_softmax_topk(l, E, a.k, a.flags, a.ids + static_cast<int64_t>(t) * a.k,
+                      a.gates + static_cast<int64_t>(t) * a.k);
+    __syncwarp();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) a.grp.hdr->route_done = 0;
+  if (a.do_group) {
+    int* hist = reinterpret_cast<int*>(rs_smem);  // [8][E]
+    __shared__ int scratch[kRsWarps + 1];
+    group_rows<kRsWarps>(a.grp, hist, scratch);
+  }
+}
+
+cudaError_t launch_route_small(const RouteSmallArgs& a, cudaStream_t stream) {
+  if (a.T == 0) return cudaSuccess;
+  const dim3 grid((a.E + a.epc - 1) / a.epc);
+  const size_t smem = static_cast<size_t>(kRsWarps) * a.E * 4;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(route_small_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  route_small_kernel<<<grid, kRsWarps * 32, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- large batches
 
 constexpr int kRouterBT = 32;  // tokens per CTA tile
 constexpr int kRouterBE = 64;  // experts per CTA tile
@@ -97,7 +258,7 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
   }
 }
 
-// One warp per token. Logits of the token live in shared memory (E <= 1024).
+// One warp per token; the split partials are summed in split order.
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ partial,
                                                           int nsplit, const float* __restrict__ bias,
                                                           int T, int E, int k, uint32_t flags,
@@ -108,54 +269,15 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
   float* lg = lg_all + warp * E;
-  float mx = -INFINITY;
   for (int e = lane; e < E; e += 32) {
     float v = 0.f;
-    for (int s = 0; s < nsplit; ++s) v += partial[(static_cast<int64_t>(s) * T + t) * E + e];
+    for (int s = 0; s < nsplit; ++s) v += __ldcg(partial + (static_cast<int64_t>(s) * T + t) * E + e);
     if (bias) v += bias[e];
     lg[e] = v;
-    mx = fmaxf(mx, v);
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float sum = 0.f;
-  for (int e = lane; e < E; e += 32) sum += expf(lg[e] - mx);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   __syncwarp();
-
-  uint32_t taken = 0;  // bit i: expert lane + 32*i already chosen
-  float gsel[STRATA_MAX_TOPK > 32 ? 32 : STRATA_MAX_TOPK];
-  int isel[STRATA_MAX_TOPK > 32 ? 32 : STRATA_MAX_TOPK];
-  float gsum = 0.f;
-  for (int j = 0; j < k; ++j) {
-    float best = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int e = lane, i = 0; e < E; e += 32, ++i) {
-      if (taken & (1u << i)) continue;
-      const float v = lg[e];
-      if (v > best || (v == best && e < bi) || bi == 0x7fffffff) { best = v; bi = e; }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > best || (ov == best && oi < bi))) {
-        best = ov; bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    const float g = expf(best - mx) / sum;
-    if (j < 32) { gsel[j] = g; isel[j] = bi; }
-    gsum += g;
-  }
-  if (lane == 0) {
-    const bool renorm = (flags & STRATA_RENORM) != 0;
-    for (int j = 0; j < k; ++j) {
-      ids[static_cast<int64_t>(t) * k + j] = isel[j];
-      gates[static_cast<int64_t>(t) * k + j] = renorm ? gsel[j] / gsum : gsel[j];
-    }
-  }
+  warp_softmax_topk(lg, E, k, flags, ids + static_cast<int64_t>(t) * k,
+                    gates + static_cast<int64_t>(t) * k);
 }
 
 int router_num_splits(int64_t T, int64_t H, int E, int num_sms) {

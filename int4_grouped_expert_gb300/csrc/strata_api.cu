@@ -25,7 +25,8 @@ static RouteLayout route_layout(int64_t T, int64_t H, int E, int k, int shared, 
   const int ns = router_num_splits(T, H, E, kRouterSplitsForSizing);
   const int64_t R = T * k;
   L.hdr = o; o = up(o + sizeof(WsHeader));
-  L.partial = o; o = up(o + sizeof(float) * ns * T * E);
+  const size_t pf = static_cast<size_t>(ns) * T * E;  // >= T * E: also the decode logits
+  L.partial = o; o = up(o + sizeof(float) * pf);
   L.ids = o; o = up(o + sizeof(int) * R);
   L.gates = o; o = up(o + sizeof(float) * R);
   L.counts = o; o = up(o + sizeof(int) * (E + 1));
@@ -38,8 +39,18 @@ static RouteLayout route_layout(int64_t T, int64_t H, int E, int k, int shared, 
 
 struct FwdLayout {
   RouteLayout r;
-  size_t seg_expert, seg_row0, seg_rows, seg_item_gu, seg_item_dn, h, y, total;
+  size_t seg_expert, seg_row0, seg_rows, seg_item_gu, seg_item_dn, chunk_list, h, y, xp,
+      split_part, split_cnt, total;
+  int ksplit;
+  bool tc;  // tensor-core path for the grouped GEMMs
 };
+
+// Tensor-core path for batches with enough rows per expert to fill 128 x N tiles.
+static bool use_tc_path(const strata_moe_layer* L, int64_t T) {
+  if (L->flags & STRATA_FORCE_WARP_PATH) return false;
+  if (L->flags & STRATA_FORCE_TC_PATH) return true;
+  return T >= 128;
+}
 static FwdLayout fwd_layout(const strata_moe_layer* L, int64_t T) {
   FwdLayout F{};
   F.r = route_layout(T, L->H, L->E, L->k, L->has_shared);
@@ -51,8 +62,18 @@ static FwdLayout fwd_layout(const strata_moe_layer* L, int64_t T) {
   F.seg_rows = o; o = up(o + sizeof(int) * nseg);
   F.seg_item_gu = o; o = up(o + sizeof(int) * nseg);
   F.seg_item_dn = o; o = up(o + sizeof(int) * nseg);
+  F.tc = use_tc_path(L, T);
+  const int64_t segs = (T * L->k < L->E ? T * L->k : L->E) + L->has_shared;
+  const int64_t max_chunks = rows / 8 + segs;  // 8-row chunks of the warp path
+  F.chunk_list = o; o = up(o + sizeof(int4) * (F.tc ? 0 : max_chunks));
   F.h = o; o = up(o + sizeof(uint16_t) * rows * L->I);
   F.y = o; o = up(o + sizeof(float) * rows * L->H);
+  F.xp = o; o = up(o + sizeof(uint16_t) * (F.tc ? rows * L->H : 0));
+  F.ksplit = F.tc ? 1 : warp_ksplit(T, L->E, L->k, L->has_shared, L->I);
+  // split-K scratch: tiles <= chunks * (I / 16)
+  const int64_t ntile = F.ksplit > 1 ? max_chunks * (L->I / 16) : 0;
+  F.split_part = o; o = up(o + sizeof(float) * 256 * F.ksplit * ntile);
+  F.split_cnt = o; o = up(o + sizeof(int) * ntile);
   F.total = o;
   return F;
 }
@@ -75,7 +96,11 @@ static strata_status check_layer(const strata_moe_layer* L) {
   if (L->has_shared != 0 && L->has_shared != 1) return STRATA_ERR_INVALID_ARG;
   if (L->E < 1 || L->E + L->has_shared > STRATA_MAX_EXPERTS) return STRATA_ERR_UNSUPPORTED;
   if (L->k < 1 || L->k > L->E || L->k > STRATA_MAX_TOPK) return STRATA_ERR_INVALID_ARG;
-  if (L->flags & ~(STRATA_RENORM | STRATA_ADD_RESIDUAL)) return STRATA_ERR_INVALID_ARG;
+  if (L->flags & ~(STRATA_RENORM | STRATA_ADD_RESIDUAL | STRATA_FORCE_WARP_PATH |
+                   STRATA_FORCE_TC_PATH))
+    return STRATA_ERR_INVALID_ARG;
+  if ((L->flags & STRATA_FORCE_WARP_PATH) && (L->flags & STRATA_FORCE_TC_PATH))
+    return STRATA_ERR_INVALID_ARG;
   if (!L->w_router || !L->gate_codes || !L->gate_scales || !L->up_codes || !L->up_scales ||
       !L->down_codes || !L->down_scales)
     return STRATA_ERR_INVALID_ARG;
@@ -129,10 +154,6 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
   if (!mark(0)) return STRATA_ERR_CUDA;
   cudaError_t e = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st);
   if (e != cudaSuccess) return STRATA_ERR_CUDA;
-  const int nsplit = router_num_splits(T, L->H, E, sms);
-  e = launch_router(x, L->w_router, L->bias, T, L->H, E, k, L->flags & STRATA_RENORM, nsplit,
-                    reinterpret_cast<float*>(base + F.r.partial), ids, gates, st);
-  if (e != cudaSuccess || !mark(1)) return STRATA_ERR_CUDA;
 
   PermuteArgs pa{};
   pa.ids = ids;
@@ -149,45 +170,113 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
   pa.seg_rows = reinterpret_cast<int*>(base + F.seg_rows);
   pa.seg_item_gu = reinterpret_cast<int*>(base + F.seg_item_gu);
   pa.seg_item_dn = reinterpret_cast<int*>(base + F.seg_item_dn);
-  pa.tokc = 8;
-  pa.mtiles_gu = static_cast<int>(L->I / 16);
-  pa.mtiles_dn = static_cast<int>(L->H / 16);
+  if (F.tc) {
+    pa.tokc = kTcRows;
+    pa.mtiles_gu = static_cast<int>(L->I / 128);
+    pa.mtiles_dn = static_cast<int>(L->H / 128);
+    pa.ksplit_gu = 1;
+    pa.chunk_list = nullptr;
+  } else {
+    pa.tokc = 8;
+    pa.mtiles_gu = static_cast<int>(L->I / 16);
+    pa.mtiles_dn = static_cast<int>(L->H / 16);
+    pa.ksplit_gu = F.ksplit;
+    pa.chunk_list = reinterpret_cast<int4*>(base + F.chunk_list);
+  }
+  pa.split_cnt = F.ksplit > 1 ? reinterpret_cast<int*>(base + F.split_cnt) : nullptr;
   pa.hdr = hdr;
   pa.status = &hdr->status;
-  e = launch_permute(pa, st);
-  if (e != cudaSuccess || !mark(2)) return STRATA_ERR_CUDA;
 
-  GemmArgs g{};
-  g.codes0 = L->gate_codes;
-  g.scales0 = static_cast<const __half*>(L->gate_scales);
-  g.codes1 = L->up_codes;
-  g.scales1 = static_cast<const __half*>(L->up_scales);
-  g.act = static_cast<const __nv_bfloat16*>(x);
-  g.perm = perm;
-  g.out = base + F.h;
-  g.K = static_cast<int>(L->H);
-  g.N = static_cast<int>(L->I);
-  g.hdr = hdr;
-  g.seg_expert = pa.seg_expert;
-  g.seg_row0 = pa.seg_row0;
-  g.seg_rows = pa.seg_rows;
-  g.seg_item = pa.seg_item_gu;
-  e = launch_gemm_warp(g, true, sms, st);
-  if (e != cudaSuccess || !mark(3)) return STRATA_ERR_CUDA;
+  if (T <= kRouteSmallMaxT) {
+    RouteSmallArgs ra{};
+    ra.x = static_cast<const __nv_bfloat16*>(x);
+    ra.wr = L->w_router;
+    ra.bias = L->bias;
+    ra.T = static_cast<int>(T);
+    ra.H = static_cast<int>(L->H);
+    ra.E = E;
+    ra.k = k;
+    ra.flags = L->flags & STRATA_RENORM;
+    ra.epc = route_small_epc(E, sms);
+    ra.logits = reinterpret_cast<float*>(base + F.r.partial);
+    ra.ids = ids;
+    ra.gates = gates;
+    ra.grp = pa;
+    ra.do_group = true;
+    e = launch_route_small(ra, st);
+    if (e != cudaSuccess || !mark(1) || !mark(2)) return STRATA_ERR_CUDA;
+  } else {
+    const int nsplit = router_num_splits(T, L->H, E, sms);
+    e = launch_router(x, L->w_router, L->bias, T, L->H, E, k, L->flags & STRATA_RENORM, nsplit,
+                      reinterpret_cast<float*>(base + F.r.partial), ids, gates, st);
+    if (e != cudaSuccess || !mark(1)) return STRATA_ERR_CUDA;
+    e = launch_permute(pa, st);
+    if (e != cudaSuccess || !mark(2)) return STRATA_ERR_CUDA;
+  }
 
-  GemmArgs d = g;
-  d.codes0 = L->down_codes;
-  d.scales0 = static_cast<const __half*>(L->down_scales);
-  d.codes1 = nullptr;
-  d.scales1 = nullptr;
-  d.act = reinterpret_cast<const __nv_bfloat16*>(base + F.h);
-  d.perm = nullptr;
-  d.out = base + F.y;
-  d.K = static_cast<int>(L->I);
-  d.N = static_cast<int>(L->H);
-  d.seg_item = pa.seg_item_dn;
-  e = launch_gemm_warp(d, false, sms, st);
-  if (e != cudaSuccess || !mark(4)) return STRATA_ERR_CUDA;
+  const int64_t rows = R + (S ? T : 0);
+  if (F.tc) {
+    e = launch_gather_rows(x, perm, rows, L->H, base + F.xp, st);
+    if (e != cudaSuccess) return STRATA_ERR_CUDA;
+    TcArgs g{};
+    g.codes0 = L->gate_codes;
+    g.scales0 = static_cast<const __half*>(L->gate_scales);
+    g.codes1 = L->up_codes;
+    g.scales1 = static_cast<const __half*>(L->up_scales);
+    g.out = base + F.h;
+    g.K = static_cast<int>(L->H);
+    g.Nw = static_cast<int>(L->I);
+    g.hdr = hdr;
+    g.seg_expert = pa.seg_expert;
+    g.seg_row0 = pa.seg_row0;
+    g.seg_rows = pa.seg_rows;
+    g.seg_item = pa.seg_item_gu;
+    g.status = &hdr->status;
+    e = launch_gemm_tc(g, true, base + F.xp, rows, sms, st);
+    if (e != cudaSuccess || !mark(3)) return STRATA_ERR_CUDA;
+    TcArgs d = g;
+    d.codes0 = L->down_codes;
+    d.scales0 = static_cast<const __half*>(L->down_scales);
+    d.codes1 = nullptr;
+    d.scales1 = nullptr;
+    d.out = base + F.y;
+    d.K = static_cast<int>(L->I);
+    d.Nw = static_cast<int>(L->H);
+    d.seg_item = pa.seg_item_dn;
+    e = launch_gemm_tc(d, false, base + F.h, rows, sms, st);
+    if (e != cudaSuccess || !mark(4)) return STRATA_ERR_CUDA;
+  } else {
+    GemmArgs g{};
+    g.codes0 = L->gate_codes;
+    g.scales0 = static_cast<const __half*>(L->gate_scales);
+    g.codes1 = L->up_codes;
+    g.scales1 = static_cast<const __half*>(L->up_scales);
+    g.act = static_cast<const __nv_bfloat16*>(x);
+    g.perm = perm;
+    g.out = base + F.h;
+    g.K = static_cast<int>(L->H);
+    g.N = static_cast<int>(L->I);
+    g.hdr = hdr;
+    g.chunk_list = pa.chunk_list;
+    g.ksplit = F.ksplit;
+    g.split_part = reinterpret_cast<float*>(base + F.split_part);
+    g.split_cnt = pa.split_cnt;
+    e = launch_gemm_warp(g, true, sms, st);
+    if (e != cudaSuccess || !mark(3)) return STRATA_ERR_CUDA;
+    GemmArgs d = g;
+    d.codes0 = L->down_codes;
+    d.scales0 = static_cast<const __half*>(L->down_scales);
+    d.codes1 = nullptr;
+    d.scales1 = nullptr;
+    d.act = reinterpret_cast<const __nv_bfloat16*>(base + F.h);
+    d.perm = nullptr;
+    d.out = base + F.y;
+    d.K = static_cast<int>(L->I);
+    d.N = static_cast<int>(L->H);
+    d.ksplit = 1;
+    e = launch_gemm_warp(d, false, sms, st);
+    if (e != cudaSuccess || !mark(4)) return STRATA_ERR_CUDA;
+  }
 
   e = launch_combine(reinterpret_cast<const float*>(base + F.y), gates, inv, x, T, L->H, k, S, R,
                      (L->flags & STRATA_ADD_RESIDUAL) ? 1 : 0, out, st);

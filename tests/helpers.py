@@ -50,7 +50,7 @@ class OracleExperts:
 
 
 def build_gpu_layer(wl, layer=0, router_kind=None, flags=0, bias=None, w_router=None,
-                    overrides=None, threads=0):
+                    overrides=None, threads=0, experts=None):
     """MoELayer with the workload's router and experts, quantized on the device."""
     from int4_grouped_expert_gb300 import MoELayer
     torch = torch_mod()
@@ -63,6 +63,8 @@ def build_gpu_layer(wl, layer=0, router_kind=None, flags=0, bias=None, w_router=
     batch = 16
     for s in range(0, n, batch):
         es = list(range(s, min(n, s + batch)))
+        if experts is not None:                 # only these experts get weights (others stay 0)
+            es = [e for e in es if e in experts]
         todo = [e for e in es if e not in overrides]
         mats = dict(zip(todo, gen.expert_weights_many(wl, todo, layer, threads)))
         mats.update({e: overrides[e] for e in es if e in overrides})

@@ -67,8 +67,8 @@ def layer(st, **kw):
 def test_workspace_sizes(st):
     s1 = st.strata_moe_workspace_size(layer(st), 1)
     s16 = st.strata_moe_workspace_size(layer(st), 16)
-    assert 0 < s1 < s16
-    assert s16 % 256 == 0
+    assert s1 > 0 and s16 > 0          # (tiny batches add split-K scratch, so no monotonicity)
+    assert s16 % 256 == 0 and s1 % 256 == 0
     # h (bf16 [T*k+T, I]) and y (fp32 [T*k+T, H]) dominate
     assert s16 >= 2 * 144 * 1536 + 4 * 144 * 4096
     assert st.strata_moe_workspace_size(layer(st, H=4000), 4) == 0

@@ -140,3 +140,20 @@ def test_forward_argument_errors():
     assert st.strata_moe_forward(s, x, 0, out, ws, need) == 0              # empty batch
     s.k = 17
     assert st.strata_moe_forward(s, x, 4, out, ws, need) == 1              # k > E
+
+
+@pytest.mark.parametrize("T,path", [(64, "tc"), (200, "warp"), (200, "tc"), (1, "tc"), (300, "tc")])
+def test_c1_both_gemm_paths(T, path):
+    """The warp (mma.sync) and tensor-core (tcgen05) grouped GEMMs on the same layer."""
+    import int4_grouped_expert_gb300 as st
+    flag = st.STRATA_FORCE_TC_PATH if path == "tc" else st.STRATA_FORCE_WARP_PATH
+    wl, L, wr, b = layer_for("c1", flags=flag)
+    check_layer(wl, L, wr, b, gen.activations(T, wl.H, wl.seed, name=f"path{T}"))
+
+
+def test_tc_path_shared_expert_and_long_segments():
+    """Shared expert with T rows spans several 256-row tiles; k = E keeps every expert busy."""
+    import int4_grouped_expert_gb300 as st
+    wl = Workload("t2", "tc-edge", H=384, I=256, E=6, k=6, shared=1, batches=(600,), router="uniform")
+    L, wr, b = build_gpu_layer(wl, flags=st.STRATA_FORCE_TC_PATH)
+    check_layer(wl, L, wr, b, gen.activations(600, wl.H, 8))
