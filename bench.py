@@ -387,6 +387,110 @@ def run_strata(args):
         print(json.dumps(rec), flush=True)
 
 
+def run_prefill(args):
+    """Prefill workloads (c3: 512 tokens; c5: 4096 tokens + on-device quantization) on the
+    tensor-core path. Reports tokens/s, gate/up and down TFLOP/s and, for c5, quantize GB/s."""
+    import torch
+    import int4_grouped_expert_gb300 as st
+    from int4_grouped_expert_gb300 import MoELayer
+    ws_n, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    st.lib()
+    wl = CONFIGS[args.workload]
+    if args.experts:  # a smaller layer of the same shapes (e.g. for profiler captures)
+        import dataclasses
+        wl = dataclasses.replace(wl, E=args.experts)
+    T = args.tokens or wl.batches[0]
+    L = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared)
+    L.set_router(gen.router_weight(wl), gen.router_bias(wl, 0, args.router) if not args.experts
+                 else None)
+    n = wl.E + wl.shared
+    quant = None
+    if args.workload == "c5" and not args.experts:
+        # fp16 experts resident on the device, then one quantize launch per projection stack
+        w16 = {"gate": torch.empty(n, wl.I, wl.H, dtype=torch.float16, device="cuda"),
+               "up": torch.empty(n, wl.I, wl.H, dtype=torch.float16, device="cuda"),
+               "down": torch.empty(n, wl.H, wl.I, dtype=torch.float16, device="cuda")}
+        for s0 in range(0, n, 16):
+            es = list(range(s0, min(n, s0 + 16)))
+            for e, (g, u, d) in zip(es, gen.expert_weights_many(wl, es)):
+                w16["gate"][e].copy_(torch.from_numpy(g))
+                w16["up"][e].copy_(torch.from_numpy(u))
+                w16["down"][e].copy_(torch.from_numpy(d))
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        jobs = [(w16["gate"], L.gate_codes, L.gate_scales, wl.I * n, wl.H),
+                (w16["up"], L.up_codes, L.up_scales, wl.I * n, wl.H),
+                (w16["down"], L.down_codes, L.down_scales, wl.H * n, wl.I)]
+
+        def quantize_all():
+            for w, c, sc, rows, cols in jobs:
+                st.check(st.strata_quantize_groups(w, rows, cols, c, sc, status), "quantize")
+        for _ in range(2):
+            quantize_all()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 3
+        e0.record()
+        for _ in range(reps):
+            quantize_all()
+        e1.record()
+        torch.cuda.synchronize()
+        qs = e0.elapsed_time(e1) / reps / 1e3
+        nw = 3 * n * wl.H * wl.I
+        qbytes = nw * 2 + nw // 2 + 2 * (nw // 128)
+        quant = {"seconds": qs, "weights": nw, "bytes": qbytes, "gbs": qbytes / qs / 1e9,
+                 "frac_of_hbm": qbytes / qs / 1e9 / peak_numbers()[0]}
+        rc, v = st.strata_read_status(status)
+        assert rc == 0, hex(v)
+        del w16
+        torch.cuda.empty_cache()
+    else:
+        for s0 in range(0, n, 16):
+            es = list(range(s0, min(n, s0 + 16)))
+            for e, m in zip(es, gen.expert_weights_many(wl, es)):
+                L.load_expert_fp16(e, *m)
+        torch.cuda.synchronize()
+        L.check_status()
+    xs_host, xs_dev = token_batches(wl, T, 2)
+    ws_bytes = L.workspace_size(T)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty(T, wl.H, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    steps = args.steps
+    clocks = ClockSampler(local)
+    elapsed_ms, _ = time_steps([L], xs_dev, T, steps, args.warmup, stream, ws, ws_bytes, out)
+    clk = clocks.stop()
+    _, stages = time_steps([L], xs_dev, T, steps, args.warmup, stream, ws, ws_bytes, out,
+                           profiled=True)
+    rows = T * wl.k + wl.shared * T
+    gu_flops = 2 * 2 * wl.H * wl.I * rows
+    dn_flops = 2 * wl.H * wl.I * rows
+    ms = elapsed_ms / steps
+    peak_tf = 1695.4
+    try:
+        peak_tf = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops_sustained"])
+    except Exception:
+        pass
+    gu_tf = gu_flops / (stages["gate_up_gemm"] / 1e3) / 1e12
+    dn_tf = dn_flops / (stages["down_gemm"] / 1e3) / 1e12
+    layer_tf = (gu_flops + dn_flops) / (ms / 1e3) / 1e12
+    rec = {"metric": f"MoE-layer tokens/s (prefill, {args.workload})", "value": T / (ms / 1e3),
+           "unit": "tokens/s", "n_gpus": ws_n, "steps": steps, "warmup": args.warmup,
+           "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": wl.name, "tokens_per_step": T, "router": args.router or wl.router},
+           "roofline": {"kernel": "gate_up_gemm (tcgen05 grouped W4A16 GEMM + SiLU)",
+                        "bound": "tensor", "achieved": gu_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                        "frac": gu_tf / peak_tf, "peak_kind": "measured sustained",
+                        "traffic": None},
+           "layer_tflops": layer_tf, "layer_frac": layer_tf / peak_tf, "down_tflops": dn_tf,
+           "stages_us": {k: v * 1e3 for k, v in stages.items()}, "quantize": quant,
+           "gpu_launches": None, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(rec), flush=True)
+
+
 def run_reference(args):
     """The oracle on the host cores, same metric and workload, each step a bounded sample."""
     ws_n, rank = init_dist("gloo")
@@ -454,6 +558,11 @@ def main(argv=None):
     p.add_argument("--impl", choices=["strata", "reference"], default="strata")
     p.add_argument("--ref-tokens", type=int, default=1)
     p.add_argument("--ref-budget-s", type=float, default=240.0)
+    p.add_argument("--workload", choices=["c2", "c3", "c5"], default="c2",
+                   help="c2: the decode layer (default, the headline); c3 / c5: prefill layers")
+    p.add_argument("--router", choices=["uniform", "zipf"], default=None)
+    p.add_argument("--experts", type=int, default=0, help="prefill: override the routed expert count")
+    p.add_argument("--tokens", type=int, default=0, help="prefill: override the batch")
     args = p.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -461,6 +570,10 @@ def main(argv=None):
         args.steps = 10 if args.impl == "reference" else 5000
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "c2":
+        if args.steps == 5000:
+            args.steps = 50
+        run_prefill(args)
     else:
         run_strata(args)
 

@@ -5,7 +5,8 @@
 // Rows r = t*k + j of the flattened [T, k] id array are ordered by (expert, token): each warp owns a
 // contiguous range of r, counts it into its own histogram row (equal ids inside a 32-row step are
 // grouped with __match_any_sync), the histograms are scanned per expert in warp order, and the same
-// walk then hands out positions. The result does not depend on thread timing.
+// walk then hands out positions. The result does not depend on thread timing. Everything the CTA
+// reads back lives in shared memory; global memory only receives the outputs.
 #pragma once
 
 #include "kernels.cuh"
@@ -43,14 +44,39 @@ __device__ __forceinline__ int block_scan_excl(int v, int* scratch, int* total) 
   return res;
 }
 
-// Group rows. hist: NW*E ints of shared memory; scratch: NW+1 ints of shared memory.
-// Per-thread expert ownership: thread i owns experts [i*EPT, i*EPT + EPT) with EPT = ceil(E / NT).
+// Shared-memory scratch of group_rows (ints).
+struct GroupSmem {
+  int* hist;    // [NW][E]
+  int* cnt;     // [E]
+  int* off;     // [E + 1]
+  int* seg_e;   // [E + 2]
+  int* seg_r0;  // [E + 2]
+  int* seg_n;   // [E + 2]
+  int* scratch; // [NW + 1]
+};
+__host__ __device__ constexpr size_t group_smem_ints(int NW, int E) {
+  return static_cast<size_t>(NW) * E + E + (E + 1) + 3 * (E + 2) + NW + 1;
+}
+__device__ __forceinline__ GroupSmem carve_group_smem(int* base, int NW, int E) {
+  GroupSmem g;
+  g.hist = base;
+  g.cnt = g.hist + NW * E;
+  g.off = g.cnt + E;
+  g.seg_e = g.off + E + 1;
+  g.seg_r0 = g.seg_e + E + 2;
+  g.seg_n = g.seg_r0 + E + 2;
+  g.scratch = g.seg_n + E + 2;
+  return g;
+}
+
+// ids: the [T, k] ids (global or shared memory).
 template <int NW>
-__device__ void group_rows(const PermuteArgs& a, int* hist, int* scratch) {
+__device__ void group_rows(const PermuteArgs& a, const int* ids, GroupSmem sm) {
   constexpr int NT = NW * 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E;
   const int R = a.T * a.k;
+  int* hist = sm.hist;
   for (int i = tid; i < NW * E; i += NT) hist[i] = 0;
   __syncthreads();
 
@@ -61,7 +87,7 @@ __device__ void group_rows(const PermuteArgs& a, int* hist, int* scratch) {
     const int r = base + lane;
     const unsigned active = __ballot_sync(0xffffffffu, r < rend);
     if (r < rend) {
-      int e = a.ids[r];
+      int e = ids[r];
       if (e < 0 || e >= E) {
         set_status(a.status, STRATA_DEV_BAD_ID);
         e = -1;
@@ -79,7 +105,7 @@ __device__ void group_rows(const PermuteArgs& a, int* hist, int* scratch) {
   for (int e = e0; e < e1; ++e)
     for (int w = 0; w < NW; ++w) my += hist[w * E + e];
   int total;
-  int run = block_scan_excl<NW>(my, scratch, &total);
+  int run = block_scan_excl<NW>(my, sm.scratch, &total);
   for (int e = e0; e < e1; ++e) {
     int c = 0;
     for (int w = 0; w < NW; ++w) {
@@ -87,18 +113,23 @@ __device__ void group_rows(const PermuteArgs& a, int* hist, int* scratch) {
       hist[w * E + e] = run + c;
       c += h;
     }
+    sm.cnt[e] = c;
+    sm.off[e] = run;
     a.counts[e] = c;
     a.offsets[e] = run;
     run += c;
   }
-  if (tid == 0) a.offsets[E] = total;
+  if (tid == 0) {
+    a.offsets[E] = total;
+    sm.off[E] = total;
+  }
   __syncthreads();
 
   for (int base = rbeg; base < rend; base += 32) {
     const int r = base + lane;
     const unsigned active = __ballot_sync(0xffffffffu, r < rend);
     if (r < rend) {
-      int e = a.ids[r];
+      int e = ids[r];
       if (e < 0 || e >= E) e = -1;
       const unsigned m = __match_any_sync(active, e);
       if (e >= 0) {
@@ -119,35 +150,40 @@ __device__ void group_rows(const PermuteArgs& a, int* hist, int* scratch) {
   // Active segments: the shared expert first (the largest), then routed experts with rows, by id.
   const int sh = (a.has_shared && a.T > 0) ? 1 : 0;
   int nz = 0;
-  for (int e = e0; e < e1; ++e) nz += (a.counts[e] > 0);
+  for (int e = e0; e < e1; ++e) nz += (sm.cnt[e] > 0);
   int nseg_routed;
-  int sidx = block_scan_excl<NW>(nz, scratch, &nseg_routed) + sh;
+  int sidx = block_scan_excl<NW>(nz, sm.scratch, &nseg_routed) + sh;
   for (int e = e0; e < e1; ++e) {
-    const int c = a.counts[e];
+    const int c = sm.cnt[e];
     if (c > 0) {
-      a.seg_expert[sidx] = e;
-      a.seg_row0[sidx] = a.offsets[e];
-      a.seg_rows[sidx] = c;
+      sm.seg_e[sidx] = e;
+      sm.seg_r0[sidx] = sm.off[e];
+      sm.seg_n[sidx] = c;
       ++sidx;
     }
   }
   const int nseg = nseg_routed + sh;
   if (sh && tid == 0) {
-    a.seg_expert[0] = E;
-    a.seg_row0[0] = R;
-    a.seg_rows[0] = a.T;
+    sm.seg_e[0] = E;
+    sm.seg_r0[0] = R;
+    sm.seg_n[0] = a.T;
   }
   __syncthreads();
+  for (int s = tid; s < nseg; s += NT) {
+    a.seg_expert[s] = sm.seg_e[s];
+    a.seg_row0[s] = sm.seg_r0[s];
+    a.seg_rows[s] = sm.seg_n[s];
+  }
   const int spt = (nseg + NT - 1) / NT;
   const int s0 = min(nseg, tid * spt), s1 = min(nseg, s0 + spt);
   if (a.chunk_list) {
     // Warp path: a flat list of tokc-row chunks; items = chunk x row tile (x contraction split).
-    int my = 0;
-    for (int s = s0; s < s1; ++s) my += (a.seg_rows[s] + a.tokc - 1) / a.tokc;
+    int my_c = 0;
+    for (int s = s0; s < s1; ++s) my_c += (sm.seg_n[s] + a.tokc - 1) / a.tokc;
     int nchunks;
-    int off = block_scan_excl<NW>(my, scratch, &nchunks);
+    int off = block_scan_excl<NW>(my_c, sm.scratch, &nchunks);
     for (int s = s0; s < s1; ++s) {
-      const int e = a.seg_expert[s], row0 = a.seg_row0[s], rows = a.seg_rows[s];
+      const int e = sm.seg_e[s], row0 = sm.seg_r0[s], rows = sm.seg_n[s];
       for (int c = 0; c * a.tokc < rows; ++c)
         a.chunk_list[off++] = make_int4(e, row0 + c * a.tokc, min(a.tokc, rows - c * a.tokc), 0);
     }
@@ -166,15 +202,15 @@ __device__ void group_rows(const PermuteArgs& a, int* hist, int* scratch) {
   // Tensor-core path: tiles per segment = (token chunks) x (row tiles); prefix over segments.
   int my_gu = 0, my_dn = 0;
   for (int s = s0; s < s1; ++s) {
-    const int chunks = (a.seg_rows[s] + a.tokc - 1) / a.tokc;
+    const int chunks = (sm.seg_n[s] + a.tokc - 1) / a.tokc;
     my_gu += chunks * a.mtiles_gu;
     my_dn += chunks * a.mtiles_dn;
   }
   int tot_gu, tot_dn;
-  int pg = block_scan_excl<NW>(my_gu, scratch, &tot_gu);
-  int pd = block_scan_excl<NW>(my_dn, scratch, &tot_dn);
+  int pg = block_scan_excl<NW>(my_gu, sm.scratch, &tot_gu);
+  int pd = block_scan_excl<NW>(my_dn, sm.scratch, &tot_dn);
   for (int s = s0; s < s1; ++s) {
-    const int chunks = (a.seg_rows[s] + a.tokc - 1) / a.tokc;
+    const int chunks = (sm.seg_n[s] + a.tokc - 1) / a.tokc;
     a.seg_item_gu[s] = pg;
     a.seg_item_dn[s] = pd;
     pg += chunks * a.mtiles_gu;

@@ -34,7 +34,7 @@ struct GemmArgs {
   const uint8_t* codes1;     // up codes (gate/up mode)
   const __half* scales1;
   const __nv_bfloat16* act;  // gate/up: x [T, K]; down: h [rows, K]
-  const int* perm;           // gate/up: token of each row; down: unused (row indexes h)
+  const int* perm;           // token (activation row) of each GEMM row, or null: row = activation row
   void* out;                 // gate/up: h bf16 [rows, N]; down: y fp32 [rows, N]
   int K;                     // contraction length (H for gate/up, I for down)
   int N;                     // weight rows per expert (I for gate/up, H for down)
@@ -74,6 +74,7 @@ struct RouteSmallArgs {
   int T, H, E, k;
   uint32_t flags;
   int epc;                 // experts per CTA (each split over 8 / epc warps along H)
+  __nv_bfloat16* x_perm;   // [T, H]: x with every 8-wide chunk in (0,4,1,5,2,6,3,7) order, or null
   float* logits;           // [T][E] scratch
   int* ids;
   float* gates;
@@ -92,7 +93,7 @@ constexpr int kRouteSmallMaxT = 64;  // tokens handled by the fused decode route
 int route_small_epc(int E, int num_sms);
 cudaError_t launch_route_small(const RouteSmallArgs& a, cudaStream_t stream);
 cudaError_t launch_gemm_warp(const GemmArgs& a, bool gate_up, int num_sms, cudaStream_t stream);
-int warp_ksplit(int64_t T, int E, int k, int shared, int64_t I);
+int warp_ksplit(int64_t T, int E, int k, int shared, int64_t I, int64_t H);
 constexpr int kTcRows = 256;  // token rows per tensor-core tile
 cudaError_t launch_gemm_tc(const TcArgs& a, bool gate_up, const void* b_rows, int64_t rows,
                            int num_sms, cudaStream_t stream);

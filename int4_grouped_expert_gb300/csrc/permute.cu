@@ -6,13 +6,12 @@
 namespace strata {
 
 __global__ void __launch_bounds__(1024) permute_kernel(PermuteArgs a) {
-  extern __shared__ int hist[];  // [32][E]
-  __shared__ int scratch[33];
-  group_rows<32>(a, hist, scratch);
+  extern __shared__ int gsm[];
+  group_rows<32>(a, a.ids, carve_group_smem(gsm, 32, a.E));
 }
 
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t stream) {
-  const size_t smem = static_cast<size_t>(32) * a.E * sizeof(int);
+  const size_t smem = group_smem_ints(32, a.E) * sizeof(int);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));

@@ -4,8 +4,8 @@
 //
 // HBM-streaming pass: 16 threads own one 128-wide group (8 fp16 = one 16-byte load each), find
 // the group's absmax with four butterfly shuffles, and write 4 bytes of packed codes each (the
-// half-warp's 64 bytes are contiguous) plus one fp16 scale. Each thread walks several groups with
-// a grid-stride loop so loads of the next group are in flight while the current one is packed.
+// half-warp's 64 bytes are contiguous) plus one fp16 scale. Each thread walks its groups with a
+// grid-stride loop, four groups' loads in flight at a time.
 //
 // Exactness: absmax / 7.0f is an IEEE fp32 division rounded once more to fp16 (no double-rounding
 // hazard: a/7 has a period-3 binary expansion, never 12 equal bits in a row), and w / s is an IEEE
@@ -15,6 +15,45 @@
 
 namespace strata {
 
+// One group: 16 lanes of a half-warp hold 8 fp16 each.
+__device__ __forceinline__ void quantize_one(const uint4& v, unsigned half_mask, int sub, int64_t g,
+                                             uint32_t* __restrict__ codes,
+                                             __half* __restrict__ scales, uint32_t* status) {
+  const __half* h = reinterpret_cast<const __half*>(&v);
+  float f[8];
+  float amax = 0.0f;
+  bool finite = true;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    f[i] = __half2float(h[i]);
+    finite &= isfinite(f[i]);
+    amax = fmaxf(amax, fabsf(f[i]));
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, o));
+    finite = __shfl_xor_sync(half_mask, finite ? 1 : 0, o) != 0 && finite;
+  }
+  __half s_h = __float2half_rn(amax / 7.0f);
+  const float s = __half2float(s_h);
+  uint32_t packed = 0;
+  if (finite && s > 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float q = rintf(f[i] / s);
+      q = fminf(fmaxf(q, -8.0f), 7.0f);
+      packed |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xFu) << (4 * i);
+    }
+  }
+  if (!finite) {
+    s_h = __ushort_as_half(0x7E00);  // NaN scale marks the group
+    if (sub == 0) set_status(status, STRATA_DEV_NONFINITE);
+  }
+  __stcs(codes + g * 16 + sub, packed);
+  if (sub == 0) scales[g] = s_h;
+}
+
+// Each half-warp walks groups g, g + stride, ... with four groups' loads in flight at a time.
 __global__ void __launch_bounds__(256) quantize_groups_kernel(const uint4* __restrict__ w,
                                                               int64_t n_groups,
                                                               uint32_t* __restrict__ codes,
@@ -25,40 +64,19 @@ __global__ void __launch_bounds__(256) quantize_groups_kernel(const uint4* __res
   const unsigned half_mask = (threadIdx.x & 16) ? 0xFFFF0000u : 0x0000FFFFu;
   const int64_t first = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
   const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4;
-  for (int64_t g = first; g < n_groups; g += stride) {
-    uint4 v = __ldcs(w + g * 16 + sub);  // streaming read: every weight is touched once
-    const __half* h = reinterpret_cast<const __half*>(&v);
-    float f[8];
-    float amax = 0.0f;
-    bool finite = true;
+  constexpr int U = 4;
+  for (int64_t g0 = first; g0 < n_groups; g0 += U * stride) {
+    uint4 v[U];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      f[i] = __half2float(h[i]);
-      finite &= isfinite(f[i]);
-      amax = fmaxf(amax, fabsf(f[i]));
+    for (int u = 0; u < U; ++u) {
+      const int64_t g = g0 + u * stride;
+      if (g < n_groups) v[u] = __ldcs(w + g * 16 + sub);  // streaming: every weight read once
     }
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) {
-      amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, o));
-      finite = __shfl_xor_sync(half_mask, finite ? 1 : 0, o) != 0 && finite;
+    for (int u = 0; u < U; ++u) {
+      const int64_t g = g0 + u * stride;
+      if (g < n_groups) quantize_one(v[u], half_mask, sub, g, codes, scales, status);
     }
-    __half s_h = __float2half_rn(amax / 7.0f);
-    const float s = __half2float(s_h);
-    uint32_t packed = 0;
-    if (finite && s > 0.0f) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float q = rintf(f[i] / s);
-        q = fminf(fmaxf(q, -8.0f), 7.0f);
-        packed |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xFu) << (4 * i);
-      }
-    }
-    if (!finite) {
-      s_h = __ushort_as_half(0x7E00);  // NaN scale marks the group
-      if (sub == 0) set_status(status, STRATA_DEV_NONFINITE);
-    }
-    __stcs(codes + g * 16 + sub, packed);
-    if (sub == 0) scales[g] = s_h;
   }
 }
 

@@ -74,8 +74,17 @@ int route_small_epc(int E, int num_sms) {
   return epc;
 }
 
+// dynamic shared memory of the last CTA (bytes): logits [8][E] floats, aliased by the grouping
+// scratch, then ids and gates [T*k]
+__host__ __device__ static size_t route_small_smem(int T, int E, int k) {
+  size_t a = static_cast<size_t>(kRsWarps) * E * 4;
+  const size_t g = group_smem_ints(kRsWarps, E) * 4;
+  if (g > a) a = g;
+  return a + static_cast<size_t>(T) * k * 8;
+}
+
 __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
-  extern __shared__ __align__(16) unsigned char rs_smem[];  // [8][E] floats / ints (last CTA)
+  extern __shared__ __align__(16) unsigned char rs_smem[];
   __shared__ float red[kRsWarps][kRouteSmallMaxT];
   __shared__ int is_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -84,33 +93,63 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   const int slot = warp / wpe, part = warp - slot * wpe;
   const int e = blockIdx.x * a.epc + slot;
 
-  // logits: each warp dots its H slice of one router row with every token (8 tokens at a time)
+  // the decode grouped GEMM reads x with every 8-wide chunk pair-interleaved; the CTAs share the copy
+  if (a.x_perm) {
+    const int nv = T * (H / 8);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += gridDim.x * blockDim.x) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
+      uint4 o;
+      o.x = prmt(v.x, v.z, 0x5410);
+      o.y = prmt(v.x, v.z, 0x7632);
+      o.z = prmt(v.y, v.w, 0x5410);
+      o.w = prmt(v.y, v.w, 0x7632);
+      reinterpret_cast<uint4*>(a.x_perm)[i] = o;
+    }
+  }
+  // logits: each warp dots its H slice of one router row with every token, 4 tokens x 4 vectors
+  // of 8 columns per lane and pass, all loads of a pass in flight together
   const int nvec = H / 8;
   const int vb = part * nvec / wpe, ve = (part + 1) * nvec / wpe;
-  for (int t0 = 0; t0 < T; t0 += 8) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const float4* wrow = reinterpret_cast<const float4*>(a.wr + static_cast<int64_t>(e < E ? e : 0) * H);
+  const uint4* xv = reinterpret_cast<const uint4*>(a.x);
+  for (int t0 = 0; t0 < T; t0 += 4) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (e < E) {
-      for (int v = vb + lane; v < ve; v += 32) {
-        const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.wr + static_cast<int64_t>(e) * H) + 2 * v);
-        const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.wr + static_cast<int64_t>(e) * H) + 2 * v + 1);
-        const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      for (int v0 = vb + lane; v0 < ve; v0 += 128) {
+        float4 w[4][2];
+        uint4 xr[4][4];
 #pragma unroll
-        for (int tt = 0; tt < 8; ++tt) {
-          if (t0 + tt < T) {
-            const uint4 raw = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t0 + tt) * H) + v);
-            const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        for (int i = 0; i < 4; ++i) {
+          const int v = v0 + 32 * i;
+          if (v < ve) {
+            w[i][0] = __ldg(wrow + 2 * v);
+            w[i][1] = __ldg(wrow + 2 * v + 1);
+#pragma unroll
+            for (int tt = 0; tt < 4; ++tt)
+              if (t0 + tt < T) xr[tt][i] = __ldg(xv + static_cast<int64_t>(t0 + tt) * nvec + v);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (v0 + 32 * i >= ve) continue;
+          const float wf[8] = {w[i][0].x, w[i][0].y, w[i][0].z, w[i][0].w,
+                               w[i][1].x, w[i][1].y, w[i][1].z, w[i][1].w};
+#pragma unroll
+          for (int tt = 0; tt < 4; ++tt) {
+            if (t0 + tt >= T) continue;
+            const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&xr[tt][i]);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const float2 f = __bfloat1622float2(p[q]);
-              acc[tt] = fmaf(f.x, w[2 * q], acc[tt]);
-              acc[tt] = fmaf(f.y, w[2 * q + 1], acc[tt]);
+              acc[tt] = fmaf(f.x, wf[2 * q], acc[tt]);
+              acc[tt] = fmaf(f.y, wf[2 * q + 1], acc[tt]);
             }
           }
         }
       }
     }
 #pragma unroll
-    for (int tt = 0; tt < 8; ++tt) {
+    for (int tt = 0; tt < 4; ++tt) {
       float v = acc[tt];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -140,29 +179,32 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   if (!is_last) return;
   __threadfence();
 
+  const size_t lg_bytes = route_small_smem(0, E, 0);
   float* lg = reinterpret_cast<float*>(rs_smem);  // [8 warps][E]
+  int* s_ids = reinterpret_cast<int*>(rs_smem + lg_bytes);
+  float* s_gates = reinterpret_cast<float*>(s_ids + T * a.k);
   for (int t = warp; t < T; t += kRsWarps) {
     float* l = lg + warp * E;
 #pragma unroll 4
     for (int e2 = lane; e2 < E; e2 += 32) l[e2] = __ldcg(a.logits + static_cast<int64_t>(t) * E + e2);
     __syncwarp();
-    warp_softmax_topk(l, E, a.k, a.flags, a.ids + static_cast<int64_t>(t) * a.k,
-                      a.gates + static_cast<int64_t>(t) * a.k);
+    warp_softmax_topk(l, E, a.k, a.flags, s_ids + t * a.k, s_gates + t * a.k);
     __syncwarp();
   }
   __syncthreads();
-  if (threadIdx.x == 0) a.grp.hdr->route_done = 0;
-  if (a.do_group) {
-    int* hist = reinterpret_cast<int*>(rs_smem);  // [8][E]
-    __shared__ int scratch[kRsWarps + 1];
-    group_rows<kRsWarps>(a.grp, hist, scratch);
+  for (int i = threadIdx.x; i < T * a.k; i += blockDim.x) {
+    a.ids[i] = s_ids[i];
+    a.gates[i] = s_gates[i];
   }
+  if (threadIdx.x == 0) a.grp.hdr->route_done = 0;
+  if (a.do_group)
+    group_rows<kRsWarps>(a.grp, s_ids, carve_group_smem(reinterpret_cast<int*>(rs_smem), kRsWarps, E));
 }
 
 cudaError_t launch_route_small(const RouteSmallArgs& a, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
   const dim3 grid((a.E + a.epc - 1) / a.epc);
-  const size_t smem = static_cast<size_t>(kRsWarps) * a.E * 4;
+  const size_t smem = route_small_smem(a.T, a.E, a.k);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(route_small_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -68,8 +68,8 @@ static FwdLayout fwd_layout(const strata_moe_layer* L, int64_t T) {
   F.chunk_list = o; o = up(o + sizeof(int4) * (F.tc ? 0 : max_chunks));
   F.h = o; o = up(o + sizeof(uint16_t) * rows * L->I);
   F.y = o; o = up(o + sizeof(float) * rows * L->H);
-  F.xp = o; o = up(o + sizeof(uint16_t) * (F.tc ? rows * L->H : 0));
-  F.ksplit = F.tc ? 1 : warp_ksplit(T, L->E, L->k, L->has_shared, L->I);
+  F.xp = o; o = up(o + sizeof(uint16_t) * rows * L->H);  // gathered / pair-interleaved x
+  F.ksplit = F.tc ? 1 : warp_ksplit(T, L->E, L->k, L->has_shared, L->I, L->H);
   // split-K scratch: tiles <= chunks * (I / 16)
   const int64_t ntile = F.ksplit > 1 ? max_chunks * (L->I / 16) : 0;
   F.split_part = o; o = up(o + sizeof(float) * 256 * F.ksplit * ntile);
@@ -179,7 +179,7 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
   } else {
     pa.tokc = 8;
     pa.mtiles_gu = static_cast<int>(L->I / 16);
-    pa.mtiles_dn = static_cast<int>(L->H / 16);
+    pa.mtiles_dn = static_cast<int>(L->H / 32);
     pa.ksplit_gu = F.ksplit;
     pa.chunk_list = reinterpret_cast<int4*>(base + F.chunk_list);
   }
@@ -201,6 +201,7 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     ra.logits = reinterpret_cast<float*>(base + F.r.partial);
     ra.ids = ids;
     ra.gates = gates;
+    ra.x_perm = F.tc ? nullptr : reinterpret_cast<__nv_bfloat16*>(base + F.xp);
     ra.grp = pa;
     ra.do_group = true;
     e = launch_route_small(ra, st);
@@ -251,8 +252,14 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     g.scales0 = static_cast<const __half*>(L->gate_scales);
     g.codes1 = L->up_codes;
     g.scales1 = static_cast<const __half*>(L->up_scales);
-    g.act = static_cast<const __nv_bfloat16*>(x);
-    g.perm = perm;
+    g.act = reinterpret_cast<const __nv_bfloat16*>(base + F.xp);
+    if (T <= kRouteSmallMaxT) {
+      g.perm = perm;  // x_perm rows are tokens
+    } else {
+      e = launch_gather_rows(x, perm, rows, L->H, base + F.xp, st);
+      if (e != cudaSuccess) return STRATA_ERR_CUDA;
+      g.perm = nullptr;  // xp rows are GEMM rows
+    }
     g.out = base + F.h;
     g.K = static_cast<int>(L->H);
     g.N = static_cast<int>(L->I);
