@@ -129,6 +129,34 @@ strata_status strata_route_topk(const void* x_bf16, const float* w_router, const
                                 strata_stream stream);
 
 /*
+ * strata_route_topk_noalloc — strata_route_topk without a workspace argument, for callers that
+ * may not allocate device memory when they call in: plugin interfaces whose enqueue step must not
+ * allocate, code running while a CUDA graph is being captured (cudaMalloc is not allowed then),
+ * processes whose device memory is all handed out up front by one custom allocator. The pages
+ * have no counterpart: this is an interface convenience, not part of the method.
+ *
+ * Scratch: a fixed array of STRATA_NOALLOC_SCRATCH_BYTES in the library's device globals. Every
+ * GPU that loads the library holds it until the process exits. Requests whose scratch would not
+ * fit (strata_route_workspace_size(T, E, k) > STRATA_NOALLOC_SCRATCH_BYTES) return
+ * STRATA_ERR_UNSUPPORTED before anything runs; everything else is identical to
+ * strata_route_topk (same arguments, outputs and checks). Nothing is allocated or freed, by the
+ * library or any routine it calls.
+ * Set-up: the first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current) and keeps it; make that first call before any stream capture.
+ * All calls share the one array: calls that overlap on the GPU (different streams, or several
+ * host threads) race and must be serialised by the caller. Each call clears the status header it
+ * needs before its kernels run; the rest of the array keeps the previous call's contents.
+ * Device status of the last call: strata_workspace_status is not available (no workspace
+ * pointer); data faults still never trap.
+ */
+#define STRATA_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB per device */
+strata_status strata_route_topk_noalloc(const void* x_bf16, const float* w_router,
+                                        const float* bias, int64_t T, int64_t H, int32_t E,
+                                        int32_t k, uint32_t flags, int32_t* ids, float* gates,
+                                        int32_t* counts, int32_t* offsets, int32_t* perm,
+                                        int32_t* inv, strata_stream stream);
+
+/*
  * One routed MoE FFN layer. Expert weights are the outputs of strata_quantize_groups, stacked
  * over experts; the shared expert, when has_shared != 0, is index E of each stack.
  * Expert e computes y = (silu(x Wg_e^T) * (x Wu_e^T)) Wd_e^T   ([glm-4090] §01: Gate/Up, Down).

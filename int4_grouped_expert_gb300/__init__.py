@@ -61,6 +61,8 @@ _SIGNATURES = {
     "strata_route_workspace_size": (_SZ, [_I64, _I32, _I32]),
     "strata_route_topk": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I32, _I32, _U32,
                                          _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "strata_route_topk_noalloc": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I32, _I32, _U32,
+                                                 _P, _P, _P, _P, _P, _P, _P]),
     "strata_moe_workspace_size": (_SZ, [ctypes.POINTER(strata_moe_layer), _I64]),
     "strata_moe_forward": (ctypes.c_int, [ctypes.POINTER(strata_moe_layer), _P, _I64, _P, _P, _SZ, _P]),
     "strata_moe_forward_ex": (ctypes.c_int, [ctypes.POINTER(strata_moe_layer), _P, _I64, _P,
@@ -143,6 +145,17 @@ def strata_route_topk(x, w_router, bias, T, H, E, k, flags, ids, gates, counts=N
     return lib().strata_route_topk(ptr(x), ptr(w_router), ptr(bias), T, H, E, k, flags, ptr(ids),
                                    ptr(gates), ptr(counts), ptr(offsets), ptr(perm), ptr(inv),
                                    ptr(workspace), ws_bytes, stream_handle(stream))
+
+
+def strata_route_topk_noalloc(x, w_router, bias, T, H, E, k, flags, ids, gates, counts=None,
+                              offsets=None, perm=None, inv=None, stream=None):
+    """strata_route_topk with the library's own fixed scratch (no workspace, no allocation)."""
+    return lib().strata_route_topk_noalloc(ptr(x), ptr(w_router), ptr(bias), T, H, E, k, flags,
+                                           ptr(ids), ptr(gates), ptr(counts), ptr(offsets),
+                                           ptr(perm), ptr(inv), stream_handle(stream))
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 def strata_moe_workspace_size(layer: strata_moe_layer, T_max: int) -> int:
