@@ -13,6 +13,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const __nv_bfloat16* __restrict__ x, int T,
                                                       int H, int k, int has_shared, int R,
                                                       int residual, __nv_bfloat16* __restrict__ out) {
+  griddep_wait();  // y comes from the down GEMM
   const int t = blockIdx.x;
   const int64_t H4 = H / 4;
   for (int64_t c = blockIdx.y * blockDim.x + threadIdx.x; c < H4; c += gridDim.y * blockDim.x) {
@@ -51,11 +52,10 @@ cudaError_t launch_combine(const float* y, const float* gates, const int* inv, c
   if (T == 0) return cudaSuccess;
   // one float4 of one token per thread: T x ceil(H / 1024) CTAs
   dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((H / 4 + 255) / 256));
-  combine_kernel<<<grid, 256, 0, stream>>>(
-      y, gates, inv, static_cast<const __nv_bfloat16*>(x), static_cast<int>(T),
-      static_cast<int>(H), k, has_shared, static_cast<int>(R), residual,
-      static_cast<__nv_bfloat16*>(out));
-  return cudaGetLastError();
+  return launch_kernel(combine_kernel, grid, dim3(256), 0, stream, true, y, gates, inv,
+                       static_cast<const __nv_bfloat16*>(x), static_cast<int>(T),
+                       static_cast<int>(H), k, has_shared, static_cast<int>(R), residual,
+                       static_cast<__nv_bfloat16*>(out));
 }
 
 }  // namespace strata

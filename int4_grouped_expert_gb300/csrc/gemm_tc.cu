@@ -33,6 +33,8 @@ constexpr int kTcBM = 128;       // weight rows per tile (MMA M)
 constexpr int kTcBK = 64;        // contraction per stage: one 128-byte swizzle row of bf16
 constexpr int kTcNMax = 256;     // token rows per tile (MMA N)
 constexpr int kTcThreads = 384;  // 12 warps
+constexpr int kTcBoxRows = 128;  // TMA box: 128 token rows x 64 columns (16 KB)
+constexpr int kTcBoxBytes = kTcBoxRows * kTcBK * 2;
 
 template <bool kGateUp>
 struct TcCfg {
@@ -76,9 +78,17 @@ __device__ __forceinline__ uint32_t codes_pair_bf16(uint32_t w, int i) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
+#ifndef STRATA_TC_SPLIT_SCALE
+#define STRATA_TC_SPLIT_SCALE 1  // 1: q*s rounded once (two-term scale); 0: q*bf16(s), two roundings
+#endif
 __device__ __forceinline__ uint32_t scale_pair(uint32_t q, __nv_bfloat162 hi, __nv_bfloat162 lo) {
   const __nv_bfloat162 qq = *reinterpret_cast<__nv_bfloat162*>(&q);
+#if STRATA_TC_SPLIT_SCALE
   const __nv_bfloat162 r = __hfma2(qq, hi, __hmul2(qq, lo));
+#else
+  const __nv_bfloat162 r = __hmul2(qq, hi);
+  (void)lo;
+#endif
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
@@ -140,12 +150,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         TcTile t;
         tc_decode(a, item, nseg, mtiles, t);
+        const int nbox = t.nmma > kTcBoxRows ? 2 : 1;  // only the rows the MMA reads
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % ST;
           const uint32_t ph = (it / ST) & 1;
           if (!tc::mbar_wait(empty + s, ph ^ 1, abort_flag, a.status)) { ok = false; break; }
-          tc::mbar_arrive_expect_tx(full_b + s, C::B_BYTES);
-          tc::tma_load_2d(B_of(s), &tmap_b, kb * kTcBK, t.row0, full_b + s);
+          tc::mbar_arrive_expect_tx(full_b + s, nbox * kTcBoxBytes);
+          for (int bx = 0; bx < nbox; ++bx)
+            tc::tma_load_2d(B_of(s) + bx * kTcBoxBytes, &tmap_b, kb * kTcBK,
+                            t.row0 + bx * kTcBoxRows, full_b + s);
         }
       }
       if (!ok)  // drain the copies that may still be in flight
@@ -218,48 +231,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint8_t* cp = codes + wrow * row_bytes + half * 16;
       const __half* sp = scales + wrow * srow;
       const uint32_t soff = (r >> 3) * 1024 + (r & 7) * 128;
-      // codes of the next stages stay in flight in registers (3 deep)
-      uint4 c0a, c0b, c1a, c1b, c2a, c2b;
+      // codes (and scales) of the next 4 stages stay in flight in fixed register slots: the loop
+      // is unrolled by 4 so slot u is refilled for stage kb + 4 right after stage kb used it
+      constexpr int PD = 4;
+      uint4 cA[PD], cB[PD];
+      float sc[PD / 2];  // scale of the group of stage kb (one per even stage)
       auto ld = [&](int kb, uint4& x0, uint4& x1) {
         if (kb < nk) {
           x0 = __ldg(reinterpret_cast<const uint4*>(cp + static_cast<int64_t>(kb) * 32));
           if (kGateUp) x1 = __ldg(reinterpret_cast<const uint4*>(cp + static_cast<int64_t>(kb) * 32 + 16));
         }
       };
-      ld(0, c0a, c0b);
-      ld(1, c1a, c1b);
-      ld(2, c2a, c2b);
-      __nv_bfloat162 s_hi, s_lo;
-      for (int kb = 0; kb < nk; ++kb, ++it) {
-        const int s = it % ST;
-        const uint32_t ph = (it / ST) & 1;
-        if ((kb & 1) == 0) {
-          const float sf = __half2float(sp[kb >> 1]);
-          const __nv_bfloat16 h = __float2bfloat16_rn(sf);
-          const __nv_bfloat16 l = __float2bfloat16_rn(sf - __bfloat162float(h));
-          s_hi = __halves2bfloat162(h, h);
-          s_lo = __halves2bfloat162(l, l);
-        }
-        const uint4 x0 = c0a, x1 = c0b;
-        c0a = c1a; c0b = c1b; c1a = c2a; c1b = c2b;
-        ld(kb + 3, c2a, c2b);
-        if (!tc::mbar_wait(empty + s, ph ^ 1, abort_flag, a.status)) { ok = false; break; }
-        uint8_t* dst = A_of(s, mat) + soff;
-        const uint32_t wds[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-        for (int j = 0; j < (kGateUp ? 8 : 4); ++j) {
-          const uint32_t w = wds[j];
-          uint4 o;
-          o.x = scale_pair(codes_pair_bf16(w, 0), s_hi, s_lo);
-          o.y = scale_pair(codes_pair_bf16(w, 1), s_hi, s_lo);
-          o.z = scale_pair(codes_pair_bf16(w, 2), s_hi, s_lo);
-          o.w = scale_pair(codes_pair_bf16(w, 3), s_hi, s_lo);
-          const int chunk = kGateUp ? j : (half * 4 + j);
-          *reinterpret_cast<uint4*>(dst + ((chunk ^ (r & 7)) << 4)) = o;
+      for (int u = 0; u < PD; ++u) {
+        ld(u, cA[u], cB[u]);
+        if ((u & 1) == 0 && u < nk) sc[u / 2] = __half2float(sp[u >> 1]);
+      }
+      for (int kb0 = 0; ok && kb0 < nk; kb0 += PD) {
+#pragma unroll
+        for (int u = 0; u < PD; ++u) {
+          const int kb = kb0 + u;
+          if (kb >= nk) break;
+          const int s = it % ST;
+          const uint32_t ph = (it / ST) & 1;
+          // scale of this stage's group as a bf16 pair split: s = s_hi + s_lo
+          const float sf = sc[u / 2];
+          const __nv_bfloat16 hb = __float2bfloat16_rn(sf);
+          const __nv_bfloat16 lb = __float2bfloat16_rn(sf - __bfloat162float(hb));
+          const __nv_bfloat162 s_hi = __halves2bfloat162(hb, hb);
+          const __nv_bfloat162 s_lo = __halves2bfloat162(lb, lb);
+          const uint4 x0 = cA[u], x1 = cB[u];
+          ld(kb + PD, cA[u], cB[u]);
+          if ((u & 1) == 1 && kb + PD - 1 < nk) sc[u / 2] = __half2float(sp[(kb + PD - 1) >> 1]);
+          if (!tc::mbar_wait(empty + s, ph ^ 1, abort_flag, a.status)) { ok = false; break; }
+          uint8_t* dst = A_of(s, mat) + soff;
+          const uint32_t wds[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+          for (int j = 0; j < (kGateUp ? 8 : 4); ++j) {
+            const uint32_t w = wds[j];
+            uint4 o;
+            o.x = scale_pair(codes_pair_bf16(w, 0), s_hi, s_lo);
+            o.y = scale_pair(codes_pair_bf16(w, 1), s_hi, s_lo);
+            o.z = scale_pair(codes_pair_bf16(w, 2), s_hi, s_lo);
+            o.w = scale_pair(codes_pair_bf16(w, 3), s_hi, s_lo);
+            const int chunk = kGateUp ? j : (half * 4 + j);
+            *reinterpret_cast<uint4*>(dst + ((chunk ^ (r & 7)) << 4)) = o;
+          }
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(full_a + s);
+          ++it;
         }
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(full_a + s);
       }
       if (!ok) break;
       // epilogue
@@ -353,13 +375,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
-// Row-major bf16 [rows, cols]: boxes of 256 rows x 64 columns, 128-byte swizzle, zero fill.
+// Row-major bf16 [rows, cols]: boxes of 128 rows x 64 columns, 128-byte swizzle, zero fill.
 static bool make_row_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {kTcBK, kTcNMax};
+  cuuint32_t box[2] = {kTcBK, kTcBoxRows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -81,6 +81,12 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 1) grouped_gemm_warp_kernel
   extern __shared__ uint4 smem_ring[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint4* ring = smem_ring + warp * kStages * kNC * 32 + lane;
+  // Gate/up reads the router's work lists: wait for it. Down reads h from gate/up, but its work
+  // lists come from the router (complete before gate/up started), so it streams its first item's
+  // weights before waiting (below).
+  if (kGateUp) griddep_wait();
+  griddep_launch();
+  bool first = true;
   const int gq = lane >> 2, t4 = lane & 3;
   int* const next_ctr = kGateUp ? &a.hdr->next_gu : &a.hdr->next_dn;
   const int n_items = kGateUp ? a.hdr->n_items_gu : a.hdr->n_items_dn;
@@ -97,6 +103,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 1) grouped_gemm_warp_kernel
   item = __shfl_sync(0xffffffffu, item, 0);
   int4 ch = make_int4(0, 0, 0, 0);
   if (item < n_items) ch = __ldg(a.chunk_list + item % nchunks);
+  if (!kGateUp && item >= n_items) griddep_wait();  // no work: still order the exit
   while (item < n_items) {
     int nxt = 0;
     if (lane == 0) nxt = atomicAdd(next_ctr, 1);  // next item, fetched while this one runs
@@ -124,16 +131,23 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 1) grouped_gemm_warp_kernel
     if (bvalid) src_row = a.perm ? a.perm[rbase + gq] : (rbase + gq);
     const char* Bp = reinterpret_cast<const char*>(a.act + src_row * a.K + t4 * 32);
 
-    auto issue = [&](int g, int slot) {
+    auto issue_a = [&](int g, int slot) {
       uint4* st = ring + slot * kNC * 32;
       const int64_t off = static_cast<int64_t>(g) * 64;
       cp_async16(st + 0 * 32, A0 + off, true);
       cp_async16(st + 1 * 32, A0 + off + 8 * row_bytes, true);
       cp_async16(st + 2 * 32, A1 + off, true);
       cp_async16(st + 3 * 32, A1 + off + 8 * row_bytes, true);
+    };
+    auto issue_b = [&](int g, int slot) {
+      uint4* st = ring + slot * kNC * 32;
       const char* b = Bp + static_cast<int64_t>(g) * 256;
 #pragma unroll
       for (int c = 0; c < 4; ++c) cp_async16(st + (4 + c) * 32, b + c * 16, bvalid);
+    };
+    auto issue = [&](int g, int slot) {
+      issue_a(g, slot);
+      issue_b(g, slot);
     };
     // scales of groups g .. g+kSD-1, rotating: [i][0..3] = rows gq, gq+8 of tile 0, then tile 1
     float sc[kSD][4];
@@ -147,11 +161,27 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 1) grouped_gemm_warp_kernel
     };
 #pragma unroll
     for (int i = 0; i < kSD; ++i) load_sc(gbeg + i, sc[i]);
+    if (!kGateUp && first) {
+      // down's first item: weights first, then wait for gate/up's h, then the activations
 #pragma unroll
-    for (int i = 0; i < kStages - 1; ++i) {
-      if (gbeg + i < gend) issue(gbeg + i, i);
+      for (int i = 0; i < kStages - 1; ++i) {
+        if (gbeg + i < gend) issue_a(gbeg + i, i);
+        cp_async_commit();
+      }
+      griddep_wait();
+#pragma unroll
+      for (int i = 0; i < kStages - 1; ++i)
+        if (gbeg + i < gend) issue_b(gbeg + i, i);
       cp_async_commit();
+      cp_async_wait<0>();
+    } else {
+#pragma unroll
+      for (int i = 0; i < kStages - 1; ++i) {
+        if (gbeg + i < gend) issue(gbeg + i, i);
+        cp_async_commit();
+      }
     }
+    first = false;
     int rd = 0, wr = kStages - 1;  // ring slots of the group read now / the group issued next
     float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
     int4 ch_next = ch;
@@ -298,8 +328,8 @@ cudaError_t launch_gemm_warp_t(const GemmArgs& a, int num_sms, cudaStream_t stre
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const Shifts sh{1u << 28, 1u << 24, 1u << 20};
-  grouped_gemm_warp_kernel<kGateUp><<<num_sms, kWarpsPerCta * 32, smem, stream>>>(a, sh);
-  return cudaGetLastError();
+  return launch_kernel(grouped_gemm_warp_kernel<kGateUp>, dim3(num_sms), dim3(kWarpsPerCta * 32),
+                       smem, stream, true, a, sh);
 }
 
 cudaError_t launch_gemm_warp(const GemmArgs& a, bool gate_up, int num_sms, cudaStream_t stream) {

@@ -19,28 +19,24 @@ namespace strata {
 __device__ __forceinline__ void quantize_one(const uint4& v, unsigned half_mask, int sub, int64_t g,
                                              uint32_t* __restrict__ codes,
                                              __half* __restrict__ scales, uint32_t* status) {
+  // |w| as fp16 bit patterns: their integer order is the order of the magnitudes, and any pattern
+  // at or above 0x7C00 is inf or nan, so one integer max gives both absmax and finiteness
+  const uint32_t m01 = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+  const uint32_t m23 = __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu);
+  const uint32_t m2 = __vmaxu2(m01, m23);
+  uint32_t mbits = max(m2 & 0xFFFFu, m2 >> 16);
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) mbits = max(mbits, __shfl_xor_sync(half_mask, mbits, o));
+  const bool finite = mbits < 0x7C00u;
+  const float amax = finite ? __half2float(__ushort_as_half(static_cast<unsigned short>(mbits))) : 0.f;
   const __half* h = reinterpret_cast<const __half*>(&v);
-  float f[8];
-  float amax = 0.0f;
-  bool finite = true;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    f[i] = __half2float(h[i]);
-    finite &= isfinite(f[i]);
-    amax = fmaxf(amax, fabsf(f[i]));
-  }
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) {
-    amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, o));
-    finite = __shfl_xor_sync(half_mask, finite ? 1 : 0, o) != 0 && finite;
-  }
   __half s_h = __float2half_rn(amax / 7.0f);
   const float s = __half2float(s_h);
   uint32_t packed = 0;
   if (finite && s > 0.0f) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      float q = rintf(f[i] / s);
+      float q = rintf(__half2float(h[i]) / s);
       q = fminf(fmaxf(q, -8.0f), 7.0f);
       packed |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xFu) << (4 * i);
     }

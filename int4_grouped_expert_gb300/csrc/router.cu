@@ -8,8 +8,9 @@
 // counter) runs softmax and top-k for every token and then groups the routed rows
 // (group_rows.cuh).
 //
-// Large batches: router_logits_kernel (fp32 tile GEMM, 32-term chunks joined by compensated
-// addition), router_topk_kernel (one warp per token), then the permute kernel.
+// Large batches: router_logits_tc_kernel (tensor cores, exact three-way bf16 split of the fp32
+// router, compensated accumulation), router_topk_kernel (one warp per token), then the permute
+// kernel.
 //
 // Top-k order: descending logit, ties to the lower expert id; gates = softmax probabilities of the
 // chosen experts (fp32, expf), renormalised over the k only with STRATA_RENORM.
@@ -19,44 +20,55 @@ namespace strata {
 
 // ----------------------------------------------------------------------------- shared pieces
 
-// Softmax + top-k of one token whose E logits sit in shared memory (one warp).
+// Order-preserving map of a float to uint32 (larger float -> larger key; -0 folded into +0).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  const uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Softmax + top-k of one token whose E (<= 1024) logits sit in shared memory (one warp). Every
+// lane keeps the keys of its experts e = lane + 32 i in registers; each of the k rounds takes the
+// warp-wide largest key with one redux.sync, breaks ties towards the lowest expert id with a second
+// one, and only the winning lane rescans its own keys.
 __device__ void warp_softmax_topk(const float* lg, int E, int k, uint32_t flags, int* ids,
                                   float* gates) {
   const int lane = threadIdx.x & 31;
-  float mx = -INFINITY;
-  for (int e = lane; e < E; e += 32) mx = fmaxf(mx, lg[e]);
+  uint32_t key[32];
+  uint32_t bk = 0;  // the lane's best key and its slot (lowest slot on equal keys)
+  int bi = 0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  for (int i = 0; i < 32; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = e < E ? float_key(lg[e]) : 0u;
+    if (key[i] > bk) { bk = key[i]; bi = i; }
+  }
+  const float mx = key_float(__reduce_max_sync(0xffffffffu, bk));
   float sum = 0.f;
   for (int e = lane; e < E; e += 32) sum += expf(lg[e] - mx);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
 
-  uint32_t taken = 0;  // bit i: expert lane + 32*i already chosen
-  float gsum = 0.f;
-  float my_g = 0.f;    // lane j keeps the j-th gate
+  float gsum = 0.f, my_g = 0.f;
   int my_i = 0;
   for (int j = 0; j < k; ++j) {
-    float best = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int e = lane, i = 0; e < E; e += 32, ++i) {
-      if (taken & (1u << i)) continue;
-      const float v = lg[e];
-      if (bi == 0x7fffffff || v > best) { best = v; bi = e; }  // e ascends: ties keep the lower id
-    }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t cand = (bk == m && bk != 0u) ? static_cast<uint32_t>(lane + 32 * bi) : 0xFFFFFFFFu;
+    const int eb = static_cast<int>(__reduce_min_sync(0xffffffffu, cand));
+    if (lane == (eb & 31)) {  // take it, then rescan this lane's remaining keys
+      bk = 0u;
+      bi = 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > best || (ov == best && oi < bi))) {
-        best = ov;
-        bi = oi;
+      for (int i = 0; i < 32; ++i) {
+        if (lane + 32 * i == eb) key[i] = 0u;
+        if (key[i] > bk) { bk = key[i]; bi = i; }
       }
     }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    const float g = expf(best - mx) / sum;
+    const float g = expf(key_float(m) - mx) / sum;
     gsum += g;
-    if (lane == j) { my_g = g; my_i = bi; }
+    if (lane == j) { my_g = g; my_i = eb; }
   }
   if (lane < k) {
     ids[lane] = my_i;
@@ -76,11 +88,20 @@ int route_small_epc(int E, int num_sms) {
 
 // dynamic shared memory of the last CTA (bytes): logits [8][E] floats, aliased by the grouping
 // scratch, then ids and gates [T*k]
-__host__ __device__ static size_t route_small_smem(int T, int E, int k) {
+__host__ __device__ static size_t route_small_lg_bytes(int T, int E) {
   size_t a = static_cast<size_t>(kRsWarps) * E * 4;
+  const size_t all = static_cast<size_t>(T) * E * 4;  // every token's logits, when it fits
+  if (all > a && all <= 96 * 1024) a = all;
+  return a;
+}
+// ids and gates follow both the logits and the grouping scratch (which alias each other)
+__host__ __device__ static size_t route_small_ids_off(int T, int E) {
+  size_t a = route_small_lg_bytes(T, E);
   const size_t g = group_smem_ints(kRsWarps, E) * 4;
-  if (g > a) a = g;
-  return a + static_cast<size_t>(T) * k * 8;
+  return g > a ? g : a;
+}
+__host__ __device__ static size_t route_small_smem(int T, int E, int k) {
+  return route_small_ids_off(T, E) + static_cast<size_t>(T) * k * 8;
 }
 
 __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
@@ -89,6 +110,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   __shared__ int is_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = a.T, H = a.H, E = a.E;
+  griddep_launch();  // the gate/up GEMM may launch now; it waits for this grid before reading
   const int wpe = kRsWarps / a.epc;  // warps per expert
   const int slot = warp / wpe, part = warp - slot * wpe;
   const int e = blockIdx.x * a.epc + slot;
@@ -112,12 +134,13 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   const int vb = part * nvec / wpe, ve = (part + 1) * nvec / wpe;
   const float4* wrow = reinterpret_cast<const float4*>(a.wr + static_cast<int64_t>(e < E ? e : 0) * H);
   const uint4* xv = reinterpret_cast<const uint4*>(a.x);
-  for (int t0 = 0; t0 < T; t0 += 4) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  constexpr int TB = 8;  // tokens per pass: every load of a pass is in flight together
+  for (int t0 = 0; t0 < T; t0 += TB) {
+    float acc[TB] = {};
     if (e < E) {
       for (int v0 = vb + lane; v0 < ve; v0 += 128) {
         float4 w[4][2];
-        uint4 xr[4][4];
+        uint4 xr[TB][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int v = v0 + 32 * i;
@@ -125,7 +148,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
             w[i][0] = __ldg(wrow + 2 * v);
             w[i][1] = __ldg(wrow + 2 * v + 1);
 #pragma unroll
-            for (int tt = 0; tt < 4; ++tt)
+            for (int tt = 0; tt < TB; ++tt)
               if (t0 + tt < T) xr[tt][i] = __ldg(xv + static_cast<int64_t>(t0 + tt) * nvec + v);
           }
         }
@@ -135,7 +158,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
           const float wf[8] = {w[i][0].x, w[i][0].y, w[i][0].z, w[i][0].w,
                                w[i][1].x, w[i][1].y, w[i][1].z, w[i][1].w};
 #pragma unroll
-          for (int tt = 0; tt < 4; ++tt) {
+          for (int tt = 0; tt < TB; ++tt) {
             if (t0 + tt >= T) continue;
             const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&xr[tt][i]);
 #pragma unroll
@@ -149,7 +172,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
       }
     }
 #pragma unroll
-    for (int tt = 0; tt < 4; ++tt) {
+    for (int tt = 0; tt < TB; ++tt) {
       float v = acc[tt];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -179,17 +202,26 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   if (!is_last) return;
   __threadfence();
 
-  const size_t lg_bytes = route_small_smem(0, E, 0);
+  const size_t lg_bytes = route_small_lg_bytes(T, E);
   float* lg = reinterpret_cast<float*>(rs_smem);  // [8 warps][E]
-  int* s_ids = reinterpret_cast<int*>(rs_smem + lg_bytes);
+  int* s_ids = reinterpret_cast<int*>(rs_smem + route_small_ids_off(T, E));
   float* s_gates = reinterpret_cast<float*>(s_ids + T * a.k);
-  for (int t = warp; t < T; t += kRsWarps) {
-    float* l = lg + warp * E;
-#pragma unroll 4
-    for (int e2 = lane; e2 < E; e2 += 32) l[e2] = __ldcg(a.logits + static_cast<int64_t>(t) * E + e2);
-    __syncwarp();
-    warp_softmax_topk(l, E, a.k, a.flags, s_ids + t * a.k, s_gates + t * a.k);
-    __syncwarp();
+  if (static_cast<size_t>(T) * E * 4 <= lg_bytes) {
+    // every token's logits in one coalesced sweep by the whole CTA, then one token per warp
+#pragma unroll 16
+    for (int i = threadIdx.x; i < T * E; i += blockDim.x) lg[i] = __ldcg(a.logits + i);
+    __syncthreads();
+    for (int t = warp; t < T; t += kRsWarps)
+      warp_softmax_topk(lg + t * E, E, a.k, a.flags, s_ids + t * a.k, s_gates + t * a.k);
+  } else {
+    for (int t = warp; t < T; t += kRsWarps) {
+      float* l = lg + warp * E;
+#pragma unroll 8
+      for (int e2 = lane; e2 < E; e2 += 32) l[e2] = __ldcg(a.logits + static_cast<int64_t>(t) * E + e2);
+      __syncwarp();
+      warp_softmax_topk(l, E, a.k, a.flags, s_ids + t * a.k, s_gates + t * a.k);
+      __syncwarp();
+    }
   }
   __syncthreads();
   for (int i = threadIdx.x; i < T * a.k; i += blockDim.x) {
@@ -300,6 +332,131 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16*
   }
 }
 
+// Large batches on tensor cores: logits = x Wr^T with Wr split exactly into three bf16 parts
+// (hi + mid + lo == the fp32 value), so every product x*part is exact and the mma.sync fp32
+// accumulation matches an fp32 GEMM. Tile 64 tokens x 64 experts, 8 warps (2 x 4), warp tile
+// 32 x 16; contraction staged 32 columns at a time (double-buffered cp.async for x, registers for
+// the fp32 router tile, split on the way into shared memory); every 256 columns the chunk sum joins
+// the running total with compensated (Kahan) addition. Split along H (blockIdx.z) like the SIMT
+// kernel so that small grids still fill the GPU.
+constexpr int kRtT = 64, kRtE = 64, kRtK = 32, kRtPad = 40;  // shared rows padded to 80 bytes
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+__device__ __forceinline__ void ldmatrix_x2(uint32_t (&r)[2], const void* p) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1]) : "r"(a));
+}
+
+__global__ void __launch_bounds__(256) router_logits_tc_kernel(const __nv_bfloat16* __restrict__ x,
+                                                               const float* __restrict__ wr, int T,
+                                                               int H, int E, int h_per_split,
+                                                               float* __restrict__ partial) {
+  __shared__ __align__(16) __nv_bfloat16 xs[2][kRtT][kRtPad];
+  __shared__ __align__(16) __nv_bfloat16 ws[3][kRtE][kRtPad];  // hi, mid, lo
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int e0 = blockIdx.x * kRtE, t0 = blockIdx.y * kRtT;
+  const int hbeg = blockIdx.z * h_per_split;
+  const int hend = min(H, hbeg + h_per_split);
+  const int wt = (warp >> 2) * 32;  // warp's token offset in the tile
+  const int we = (warp & 3) * 16;   // warp's expert offset
+  float acc[2][2][4] = {}, comp[2][2][4] = {}, part[2][2][4] = {};
+
+  // x tile: 64 rows x 32 bf16 = 256 x 16 bytes, one cp.async per thread
+  const int xr = tid >> 2, xc = (tid & 3) * 8;
+  const bool xok = t0 + xr < T;
+  const __nv_bfloat16* xsrc = x + static_cast<int64_t>(xok ? t0 + xr : 0) * H + xc;
+  // router tile: 64 experts x 32 fp32 = 8 floats per thread
+  const int wrr = tid >> 2, wc = (tid & 3) * 8;
+  const bool wok = e0 + wrr < E;
+  const float* wsrc = wr + static_cast<int64_t>(wok ? e0 + wrr : 0) * H + wc;
+
+  auto stage_x = [&](int buf, int hc) { cp_async16(&xs[buf][xr][xc], xsrc + hc, xok); };
+  auto stage_w = [&](int hc) {
+    float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (wok) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(wsrc + hc));
+      const float4 b = __ldg(reinterpret_cast<const float4*>(wsrc + hc) + 1);
+      f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
+    __nv_bfloat16 hi[8], mid[8], lo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {  // f = hi + mid + lo exactly (24 = 8 + 8 + 8 significant bits)
+      hi[i] = __float2bfloat16_rn(f[i]);
+      const float r1 = f[i] - __bfloat162float(hi[i]);
+      mid[i] = __float2bfloat16_rn(r1);
+      lo[i] = __float2bfloat16_rn(r1 - __bfloat162float(mid[i]));
+    }
+    *reinterpret_cast<uint4*>(&ws[0][wrr][wc]) = *reinterpret_cast<uint4*>(hi);
+    *reinterpret_cast<uint4*>(&ws[1][wrr][wc]) = *reinterpret_cast<uint4*>(mid);
+    *reinterpret_cast<uint4*>(&ws[2][wrr][wc]) = *reinterpret_cast<uint4*>(lo);
+  };
+
+  int buf = 0;
+  if (hbeg < hend) stage_x(0, hbeg);
+  cp_async_commit();
+  int chunk_cols = 0;
+  for (int hc = hbeg; hc < hend; hc += kRtK) {
+    if (hc + kRtK < hend) stage_x(buf ^ 1, hc + kRtK);
+    cp_async_commit();
+    stage_w(hc);
+    cp_async_wait<1>();
+    __syncthreads();
+#pragma unroll
+    for (int ks = 0; ks < kRtK; ks += 16) {
+      uint32_t a[2][4];
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+        ldmatrix_x4(a[mi], &xs[buf][wt + mi * 16 + (lane & 15)][ks + (lane >> 4) * 8]);
+#pragma unroll
+      for (int sp = 0; sp < 3; ++sp) {
+#pragma unroll
+        for (int ni = 0; ni < 2; ++ni) {
+          uint32_t b[2];
+          ldmatrix_x2(b, &ws[sp][we + ni * 8 + (lane & 7)][ks + ((lane >> 3) & 1) * 8]);
+#pragma unroll
+          for (int mi = 0; mi < 2; ++mi) mma_bf16_16816(part[mi][ni], a[mi], b[0], b[1], part[mi][ni]);
+        }
+      }
+    }
+    chunk_cols += kRtK;
+    if (chunk_cols == 256 || hc + kRtK >= hend) {  // join the running total (compensated)
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int ni = 0; ni < 2; ++ni)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float y = part[mi][ni][c] - comp[mi][ni][c];
+            const float t = acc[mi][ni][c] + y;
+            comp[mi][ni][c] = (t - acc[mi][ni][c]) - y;
+            acc[mi][ni][c] = t;
+            part[mi][ni][c] = 0.f;
+          }
+      chunk_cols = 0;
+    }
+    __syncthreads();
+    buf ^= 1;
+  }
+  cp_async_wait<0>();
+  // C fragment: rows (tokens) lane/4 and lane/4 + 8, columns (experts) 2*(lane%4) + {0,1}
+  float* out = partial + static_cast<int64_t>(blockIdx.z) * T * E;
+#pragma unroll
+  for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+    for (int ni = 0; ni < 2; ++ni)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int t = t0 + wt + mi * 16 + (lane >> 2) + (c >= 2 ? 8 : 0);
+        const int e = e0 + we + ni * 8 + 2 * (lane & 3) + (c & 1);
+        if (t < T && e < E) out[static_cast<int64_t>(t) * E + e] = acc[mi][ni][c];
+      }
+}
+
 // One warp per token; the split partials are summed in split order.
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ partial,
                                                           int nsplit, const float* __restrict__ bias,
@@ -323,8 +480,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 }
 
 int router_num_splits(int64_t T, int64_t H, int E, int num_sms) {
-  const int64_t tiles = ((E + kRouterBE - 1) / kRouterBE) * ((T + kRouterBT - 1) / kRouterBT);
-  int64_t want = (2 * num_sms + tiles - 1) / tiles;  // ~2 CTAs per SM
+  const int64_t tiles = ((E + kRtE - 1) / kRtE) * ((T + kRtT - 1) / kRtT);
+  int64_t want = (num_sms + tiles - 1) / tiles;  // about one CTA per SM
   const int64_t max_split = H / 128;
   if (want > max_split) want = max_split;
   if (want > 16) want = 16;
@@ -341,11 +498,10 @@ cudaError_t launch_router(const void* x, const float* wr, const float* bias, int
   const int64_t gps = (groups + nsplit - 1) / nsplit;
   const int h_per_split = static_cast<int>(gps * 128);
   const int used = static_cast<int>((groups + gps - 1) / gps);
-  dim3 grid((E + kRouterBE - 1) / kRouterBE, static_cast<unsigned>((T + kRouterBT - 1) / kRouterBT),
-            used);
-  router_logits_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), wr,
-                                                 static_cast<int>(T), static_cast<int>(H), E,
-                                                 h_per_split, partial);
+  dim3 grid((E + kRtE - 1) / kRtE, static_cast<unsigned>((T + kRtT - 1) / kRtT), used);
+  router_logits_tc_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), wr,
+                                                    static_cast<int>(T), static_cast<int>(H), E,
+                                                    h_per_split, partial);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const size_t smem = static_cast<size_t>(8) * E * sizeof(float);
