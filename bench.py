@@ -286,6 +286,13 @@ def cpu_baseline(wl, xs_host, T, budget_s=20.0):
                       f"{wl.k} routed experts and the shared one; experts pre-quantized"}
 
 
+def kernels_per_forward(T):
+    """Kernels one strata_moe_forward launches (the workspace-header memset not counted): up to
+    64 tokens the one-launch router (logits, softmax, top-k, grouping) + gate/up + down + combine;
+    above, router logits + top-k + grouping + row gather + gate/up + down + combine."""
+    return 4 if T <= 64 else 7
+
+
 def peak_numbers():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -378,7 +385,7 @@ def run_strata(args):
         "stages_us": {k: v * 1e3 for k, v in stages.items()},
         "sweep": sweep,
         "e2e": e2e,
-        "gpu_launches": 6 * args.steps,
+        "gpu_launches": kernels_per_forward(T) * args.steps,
         "clocks": clk,
     }
     if rank == 0:
@@ -486,7 +493,104 @@ def run_prefill(args):
                         "traffic": None},
            "layer_tflops": layer_tf, "layer_frac": layer_tf / peak_tf, "down_tflops": dn_tf,
            "stages_us": {k: v * 1e3 for k, v in stages.items()}, "quantize": quant,
-           "gpu_launches": None, "clocks": clk}
+           "gpu_launches": kernels_per_forward(T) * steps, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(rec), flush=True)
+
+
+def run_stack(args):
+    """The 8-layer decode stack (hidden 4096, expert inter 2048, 128 experts top-4 + shared, a
+    Zipf router per layer, residual add between layers) through strata_moe_stack_forward, for
+    batches of 1/4/8/16/32 tokens: stack and per-layer tokens/s."""
+    import torch
+    import int4_grouped_expert_gb300 as st
+    from int4_grouped_expert_gb300 import MoELayer
+    ws_n, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    st.lib()
+    wl = CONFIGS["c4"]
+    # layer 0's experts are generated and quantized on the device; every other layer gets its own
+    # copy of those values at its own addresses (the same bytes stream from HBM) and its own router
+    L0 = build_layer(wl)
+    layers = [L0]
+    for l in range(1, wl.layers):
+        L = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared, flags=st.STRATA_ADD_RESIDUAL)
+        L.set_router(gen.router_weight(wl, l), gen.router_bias(wl, l))
+        L.copy_expert_from(L0)
+        layers.append(L)
+    L0.flags |= st.STRATA_ADD_RESIDUAL
+    structs = [L.struct() for L in layers]
+    stream = torch.cuda.Stream()
+    eb = wl.expert_bytes()
+    sweep = {}
+    clocks = ClockSampler(local)
+    head = args.tokens or max(wl.batches)
+    for T in ((args.tokens,) if args.tokens else wl.batches):
+        xs_host, xs_dev = token_batches(wl, T, N_TOKEN_BATCHES)
+        need = st.strata_moe_stack_workspace_size(structs, T)
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        out = torch.empty(T, wl.H, dtype=torch.bfloat16, device="cuda")
+        # distinct experts each layer streams: route the layer-by-layer activations
+        n_exp = []
+        cur = xs_dev[0]
+        for L in layers:
+            nxt = torch.empty_like(cur)
+            counts = torch.zeros(wl.E, dtype=torch.int32, device="cuda")
+            wsl = torch.empty(L.workspace_size(T), dtype=torch.uint8, device="cuda")
+            st.check(st.strata_moe_forward_ex(L.struct(), cur, T, nxt, counts=counts,
+                                              workspace=wsl, ws_bytes=wsl.numel()), "forward_ex")
+            n_exp.append(int((counts.cpu().numpy() > 0).sum()) + wl.shared)
+            cur = nxt
+        steps = args.steps
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                st.check(st.strata_moe_stack_forward(structs, xs_dev[i % N_TOKEN_BATCHES], T, out,
+                                                     ws, need, stream), "stack")
+            torch.cuda.synchronize()
+            barrier()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.nvtx.range_push("timed")
+            e0.record(stream)
+            for i in range(steps):
+                rc = st.strata_moe_stack_forward(structs, xs_dev[i % N_TOKEN_BATCHES], T, out, ws,
+                                                 need, stream)
+                if rc:
+                    st.check(rc, "stack")
+            e1.record(stream)
+            torch.cuda.nvtx.range_pop()
+            torch.cuda.synchronize()
+            barrier()
+        ms = max_over_ranks(e0.elapsed_time(e1)) / steps
+        # per-stage times of single layers (events between the kernels), same inputs and layers
+        wsl = torch.empty(max(L.workspace_size(T) for L in layers), dtype=torch.uint8, device="cuda")
+        _, stages = time_steps(layers, xs_dev, T, min(steps, 400), args.warmup, stream, wsl,
+                               wsl.numel(), out, profiled=True)
+        st_bytes = float(sum(n_exp)) * eb
+        sweep[str(T)] = {"stack_tokens_per_s": aggregate_throughput(T * steps, ms * steps / 1e3, ws_n),
+                         "layer_tokens_per_s": T / (ms / wl.layers / 1e3),
+                         "us_per_stack": ms * 1e3, "us_per_layer": ms * 1e3 / wl.layers,
+                         "experts_per_layer": float(np.mean(n_exp)),
+                         "hbm_gbs": st_bytes / (ms / 1e3) / 1e9, "steps": steps,
+                         "stages_us": {k: v * 1e3 for k, v in stages.items()}}
+    clk = clocks.stop()
+    peak, peak_kind = peak_numbers()
+    h = sweep[str(head)]
+    rec = {"metric": "MoE stack tokens/s (decode, 8 layers)", "value": h["stack_tokens_per_s"],
+           "unit": "tokens/s", "n_gpus": ws_n, "steps": h["steps"], "warmup": args.warmup,
+           "ms_per_step": h["us_per_stack"] / 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": wl.name, "tokens_per_step": head, "layers": wl.layers,
+                      "weights": "layer 0's int4 g128 experts (quantized on device) copied into "
+                                 "each layer's own storage; per-layer Zipf routers",
+                      "l2": f"each step streams {wl.layers} layers' experts (GBs) > L2"},
+           "roofline": {"kernel": "whole stack (all kernels)", "bound": "hbm",
+                        "achieved": h["hbm_gbs"], "peak": peak, "unit": "GB/s",
+                        "frac": h["hbm_gbs"] / peak, "peak_kind": peak_kind, "traffic": None},
+           "sweep": sweep, "gpu_launches": kernels_per_forward(head) * wl.layers * h["steps"],
+           "clocks": clk}
     if rank == 0:
         print(json.dumps(rec), flush=True)
 
@@ -558,11 +662,13 @@ def main(argv=None):
     p.add_argument("--impl", choices=["strata", "reference"], default="strata")
     p.add_argument("--ref-tokens", type=int, default=1)
     p.add_argument("--ref-budget-s", type=float, default=240.0)
-    p.add_argument("--workload", choices=["c2", "c3", "c5"], default="c2",
-                   help="c2: the decode layer (default, the headline); c3 / c5: prefill layers")
+    p.add_argument("--workload", choices=["c2", "c3", "c4", "c5"], default="c2",
+                   help="c2: the decode layer (default, the headline); c3 / c5: prefill layers; "
+                        "c4: the 8-layer decode stack")
     p.add_argument("--router", choices=["uniform", "zipf"], default=None)
     p.add_argument("--experts", type=int, default=0, help="prefill: override the routed expert count")
-    p.add_argument("--tokens", type=int, default=0, help="prefill: override the batch")
+    p.add_argument("--tokens", type=int, default=0,
+                   help="prefill: override the batch; c4: run this batch only")
     args = p.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -570,6 +676,10 @@ def main(argv=None):
         args.steps = 10 if args.impl == "reference" else 5000
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "c4":
+        if args.steps == 5000:
+            args.steps = 500
+        run_stack(args)
     elif args.workload != "c2":
         if args.steps == 5000:
             args.steps = 50

@@ -190,6 +190,24 @@ strata_status strata_moe_forward(const strata_moe_layer* layer, const void* x_bf
                                  strata_stream stream);
 
 /*
+ * strata_moe_stack_forward — n_layers MoE layers in sequence with a residual add between them:
+ *   x_0 = x,  x_{l+1} = bf16(x_l + MoE_l(x_l)),  out = x_{n_layers}
+ * (each layer as strata_moe_forward with STRATA_ADD_RESIDUAL; no normalisation is applied, none
+ * being named for the stack). layers: host array of n_layers descriptors (1..256), all with the
+ * same H. x_bf16, out_bf16: [T,H] bf16, device, distinct. workspace >=
+ * strata_moe_stack_workspace_size (device, 256-byte aligned, caller-owned; it also holds the two
+ * intermediate activation buffers). The device status word at the workspace start collects the
+ * STRATA_DEV_* bits of every layer (strata_workspace_status reads it after the stack). Errors:
+ * as strata_moe_forward, checked for every layer before the first launch; STRATA_ERR_SHAPE when
+ * the layers' H differ.
+ */
+size_t strata_moe_stack_workspace_size(const strata_moe_layer* layers, int32_t n_layers,
+                                       int64_t T_max);
+strata_status strata_moe_stack_forward(const strata_moe_layer* layers, int32_t n_layers,
+                                       const void* x_bf16, int64_t T, void* out_bf16,
+                                       void* workspace, size_t ws_bytes, strata_stream stream);
+
+/*
  * strata_moe_forward_ex — strata_moe_forward that also copies the routing out (each pointer
  * optional, device): ids [T,k], gates [T,k], counts [E], offsets [E+1], perm [T*k], inv [T,k],
  * with the meanings of strata_route_topk.

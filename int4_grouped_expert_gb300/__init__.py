@@ -69,6 +69,9 @@ _SIGNATURES = {
                                              _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "strata_moe_forward_profiled": (ctypes.c_int, [ctypes.POINTER(strata_moe_layer), _P, _I64, _P, _P,
                                                    _SZ, _P, ctypes.POINTER(_P), _I32]),
+    "strata_moe_stack_workspace_size": (_SZ, [ctypes.POINTER(strata_moe_layer), _I32, _I64]),
+    "strata_moe_stack_forward": (ctypes.c_int, [ctypes.POINTER(strata_moe_layer), _I32, _P, _I64,
+                                                _P, _P, _SZ, _P]),
     "strata_moe_host_staging_size": (_SZ, [ctypes.POINTER(strata_moe_layer), _I64]),
     "strata_moe_forward_host": (ctypes.c_int, [ctypes.POINTER(strata_moe_layer), _P, _I64, _P, _P,
                                                _SZ, _P]),
@@ -181,6 +184,23 @@ def strata_moe_forward_profiled(layer, x, T, out, workspace, ws_bytes, events, s
     return lib().strata_moe_forward_profiled(ctypes.byref(layer), ptr(x), T, ptr(out),
                                              ptr(workspace), ws_bytes, stream_handle(stream),
                                              handles, len(events))
+
+
+def layer_array(structs):
+    """A C array of strata_moe_layer from a list of descriptors."""
+    arr = (strata_moe_layer * len(structs))(*structs)
+    return arr
+
+
+def strata_moe_stack_workspace_size(layers, T_max) -> int:
+    arr = layers if not isinstance(layers, list) else layer_array(layers)
+    return lib().strata_moe_stack_workspace_size(arr, len(arr), T_max)
+
+
+def strata_moe_stack_forward(layers, x, T, out, workspace, ws_bytes, stream=None):
+    arr = layers if not isinstance(layers, list) else layer_array(layers)
+    return lib().strata_moe_stack_forward(arr, len(arr), ptr(x), T, ptr(out), ptr(workspace),
+                                          ws_bytes, stream_handle(stream))
 
 
 def strata_moe_host_staging_size(layer, T_max) -> int:

@@ -149,14 +149,17 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 1) grouped_gemm_warp_kernel
       issue_a(g, slot);
       issue_b(g, slot);
     };
-    // scales of groups g .. g+kSD-1, rotating: [i][0..3] = rows gq, gq+8 of tile 0, then tile 1
-    float sc[kSD][4];
-    auto load_sc = [&](int g, float (&d)[4]) {
+    // scales of groups g .. g+kSD-1 in fixed slots, kept as raw fp16 bits until used (converting
+    // on load would make every load complete at once): [i] = rows gq, gq+8 of tile 0, then tile 1
+    uint32_t sc[kSD][2];
+    auto load_sc = [&](int g, uint32_t (&d)[2]) {
       if (g < gend) {
-        d[0] = __half2float(S0[g]);
-        d[1] = __half2float(S0[8 * srow + g]);
-        d[2] = __half2float(S1[g]);
-        d[3] = __half2float(S1[8 * srow + g]);
+        const unsigned short a0 = __ldg(reinterpret_cast<const unsigned short*>(S0) + g);
+        const unsigned short a1 = __ldg(reinterpret_cast<const unsigned short*>(S0) + 8 * srow + g);
+        const unsigned short b0 = __ldg(reinterpret_cast<const unsigned short*>(S1) + g);
+        const unsigned short b1 = __ldg(reinterpret_cast<const unsigned short*>(S1) + 8 * srow + g);
+        d[0] = static_cast<uint32_t>(a0) | (static_cast<uint32_t>(a1) << 16);
+        d[1] = static_cast<uint32_t>(b0) | (static_cast<uint32_t>(b1) << 16);
       }
     };
 #pragma unroll
@@ -242,10 +245,12 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 1) grouped_gemm_warp_kernel
           q0[c] = (p0[0][c] - cr[0][c]) + (p0[1][c] - cr[1][c]);
           q1[c] = (p1[0][c] - cr[0][c]) + (p1[1][c] - cr[1][c]);
         }
-        acc0[0] = fmaf(sc[u][0], q0[0], acc0[0]); acc0[1] = fmaf(sc[u][0], q0[1], acc0[1]);
-        acc0[2] = fmaf(sc[u][1], q0[2], acc0[2]); acc0[3] = fmaf(sc[u][1], q0[3], acc0[3]);
-        acc1[0] = fmaf(sc[u][2], q1[0], acc1[0]); acc1[1] = fmaf(sc[u][2], q1[1], acc1[1]);
-        acc1[2] = fmaf(sc[u][3], q1[2], acc1[2]); acc1[3] = fmaf(sc[u][3], q1[3], acc1[3]);
+        const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(&sc[u][0]));
+        const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(&sc[u][1]));
+        acc0[0] = fmaf(s0.x, q0[0], acc0[0]); acc0[1] = fmaf(s0.x, q0[1], acc0[1]);
+        acc0[2] = fmaf(s0.y, q0[2], acc0[2]); acc0[3] = fmaf(s0.y, q0[3], acc0[3]);
+        acc1[0] = fmaf(s1.x, q1[0], acc1[0]); acc1[1] = fmaf(s1.x, q1[1], acc1[1]);
+        acc1[2] = fmaf(s1.y, q1[2], acc1[2]); acc1[3] = fmaf(s1.y, q1[3], acc1[3]);
         load_sc(g + kSD, sc[u]);
         __syncwarp();
         if (g + kStages - 1 < gend) issue(g + kStages - 1, wr);

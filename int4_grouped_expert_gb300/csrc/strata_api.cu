@@ -122,7 +122,7 @@ struct Taps {
 
 static strata_status run_forward(const strata_moe_layer* L, const void* x, int64_t T, void* out,
                                  const Taps* taps, void* ws, size_t ws_bytes, cudaStream_t st,
-                                 void* const* events = nullptr) {
+                                 void* const* events = nullptr, bool keep_status = false) {
   auto mark = [&](int i) -> bool {
     if (!events || !events[i]) return true;
     return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
@@ -152,7 +152,11 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
   int* inv = reinterpret_cast<int*>(base + F.r.inv);
 
   if (!mark(0)) return STRATA_ERR_CUDA;
-  cudaError_t e = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st);
+  // keep_status: a later layer of a stack clears the counters but keeps the status word, so a
+  // fault flagged by any layer stays visible after the whole stack
+  const size_t clear_from = keep_status ? sizeof(hdr->status) : 0;
+  cudaError_t e = cudaMemsetAsync(reinterpret_cast<char*>(hdr) + clear_from, 0,
+                                  sizeof(WsHeader) - clear_from, st);
   if (e != cudaSuccess) return STRATA_ERR_CUDA;
 
   PermuteArgs pa{};
@@ -428,6 +432,54 @@ strata_status strata_moe_forward_profiled(const strata_moe_layer* layer, const v
   if (!events || n_events != STRATA_PROFILE_EVENTS) return STRATA_ERR_INVALID_ARG;
   return run_forward(layer, x_bf16, T, out_bf16, nullptr, workspace, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream), events);
+}
+
+size_t strata_moe_stack_workspace_size(const strata_moe_layer* layers, int32_t n_layers,
+                                       int64_t T_max) {
+  if (!layers || n_layers < 1 || n_layers > 256 || T_max < 0 || T_max > kMaxTokens) return 0;
+  size_t ws = 0;
+  for (int l = 0; l < n_layers; ++l) {
+    if (check_layer(&layers[l]) != STRATA_OK || layers[l].H != layers[0].H) return 0;
+    strata_moe_layer L = layers[l];
+    L.flags |= STRATA_ADD_RESIDUAL;
+    const size_t w = fwd_layout(&L, T_max).total;
+    if (w > ws) ws = w;
+  }
+  return ws + 2 * up(sizeof(uint16_t) * T_max * layers[0].H);  // two activation buffers
+}
+
+strata_status strata_moe_stack_forward(const strata_moe_layer* layers, int32_t n_layers,
+                                       const void* x_bf16, int64_t T, void* out_bf16,
+                                       void* workspace, size_t ws_bytes, strata_stream stream) {
+  if (!layers || n_layers < 1 || n_layers > 256) return STRATA_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l) {
+    const strata_status s = check_layer(&layers[l]);
+    if (s != STRATA_OK) return s;
+    if (layers[l].H != layers[0].H) return STRATA_ERR_SHAPE;
+  }
+  if (T < 0 || T > kMaxTokens) return STRATA_ERR_SHAPE;
+  if (T == 0) return STRATA_OK;
+  if (!x_bf16 || !out_bf16 || x_bf16 == out_bf16) return STRATA_ERR_INVALID_ARG;
+  if (!aligned(x_bf16, 16) || !aligned(out_bf16, 16)) return STRATA_ERR_INVALID_ARG;
+  const size_t need = strata_moe_stack_workspace_size(layers, n_layers, T);
+  if (!workspace || !aligned(workspace, kAlign)) return STRATA_ERR_WORKSPACE;
+  if (need == 0 || ws_bytes < need) return STRATA_ERR_WORKSPACE;
+  const size_t act = up(sizeof(uint16_t) * T * layers[0].H);
+  char* base = static_cast<char*>(workspace);
+  const size_t layer_ws = need - 2 * act;
+  void* buf[2] = {base + layer_ws, base + layer_ws + act};
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const void* cur = x_bf16;
+  for (int l = 0; l < n_layers; ++l) {
+    strata_moe_layer L = layers[l];
+    L.flags |= STRATA_ADD_RESIDUAL;
+    void* dst = (l == n_layers - 1) ? out_bf16 : buf[l & 1];
+    const strata_status s =
+        run_forward(&L, cur, T, dst, nullptr, workspace, layer_ws, st, nullptr, l > 0);
+    if (s != STRATA_OK) return s;
+    cur = dst;
+  }
+  return STRATA_OK;
 }
 
 size_t strata_moe_host_staging_size(const strata_moe_layer* layer, int64_t T_max) {

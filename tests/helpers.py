@@ -120,15 +120,23 @@ def compare_routing(gpu, ref_route, E):
     return diff, near
 
 
-def compare_output(out_bits, ref_out, rows=None):
+def compare_output(out_bits, ref_out, rows=None, scale_max_abs=False):
+    """Relative L2 and max-abs error of bf16 outputs against the oracle's fp64 outputs.
+
+    The max-abs bound is stated for N(0,1)-scale activations. With scale_max_abs it is multiplied
+    by max(1, rms of the reference): a residual stream with no normalisation grows layer after
+    layer, and the final bf16 rounding alone then errs by up to half an ulp of that magnitude."""
     o = gen.bf16_bits_to_f32(out_bits).astype(np.float64)
     if rows is not None:
         o, ref_out = o[rows], ref_out[rows]
     err = o - ref_out
     rel = np.linalg.norm(err) / max(np.linalg.norm(ref_out), 1e-30)
     mx = np.abs(err).max() if err.size else 0.0
+    tol = MAX_ABS_TOL
+    if scale_max_abs and ref_out.size:
+        tol *= max(1.0, float(np.sqrt(np.mean(ref_out ** 2))))
     assert rel <= REL_L2_TOL, f"relative L2 {rel:.3e}"
-    assert mx <= MAX_ABS_TOL, f"max abs {mx:.3e}"
+    assert mx <= tol, f"max abs {mx:.3e} > {tol:.3e}"
     return rel, mx
 
 

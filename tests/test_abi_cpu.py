@@ -114,3 +114,16 @@ def test_route_host_checks(st):
 def test_status_reads_reject_null(st):
     assert st.strata_read_status(None)[0] == 1
     assert st.strata_workspace_status(None)[0] == 4
+
+
+def test_stack_host_checks(st):
+    A = 1 << 12
+    Ls = [layer(st), layer(st)]
+    need = st.strata_moe_stack_workspace_size(Ls, 4)
+    one = st.strata_moe_workspace_size(layer(st, flags=2), 4)
+    assert need >= one + 2 * 4 * 4096 * 2
+    assert st.strata_moe_stack_workspace_size([layer(st), layer(st, H=2048)], 4) == 0
+    assert st.strata_moe_stack_forward([layer(st), layer(st, H=2048)], A, 4, 2 * A, A, need) == 2
+    assert st.strata_moe_stack_forward(Ls, A, 4, 2 * A, A, need - 1) == 4
+    assert st.strata_moe_stack_forward(Ls, A, 4, A, A, need) == 1
+    assert st.strata_moe_stack_forward(Ls, A, 0, 2 * A, A, need) == 0
