@@ -227,4 +227,147 @@ __device__ void group_rows(const PermuteArgs& a, const int* ids, GroupSmem sm) {
   }
 }
 
+// ----------------------------------------------------------------------------- small batches
+// The same grouping for the warp path when the routed rows are few (R = T*k <= 512), written for
+// the one CTA that runs it once per layer: every loop is rolled, so the code the CTA fetches stays
+// small. Rows are marked in a per-expert bitmask (atomicOr: order-free), a row's position is the
+// expert's offset plus the marked rows below it, and one scan over the experts yields offsets,
+// segment indices and chunk offsets together. Outputs are identical to group_rows.
+constexpr int kGroupSmallMaxR = 512;
+__host__ __device__ constexpr size_t group_small_ints(int NW, int E, int R) {
+  return static_cast<size_t>(E) * ((R + 31) / 32) + (E + 1) + 2 * (NW + 1) + 1;
+}
+
+// Exclusive block scan of a 64-bit value (blockDim.x = 32 * NW); scratch holds 2 * (NW + 1) ints.
+template <int NW>
+__device__ __forceinline__ unsigned long long block_scan_excl64(unsigned long long v, int* scratch,
+                                                                unsigned long long* total) {
+  unsigned long long* sc = reinterpret_cast<unsigned long long*>(scratch);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long inc = v;
+#pragma unroll 1
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) sc[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long w = lane < NW ? sc[lane] : 0ull;
+    unsigned long long winc = w;
+#pragma unroll 1
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long n = __shfl_up_sync(0xffffffffu, winc, o);
+      if (lane >= o) winc += n;
+    }
+    __syncwarp();
+    if (lane < NW) sc[lane] = winc - w;
+    if (lane == 31) sc[NW] = winc;
+  }
+  __syncthreads();
+  const unsigned long long res = sc[warp] + inc - v;
+  *total = sc[NW];
+  return res;
+}
+
+// ids: the [T, k] ids in shared memory; smem: group_small_ints(NW, E, T*k) ints, 8-byte aligned.
+template <int NW>
+__device__ void group_rows_small(const PermuteArgs& a, const int* ids, int* smem) {
+  constexpr int NT = NW * 32;
+  const int tid = threadIdx.x;
+  const int E = a.E, R = a.T * a.k, MW = (R + 31) / 32;
+  uint32_t* mask = reinterpret_cast<uint32_t*>(smem);  // [E][MW]
+  int* off = smem + E * MW;                              // [E + 1]
+  int* scratch = off + E + 1;
+  scratch += (reinterpret_cast<uintptr_t>(scratch) & 7) ? 1 : 0;
+#pragma unroll 1
+  for (int i = tid; i < E * MW; i += NT) mask[i] = 0u;
+  __syncthreads();
+#pragma unroll 1
+  for (int r = tid; r < R; r += NT) {
+    const int e = ids[r];
+    if (e < 0 || e >= E) set_status(a.status, STRATA_DEV_BAD_ID);
+    else atomicOr(&mask[e * MW + (r >> 5)], 1u << (r & 31));
+  }
+  __syncthreads();
+  // experts [e0, e1) of this thread: rows, active segments, chunks, packed 21 bits apart
+  const int ept = (E + NT - 1) / NT;
+  const int e0 = min(E, tid * ept), e1 = min(E, e0 + ept);
+  unsigned long long mine = 0ull;
+#pragma unroll 1
+  for (int e = e0; e < e1; ++e) {
+    int c = 0;
+#pragma unroll 1
+    for (int w = 0; w < MW; ++w) c += __popc(mask[e * MW + w]);
+    if (c > 0) mine += static_cast<unsigned long long>(c) |
+                       (1ull << 21) | (static_cast<unsigned long long>((c + a.tokc - 1) / a.tokc) << 42);
+  }
+  unsigned long long tot;
+  unsigned long long run = block_scan_excl64<NW>(mine, scratch, &tot);
+  const int sh = (a.has_shared && a.T > 0) ? 1 : 0;
+  const int sh_chunks = sh ? (a.T + a.tokc - 1) / a.tokc : 0;
+  const int nseg = static_cast<int>((tot >> 21) & 0x1FFFFF) + sh;
+  const int nchunks = static_cast<int>(tot >> 42) + sh_chunks;
+#pragma unroll 1
+  for (int e = e0; e < e1; ++e) {
+    int c = 0;
+#pragma unroll 1
+    for (int w = 0; w < MW; ++w) c += __popc(mask[e * MW + w]);
+    const int row0 = static_cast<int>(run & 0x1FFFFF);
+    off[e] = row0;
+    a.counts[e] = c;
+    a.offsets[e] = row0;
+    if (c > 0) {
+      const int sidx = static_cast<int>((run >> 21) & 0x1FFFFF) + sh;
+      a.seg_expert[sidx] = e;
+      a.seg_row0[sidx] = row0;
+      a.seg_rows[sidx] = c;
+      int ch = static_cast<int>(run >> 42) + sh_chunks;
+#pragma unroll 1
+      for (int q = 0; q * a.tokc < c; ++q)
+        a.chunk_list[ch++] = make_int4(e, row0 + q * a.tokc, min(a.tokc, c - q * a.tokc), 0);
+      run += static_cast<unsigned long long>(c) | (1ull << 21) |
+             (static_cast<unsigned long long>((c + a.tokc - 1) / a.tokc) << 42);
+    }
+  }
+  if (tid == 0) {
+    a.offsets[E] = static_cast<int>(tot & 0x1FFFFF);
+    if (sh) {
+      a.seg_expert[0] = E;
+      a.seg_row0[0] = R;
+      a.seg_rows[0] = a.T;
+    }
+    a.hdr->nseg = nseg;
+    a.hdr->n_chunks = nchunks;
+    a.hdr->n_items_gu = nchunks * a.mtiles_gu * a.ksplit_gu;
+    a.hdr->n_items_dn = nchunks * a.mtiles_dn;
+    a.hdr->next_gu = 0;
+    a.hdr->next_dn = 0;
+  }
+#pragma unroll 1
+  for (int q = tid; q < sh_chunks; q += NT)
+    a.chunk_list[q] = make_int4(E, R + q * a.tokc, min(a.tokc, a.T - q * a.tokc), 0);
+  if (a.split_cnt && a.ksplit_gu > 1) {
+#pragma unroll 1
+    for (int i = tid; i < nchunks * a.mtiles_gu; i += NT) a.split_cnt[i] = 0;
+  }
+  __syncthreads();
+  // positions: expert offset + marked rows of that expert below r (stable by token)
+#pragma unroll 1
+  for (int r = tid; r < R; r += NT) {
+    const int e = ids[r];
+    if (e < 0 || e >= E) continue;
+    const uint32_t* m = mask + e * MW;
+    int pos = off[e] + __popc(m[r >> 5] & ((1u << (r & 31)) - 1u));
+#pragma unroll 1
+    for (int w = 0; w < (r >> 5); ++w) pos += __popc(m[w]);
+    a.perm[pos] = r / a.k;
+    a.inv[r] = pos;
+  }
+  if (a.has_shared) {
+#pragma unroll 1
+    for (int t = tid; t < a.T; t += NT) a.perm[R + t] = t;
+  }
+}
+
 }  // namespace strata

@@ -29,51 +29,86 @@ __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Softmax + top-k of one token whose E (<= 1024) logits sit in shared memory (one warp). Every
-// lane keeps the keys of its experts e = lane + 32 i in registers; each of the k rounds takes the
-// warp-wide largest key with one redux.sync, breaks ties towards the lowest expert id with a second
-// one, and only the winning lane rescans its own keys.
-__device__ void warp_softmax_topk(const float* lg, int E, int k, uint32_t flags, int* ids,
-                                  float* gates) {
+// Softmax + top-k of one token's E (<= 1024) logits by one warp. Lane l keeps the keys of experts
+// e = l + 32 i (i < NPL) in registers, with its best remaining key. Each of the k rounds takes the
+// warp-wide largest best key with one redux.sync; the lane holding it is found with a ballot (a
+// second redux picks the lowest expert id when several lanes hold an equal key), and only that lane
+// drops the key and rescans its registers. Gates are computed by lanes 0..k-1 at the end.
+// kGlobal: lg is global memory written by other CTAs of this grid (read through L2).
+template <int NPL, bool kGlobal>
+__device__ __forceinline__ void warp_topk_regs(const float* lg, int E, int k, uint32_t flags,
+                                               int* ids, float* gates) {
   const int lane = threadIdx.x & 31;
-  uint32_t key[32];
-  uint32_t bk = 0;  // the lane's best key and its slot (lowest slot on equal keys)
+  uint32_t key[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    float v = 0.f;
+    if (e < E) v = kGlobal ? __ldcg(lg + e) : lg[e];
+    key[i] = e < E ? float_key(v) : 0u;
+  }
+  uint32_t bk = 0u;
   int bi = 0;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int e = lane + 32 * i;
-    key[i] = e < E ? float_key(lg[e]) : 0u;
-    if (key[i] > bk) { bk = key[i]; bi = i; }
-  }
+  for (int i = 0; i < NPL; ++i)
+    if (key[i] > bk) { bk = key[i]; bi = i; }  // ascending i: ties keep the lower expert id
   const float mx = key_float(__reduce_max_sync(0xffffffffu, bk));
   float sum = 0.f;
-  for (int e = lane; e < E; e += 32) sum += expf(lg[e] - mx);
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (lane + 32 * i < E) sum += expf(key_float(key[i]) - mx);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
 
-  float gsum = 0.f, my_g = 0.f;
-  int my_i = 0;
+  uint32_t my_key = 0u, my_id = 0u;
+#pragma unroll 1
   for (int j = 0; j < k; ++j) {
     const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
-    const uint32_t cand = (bk == m && bk != 0u) ? static_cast<uint32_t>(lane + 32 * bi) : 0xFFFFFFFFu;
-    const int eb = static_cast<int>(__reduce_min_sync(0xffffffffu, cand));
-    if (lane == (eb & 31)) {  // take it, then rescan this lane's remaining keys
+    const uint32_t cand = static_cast<uint32_t>(lane + 32 * bi);
+    const unsigned holders = __ballot_sync(0xffffffffu, bk == m);
+    uint32_t eb;
+    if ((holders & (holders - 1u)) == 0u)
+      eb = __shfl_sync(0xffffffffu, cand, __ffs(holders) - 1);
+    else
+      eb = __reduce_min_sync(0xffffffffu, bk == m ? cand : 0xFFFFFFFFu);
+    if (lane == j) { my_key = m; my_id = eb; }
+    if (cand == eb && bk == m) {  // this lane held the winner: drop it, rescan
+#pragma unroll
+      for (int i = 0; i < NPL; ++i)
+        if (i == bi) key[i] = 0u;
       bk = 0u;
       bi = 0;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        if (lane + 32 * i == eb) key[i] = 0u;
+      for (int i = 0; i < NPL; ++i)
         if (key[i] > bk) { bk = key[i]; bi = i; }
-      }
     }
-    const float g = expf(key_float(m) - mx) / sum;
-    gsum += g;
-    if (lane == j) { my_g = g; my_i = eb; }
+  }
+  const float g = lane < k ? expf(key_float(my_key) - mx) / sum : 0.f;
+  float gsum = g;
+  if (flags & STRATA_RENORM) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) gsum += __shfl_xor_sync(0xffffffffu, gsum, o);
   }
   if (lane < k) {
-    ids[lane] = my_i;
-    gates[lane] = (flags & STRATA_RENORM) ? my_g / gsum : my_g;
+    ids[lane] = static_cast<int>(my_id);
+    gates[lane] = (flags & STRATA_RENORM) ? g / gsum : g;
   }
+}
+
+template <bool kGlobal>
+__device__ void warp_softmax_topk(const float* lg, int E, int k, uint32_t flags, int* ids,
+                                  float* gates) {
+  const int npl = (E + 31) / 32;
+  if (npl <= 1) warp_topk_regs<1, kGlobal>(lg, E, k, flags, ids, gates);
+  else if (npl <= 2) warp_topk_regs<2, kGlobal>(lg, E, k, flags, ids, gates);
+  else if (npl <= 4) warp_topk_regs<4, kGlobal>(lg, E, k, flags, ids, gates);
+  else if (npl <= 6) warp_topk_regs<6, kGlobal>(lg, E, k, flags, ids, gates);
+  else if (npl <= 8) warp_topk_regs<8, kGlobal>(lg, E, k, flags, ids, gates);
+  else if (npl <= 10) warp_topk_regs<10, kGlobal>(lg, E, k, flags, ids, gates);
+  else if (npl <= 12) warp_topk_regs<12, kGlobal>(lg, E, k, flags, ids, gates);
+  else if (npl <= 16) warp_topk_regs<16, kGlobal>(lg, E, k, flags, ids, gates);
+  else if (npl <= 24) warp_topk_regs<24, kGlobal>(lg, E, k, flags, ids, gates);
+  else warp_topk_regs<32, kGlobal>(lg, E, k, flags, ids, gates);
 }
 
 // ----------------------------------------------------------------------------- decode: fused
@@ -86,22 +121,17 @@ int route_small_epc(int E, int num_sms) {
   return epc;
 }
 
-// dynamic shared memory of the last CTA (bytes): logits [8][E] floats, aliased by the grouping
-// scratch, then ids and gates [T*k]
-__host__ __device__ static size_t route_small_lg_bytes(int T, int E) {
-  size_t a = static_cast<size_t>(kRsWarps) * E * 4;
-  const size_t all = static_cast<size_t>(T) * E * 4;  // every token's logits, when it fits
-  if (all > a && all <= 96 * 1024) a = all;
-  return a;
+// dynamic shared memory of the last CTA (bytes): the grouping scratch, then ids and gates [T*k]
+__host__ __device__ static bool route_small_compact_group(const RouteSmallArgs& a) {
+  return a.grp.chunk_list != nullptr && a.T * a.k <= kGroupSmallMaxR;
 }
-// ids and gates follow both the logits and the grouping scratch (which alias each other)
-__host__ __device__ static size_t route_small_ids_off(int T, int E) {
-  size_t a = route_small_lg_bytes(T, E);
-  const size_t g = group_smem_ints(kRsWarps, E) * 4;
-  return g > a ? g : a;
+__host__ __device__ static size_t route_small_ids_off(const RouteSmallArgs& a) {
+  const size_t g = route_small_compact_group(a) ? group_small_ints(kRsWarps, a.E, a.T * a.k)
+                                                : group_smem_ints(kRsWarps, a.E);
+  return (g * 4 + 15) & ~static_cast<size_t>(15);
 }
-__host__ __device__ static size_t route_small_smem(int T, int E, int k) {
-  return route_small_ids_off(T, E) + static_cast<size_t>(T) * k * 8;
+__host__ __device__ static size_t route_small_smem(const RouteSmallArgs& a) {
+  return route_small_ids_off(a) + static_cast<size_t>(a.T) * a.k * 8;
 }
 
 __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
@@ -202,41 +232,31 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   if (!is_last) return;
   __threadfence();
 
-  const size_t lg_bytes = route_small_lg_bytes(T, E);
-  float* lg = reinterpret_cast<float*>(rs_smem);  // [8 warps][E]
-  int* s_ids = reinterpret_cast<int*>(rs_smem + route_small_ids_off(T, E));
+  int* s_ids = reinterpret_cast<int*>(rs_smem + route_small_ids_off(a));
   float* s_gates = reinterpret_cast<float*>(s_ids + T * a.k);
-  if (static_cast<size_t>(T) * E * 4 <= lg_bytes) {
-    // every token's logits in one coalesced sweep by the whole CTA, then one token per warp
-#pragma unroll 16
-    for (int i = threadIdx.x; i < T * E; i += blockDim.x) lg[i] = __ldcg(a.logits + i);
-    __syncthreads();
-    for (int t = warp; t < T; t += kRsWarps)
-      warp_softmax_topk(lg + t * E, E, a.k, a.flags, s_ids + t * a.k, s_gates + t * a.k);
-  } else {
-    for (int t = warp; t < T; t += kRsWarps) {
-      float* l = lg + warp * E;
-#pragma unroll 8
-      for (int e2 = lane; e2 < E; e2 += 32) l[e2] = __ldcg(a.logits + static_cast<int64_t>(t) * E + e2);
-      __syncwarp();
-      warp_softmax_topk(l, E, a.k, a.flags, s_ids + t * a.k, s_gates + t * a.k);
-      __syncwarp();
-    }
-  }
+  // one token per warp, its logits read from L2 straight into registers
+#pragma unroll 1
+  for (int t = warp; t < T; t += kRsWarps)
+    warp_softmax_topk<true>(a.logits + static_cast<int64_t>(t) * E, E, a.k, a.flags,
+                            s_ids + t * a.k, s_gates + t * a.k);
   __syncthreads();
   for (int i = threadIdx.x; i < T * a.k; i += blockDim.x) {
     a.ids[i] = s_ids[i];
     a.gates[i] = s_gates[i];
   }
   if (threadIdx.x == 0) a.grp.hdr->route_done = 0;
-  if (a.do_group)
-    group_rows<kRsWarps>(a.grp, s_ids, carve_group_smem(reinterpret_cast<int*>(rs_smem), kRsWarps, E));
+  if (a.do_group) {
+    if (route_small_compact_group(a))
+      group_rows_small<kRsWarps>(a.grp, s_ids, reinterpret_cast<int*>(rs_smem));
+    else
+      group_rows<kRsWarps>(a.grp, s_ids, carve_group_smem(reinterpret_cast<int*>(rs_smem), kRsWarps, E));
+  }
 }
 
 cudaError_t launch_route_small(const RouteSmallArgs& a, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;
   const dim3 grid((a.E + a.epc - 1) / a.epc);
-  const size_t smem = route_small_smem(a.T, a.E, a.k);
+  const size_t smem = route_small_smem(a);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(route_small_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -475,8 +495,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
     lg[e] = v;
   }
   __syncwarp();
-  warp_softmax_topk(lg, E, k, flags, ids + static_cast<int64_t>(t) * k,
-                    gates + static_cast<int64_t>(t) * k);
+  warp_softmax_topk<false>(lg, E, k, flags, ids + static_cast<int64_t>(t) * k,
+                           gates + static_cast<int64_t>(t) * k);
 }
 
 int router_num_splits(int64_t T, int64_t H, int E, int num_sms) {
