@@ -1,0 +1,448 @@
+// K4 (decode path): W4A16 grouped GEMM for segments with few rows, where the layer is bound by
+// streaming the activated experts' int4 weights from HBM. One launch covers every expert's group
+// ("Strata" 3090 tuning, xdnf.cn/news/329730, §3.2: one grouped GEMM instead of one GEMM launch per
+// expert); dequantization happens in registers ("Strata" architecture essay, dpshk.com/news/6309482,
+// §3.2: decode is bandwidth-bound, so use wide loads and keep the small operands close).
+//
+// Work item = (8-row chunk of one expert's rows, block of weight rows, contraction split). A
+// persistent CTA (two per SM) has one producer warp and 8 consumer warps sharing a ring of stages;
+// a stage holds one 128-wide contraction group of the block:
+//  * weights: gate/up 128 gate + 128 up rows, down 256 rows, 64 bytes each, by one TMA box per
+//    matrix (canonical row-major codes, no re-layout);
+//  * activations: the chunk's 8 rows x 128 bf16, gathered through the routing permutation by
+//    cp.async, 16-byte pieces swizzled so that the consumers' fragment loads do not conflict;
+//  * scales: the fp16 pair holding each row's scale, by 4-byte cp.async.
+// The producer streams stages ahead (mbarrier full/empty pairs; every wait is time-bounded) while
+// the consumers compute; consumer warp w owns 16 gate + 16 up rows (gate/up) or 32 rows (down).
+//
+// A consumer warp computes with mma.sync m16n8k16 (bf16 in, fp32 accumulate) and swapped operands:
+// weight rows are the A operand, the (up to 8) tokens the B operand.
+//  * Lane (g = lane/4, t = lane%4) takes 16 bytes = 32 codes of rows g and g+8 per group, and the
+//    contraction order inside the group is permuted so that they feed exactly the lane's A-fragment
+//    slots. The activations are stored with every 8-wide chunk in (0,4,1,5,2,6,3,7) order (x by the
+//    router, h by the gate/up epilogue), which is exactly the B-fragment pairing. A dot product does
+//    not depend on the order of its terms, so no weight re-layout is needed.
+//  * int4 -> bf16 in one LOP3 per code pair: flipping each nibble's sign bit and OR-ing it into the
+//    low mantissa of bf16 128 yields q + 136 exactly. The +136 is removed after the group's MMAs
+//    with a correction MMA (A = 136 everywhere, same B) shared by both tiles, and the group's fp16
+//    scale is applied in fp32: acc += s * (partial - correction). Weights are never rounded.
+//  * Small batches split the contraction; the last split to arrive (device counter per warp tile)
+//    sums the partials in split order and applies the epilogue, so results stay deterministic.
+// Gate/up writes h = silu(u) * v (bf16); down writes y (fp32) for the combine.
+#include <cudaTypedefs.h>
+
+#include "kernels.cuh"
+#include "tc_ptx.cuh"
+
+namespace strata {
+namespace {
+
+constexpr int kCW = 8;                     // consumer warps
+constexpr int kThreads = (kCW + 1) * 32;   // + one producer warp
+constexpr int kStages = 5;
+constexpr int kWBytes = 16384;             // weights of one stage (256 rows x 64 bytes)
+constexpr int kActOff = kWBytes;           // 8 rows x 256 bytes
+constexpr int kScOff = kActOff + 2048;     // 256 rows x 4 bytes
+constexpr int kHdrOff = kScOff + 1024;
+constexpr int kStageBytes = 19584;         // 128-byte multiple >= kHdrOff + sizeof(StageHdr)
+constexpr int kBarOff = kStages * kStageBytes;
+constexpr int kSmemBytes = kBarOff + 2 * kStages * 8 + 16;
+constexpr int kCtasPerSm = 2;
+
+struct StageHdr {
+  int e, rbase, nvalid, blk, ks, cidx;  // item: expert, first GEMM row, rows, row block, split, chunk
+  int g, gbeg, gend;                    // this stage's group and the item's group range
+  int done;                             // no more items
+};
+static_assert(kHdrOff + static_cast<int>(sizeof(StageHdr)) <= kStageBytes, "stage layout");
+
+__device__ __forceinline__ uint32_t codes_to_bf16_biased(uint32_t v) {
+  uint32_t d;
+  // d = mask ? (v ^ c) : c, mask = 0x000F000F, c = 0x43084308: flips the nibble sign bits and
+  // puts the exponent of 128 around them
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(v), "n"(0x000F000F), "n"(0x43084308));
+  return d;
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t saddr, const void* gmem, bool pred) {
+  const int sz = pred ? 4 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(saddr), "l"(gmem), "r"(sz));
+}
+__device__ __forceinline__ void cp_async16s(uint32_t saddr, const void* gmem, bool pred) {
+  const int sz = pred ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(saddr), "l"(gmem), "r"(sz));
+}
+// The barrier receives one arrival once every cp.async this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar))
+               : "memory");
+}
+
+// Position of 16-byte piece q (0..15) of activation row n inside the row. A 128-bit shared load
+// is served 8 lanes at a time: lanes 8p..8p+7 read rows 2p, 2p+1, pieces 4t + c (t = 0..3, fixed
+// c). The map sends those 8 pieces to 8 different 16-byte bank groups, so no load conflicts.
+__device__ __forceinline__ int act_swz(int n, int q) { return q ^ ((q >> 3) & 1) ^ ((n & 1) << 1); }
+
+struct CtaGemmParams {
+  GemmArgs a;
+  int nblk;   // row blocks per expert
+  int RB;     // rows per block (gate/up: per matrix)
+};
+
+template <bool kGateUp>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    grouped_gemm_cta_kernel(const __grid_constant__ CUtensorMap map0,
+                            const __grid_constant__ CUtensorMap map1, const CtaGemmParams p) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const GemmArgs& a = p.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* empty = full + kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+  uint32_t* status = &a.hdr->status;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&full[s], 1 + 32);  // producer expect_tx arrival + 32 cp.async arrivals
+      tc::mbar_init(&empty[s], kCW);    // one arrival per consumer warp
+    }
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+
+  const int ngroups = a.K / kGroup;
+  const int KS = a.ksplit;
+
+  if (warp == kCW) {
+    // ------------------------------------------------------------------ producer warp
+    if (lane == 0) {
+      tc::prefetch_tmap(&map0);
+      if (kGateUp) tc::prefetch_tmap(&map1);
+    }
+    if (kGateUp) griddep_wait();  // the work lists and x come from the router
+    griddep_launch();
+    int* const next_ctr = kGateUp ? &a.hdr->next_gu : &a.hdr->next_dn;
+    const int n_items = kGateUp ? a.hdr->n_items_gu : a.hdr->n_items_dn;
+    const int nchunks = a.hdr->n_chunks;
+    const int64_t srow = a.K / kGroup;            // scale row stride (fp16)
+    const int q = lane & 15;                      // activation piece of this lane
+    const uint32_t tx_bytes = kGateUp ? 2u * p.RB * 64u : static_cast<uint32_t>(p.RB) * 64u;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool waited = kGateUp;  // down: griddep_wait still pending (h comes from gate/up)
+    int npend = 0;          // down, first item: stages whose activation copies wait for it
+    int item = 0;
+    if (lane == 0) item = atomicAdd(next_ctr, 1);
+    item = __shfl_sync(0xffffffffu, item, 0);
+    bool ok = true;
+    while (item < n_items && ok) {
+      int nxt = 0;
+      if (lane == 0) nxt = atomicAdd(next_ctr, 1);
+      const int cidx = item % nchunks;
+      const int rest = item / nchunks;
+      const int blk = rest % p.nblk;
+      const int ks = rest / p.nblk;
+      const int4 ch = __ldg(a.chunk_list + cidx);
+      const int e = ch.x, rbase = ch.y, nvalid = ch.z;
+      const int gbeg = (ks * ngroups) / KS, gend = ((ks + 1) * ngroups) / KS;
+      const int64_t wrow0 = static_cast<int64_t>(e) * a.N + static_cast<int64_t>(blk) * p.RB;
+      // activation rows of this lane's pieces: n = 2 i + lane / 16
+      const __nv_bfloat16* arow[4];
+      bool avalid[4];
+      // down: h rows come from gate/up (wait for it before the first activation copy)
+      for (int g = gbeg; g < gend; ++g) {
+        if (!tc::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
+        unsigned char* st = smem + stage * kStageBytes;
+        if (lane == 0) {
+          StageHdr* h = reinterpret_cast<StageHdr*>(st + kHdrOff);
+          h->e = e; h->rbase = rbase; h->nvalid = nvalid; h->blk = blk; h->ks = ks; h->cidx = cidx;
+          h->g = g; h->gbeg = gbeg; h->gend = gend; h->done = 0;
+          tc::mbar_arrive_expect_tx(&full[stage], tx_bytes);
+          tc::tma_load_2d(st, &map0, g * 64, static_cast<int32_t>(wrow0), &full[stage]);
+          if (kGateUp)
+            tc::tma_load_2d(st + p.RB * 64, &map1, g * 64, static_cast<int32_t>(wrow0), &full[stage]);
+        }
+        // scales: the 4-byte fp16 pair holding group g, 8 rows per lane
+        const int gp = g & ~1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = lane + 32 * i;  // stage scale row
+          const __half* sbase;
+          int64_t row;
+          if (kGateUp) {
+            sbase = r < p.RB ? a.scales0 : a.scales1;
+            row = wrow0 + (r < p.RB ? r : r - p.RB);
+          } else {
+            sbase = a.scales0;
+            row = wrow0 + r;
+          }
+          const bool in = kGateUp ? true : (blk * p.RB + r < a.N);
+          cp_async4(tc::smem_u32(st + kScOff + r * 4), sbase + (in ? row : wrow0) * srow + gp, in);
+        }
+        if (g == gbeg) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int n = 2 * i + (lane >> 4);
+            avalid[i] = n < nvalid;
+            int64_t src = rbase + (avalid[i] ? n : 0);
+            if (a.perm) src = __ldg(a.perm + src);
+            arow[i] = a.act + src * a.K;
+          }
+        }
+        auto issue_act = [&](int gg, unsigned char* sst, uint64_t* bar) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int n = 2 * i + (lane >> 4);
+            const uint32_t dst = tc::smem_u32(sst + kActOff + n * 256 + (act_swz(n, q) << 4));
+            cp_async16s(dst, reinterpret_cast<const char*>(arow[i] + gg * kGroup) + q * 16,
+                        avalid[i]);
+          }
+          cp_async_arrive_noinc(bar);
+        };
+        if (waited) {
+          issue_act(g, st, &full[stage]);
+        } else {
+          // down, first item: weights and scales of up to kStages groups go out before waiting
+          // for gate/up (which writes h); their activation copies follow the wait
+          ++npend;
+          if (npend == kStages || g == gend - 1) {
+            griddep_wait();
+            waited = true;
+            int s0 = stage - (npend - 1);
+            if (s0 < 0) s0 += kStages;
+            for (int j = 0; j < npend; ++j) {
+              const int ss = (s0 + j) % kStages;
+              issue_act(g - (npend - 1) + j, smem + ss * kStageBytes, &full[ss]);
+            }
+          }
+        }
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+      item = __shfl_sync(0xffffffffu, nxt, 0);
+    }
+    if (!waited) griddep_wait();
+    if (ok && tc::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status)) {
+      if (lane == 0) reinterpret_cast<StageHdr*>(smem + stage * kStageBytes + kHdrOff)->done = 1;
+      __syncwarp();
+      tc::mbar_arrive(&full[stage]);      // 32 lane arrivals
+      if (lane == 0) tc::mbar_arrive(&full[stage]);  // + the expect_tx slot
+    }
+    // leave no copy in flight into this CTA's shared memory
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
+    if (*abort_flag) {
+      // outstanding TMA boxes land on their full barriers: wait (bounded) for the last stages
+      for (int s = 0; s < kStages; ++s) tc::mbar_wait_drain(&full[s], 0), tc::mbar_wait_drain(&full[s], 1);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------------- consumer warps
+  griddep_wait();  // outputs and split-K scratch follow the previous kernel
+  const int gq = lane >> 2, t4 = lane & 3;
+  const uint32_t a136[4] = {0x43084308u, 0x43084308u, 0x43084308u, 0x43084308u};
+  const int mtile = kGateUp ? 16 : 32;
+  int stage = 0;
+  uint32_t phase = 0;
+  float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+  while (true) {
+    if (!tc::mbar_wait(&full[stage], phase, abort_flag, status)) break;
+    const unsigned char* st = smem + stage * kStageBytes;
+    const StageHdr hd = *reinterpret_cast<const StageHdr*>(st + kHdrOff);
+    if (hd.done) break;
+    // weights: tile 0 rows (gate: w*16.., down: w*32..), tile 1 (up rows w*16.. / down w*32+16..)
+    const unsigned char* t0 = st + (kGateUp ? warp * 16 : warp * 32) * 64;
+    const unsigned char* t1 = kGateUp ? t0 + p.RB * 64 : t0 + 16 * 64;
+    const uint4 a0l = *reinterpret_cast<const uint4*>(t0 + gq * 64 + t4 * 16);
+    const uint4 a0h = *reinterpret_cast<const uint4*>(t0 + (gq + 8) * 64 + t4 * 16);
+    const uint4 a1l = *reinterpret_cast<const uint4*>(t1 + gq * 64 + t4 * 16);
+    const uint4 a1h = *reinterpret_cast<const uint4*>(t1 + (gq + 8) * 64 + t4 * 16);
+    uint32_t X[16];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int qq = t4 * 4 + c;
+      const uint4 b = *reinterpret_cast<const uint4*>(st + kActOff + gq * 256 + (act_swz(gq, qq) << 4));
+      X[4 * c] = b.x; X[4 * c + 1] = b.y; X[4 * c + 2] = b.z; X[4 * c + 3] = b.w;
+    }
+    // scale pairs of rows gq, gq+8 of both tiles
+    const int sr0 = kGateUp ? warp * 16 + gq : warp * 32 + gq;
+    const int sr1 = kGateUp ? p.RB + warp * 16 + gq : warp * 32 + 16 + gq;
+    const uint32_t* sc = reinterpret_cast<const uint32_t*>(st + kScOff);
+    const uint32_t s0a = sc[sr0], s0b = sc[sr0 + 8], s1a = sc[sr1], s1b = sc[sr1 + 8];
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&empty[stage]);
+    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+
+    if (hd.g == hd.gbeg) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) { acc0[c] = 0.f; acc1[c] = 0.f; }
+    }
+    const uint32_t w0l[4] = {a0l.x, a0l.y, a0l.z, a0l.w}, w0h[4] = {a0h.x, a0h.y, a0h.z, a0h.w};
+    const uint32_t w1l[4] = {a1l.x, a1l.y, a1l.z, a1l.w}, w1h[4] = {a1h.x, a1h.y, a1h.z, a1h.w};
+    // two accumulator sets (even / odd j) halve the MMA dependency chains
+    float p0[2][4] = {}, p1[2][4] = {}, cr[2][4] = {};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int h = j & 1;
+      // activations are stored pair-interleaved: X[4j+m] = {x[8j+m], x[8j+m+4]}
+      const uint32_t b00 = X[4 * j], b01 = X[4 * j + 1], b10 = X[4 * j + 2], b11 = X[4 * j + 3];
+      mma_bf16_16816(cr[h], a136, b00, b01, cr[h]);
+      mma_bf16_16816(cr[h], a136, b10, b11, cr[h]);
+      {
+        const uint32_t vl = w0l[j], vh = w0h[j];
+        const uint32_t fa[4] = {codes_to_bf16_biased(vl), codes_to_bf16_biased(vh),
+                                codes_to_bf16_biased(vl >> 4), codes_to_bf16_biased(vh >> 4)};
+        mma_bf16_16816(p0[h], fa, b00, b01, p0[h]);
+        const uint32_t fb[4] = {codes_to_bf16_biased(vl >> 8), codes_to_bf16_biased(vh >> 8),
+                                codes_to_bf16_biased(vl >> 12), codes_to_bf16_biased(vh >> 12)};
+        mma_bf16_16816(p0[h], fb, b10, b11, p0[h]);
+      }
+      {
+        const uint32_t vl = w1l[j], vh = w1h[j];
+        const uint32_t fa[4] = {codes_to_bf16_biased(vl), codes_to_bf16_biased(vh),
+                                codes_to_bf16_biased(vl >> 4), codes_to_bf16_biased(vh >> 4)};
+        mma_bf16_16816(p1[h], fa, b00, b01, p1[h]);
+        const uint32_t fb[4] = {codes_to_bf16_biased(vl >> 8), codes_to_bf16_biased(vh >> 8),
+                                codes_to_bf16_biased(vl >> 12), codes_to_bf16_biased(vh >> 12)};
+        mma_bf16_16816(p1[h], fb, b10, b11, p1[h]);
+      }
+    }
+    // the scale of group g is the low half of its pair for even g, the high half for odd g
+    const int sh = (hd.g & 1) * 16;
+    const float sa0 = __half2float(__ushort_as_half(static_cast<unsigned short>(s0a >> sh)));
+    const float sb0 = __half2float(__ushort_as_half(static_cast<unsigned short>(s0b >> sh)));
+    const float sa1 = __half2float(__ushort_as_half(static_cast<unsigned short>(s1a >> sh)));
+    const float sb1 = __half2float(__ushort_as_half(static_cast<unsigned short>(s1b >> sh)));
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float q0 = (p0[0][c] - cr[0][c]) + (p0[1][c] - cr[1][c]);
+      const float q1 = (p1[0][c] - cr[0][c]) + (p1[1][c] - cr[1][c]);
+      acc0[c] = fmaf(c < 2 ? sa0 : sb0, q0, acc0[c]);
+      acc1[c] = fmaf(c < 2 ? sa1 : sb1, q1, acc1[c]);
+    }
+    if (hd.g != hd.gend - 1) continue;
+
+    // ------------------------------------------------------------------ item epilogue
+    const int mt = hd.blk * kCW + warp;  // global tile index of this warp inside the expert
+    if (mt * mtile >= a.N) continue;     // rows past the expert (last, partial block)
+    bool write = true;
+    if (KS > 1) {
+      // split-K: publish this split's partial sums; the last split to arrive reduces them
+      const int tile = (hd.cidx * p.nblk + hd.blk) * kCW + warp;
+      float* part = a.split_part + (static_cast<int64_t>(tile) * KS + hd.ks) * 256 + lane * 8;
+      reinterpret_cast<float4*>(part)[0] = make_float4(acc0[0], acc0[1], acc0[2], acc0[3]);
+      reinterpret_cast<float4*>(part)[1] = make_float4(acc1[0], acc1[1], acc1[2], acc1[3]);
+      __threadfence();
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        last = (atomicAdd(a.split_cnt + tile, 1) == KS - 1);
+        if (last) a.split_cnt[tile] = 0;  // ready for the next launch that uses the scratch
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      write = last != 0;
+      if (last) {
+        __threadfence();
+        const float* base = a.split_part + static_cast<int64_t>(tile) * KS * 256 + lane * 8;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) { acc0[c] = 0.f; acc1[c] = 0.f; }
+        for (int s = 0; s < KS; ++s) {  // split order: deterministic
+          const float4 u = __ldcg(reinterpret_cast<const float4*>(base + s * 256));
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(base + s * 256) + 1);
+          acc0[0] += u.x; acc0[1] += u.y; acc0[2] += u.z; acc0[3] += u.w;
+          acc1[0] += v.x; acc1[1] += v.y; acc1[2] += v.z; acc1[3] += v.w;
+        }
+      }
+    }
+    if (write) {
+      // C fragment: c0,c1 -> weight row gq, token columns 2t4, 2t4+1; c2,c3 -> row gq+8
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col = 2 * t4 + c;
+        if (col >= hd.nvalid) continue;
+        const int64_t orow = hd.rbase + col;
+        if (kGateUp) {
+          // h columns are stored pair-interleaved inside every 8 (the down GEMM's B order)
+          const int n0 = mt * 16 + (gq < 4 ? 2 * gq : 2 * gq - 7);
+          __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(a.out) + orow * a.N;
+          hrow[n0] = __float2bfloat16_rn(silu_f(acc0[c]) * acc1[c]);
+          hrow[n0 + 8] = __float2bfloat16_rn(silu_f(acc0[c + 2]) * acc1[c + 2]);
+        } else {
+          const int n0 = mt * 32 + gq;
+          float* y = static_cast<float*>(a.out) + orow * a.N;
+          y[n0] = acc0[c];
+          y[n0 + 8] = acc0[c + 2];
+          y[n0 + 16] = acc1[c];
+          y[n0 + 24] = acc1[c + 2];
+        }
+      }
+    }
+  }
+}
+
+// Codes [rows, K/2] bytes: boxes of 64 bytes (one group) x box_rows rows, no swizzle, zero fill.
+static PFN_cuTensorMapEncodeTiled_v12000 cta_tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &qr) != cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+static bool make_codes_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t K,
+                            int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = cta_tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kGateUp>
+cudaError_t launch_t(const GemmArgs& a, int64_t experts, int num_sms, cudaStream_t stream) {
+  CtaGemmParams p;
+  p.a = a;
+  p.RB = cta_gemm_block_rows(kGateUp);
+  p.nblk = static_cast<int>((a.N + p.RB - 1) / p.RB);
+  CUtensorMap m0, m1;
+  const int64_t rows = experts * a.N;
+  if (!make_codes_tmap(&m0, a.codes0, rows, a.K, p.RB)) return cudaErrorInvalidValue;
+  if (!make_codes_tmap(&m1, kGateUp ? a.codes1 : a.codes0, rows, a.K, p.RB))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_cta_kernel<kGateUp>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(grouped_gemm_cta_kernel<kGateUp>, dim3(num_sms * kCtasPerSm),
+                       dim3(kThreads), kSmemBytes, stream, true, m0, m1, p);
+}
+
+}  // namespace
+
+int cta_gemm_block_rows(bool gate_up) { return gate_up ? kCW * 16 : kCW * 32; }
+int cta_gemm_warps() { return kCW; }
+
+cudaError_t launch_gemm_cta(const GemmArgs& a, bool gate_up, int64_t experts, int num_sms,
+                            cudaStream_t stream) {
+  return gate_up ? launch_t<true>(a, experts, num_sms, stream)
+                 : launch_t<false>(a, experts, num_sms, stream);
+}
+
+// Contraction splits for a batch whose grouped GEMM has `items` (chunk x row block) work items:
+// enough for about two items per CTA, each split keeping at least two 128-wide groups.
+int cta_gemm_ksplit(int64_t items, int64_t K, int num_sms) {
+  const int64_t want = 2 * static_cast<int64_t>(num_sms) * kCtasPerSm;
+  const int64_t groups = K / kGroup;
+  int ks = 1;
+  while (items * ks < want && 2 * ks * 2 <= groups && ks < 16) ks *= 2;
+  return ks;
+}
+
+}  // namespace strata

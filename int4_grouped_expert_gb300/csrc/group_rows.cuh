@@ -191,12 +191,12 @@ __device__ void group_rows(const PermuteArgs& a, const int* ids, GroupSmem sm) {
       a.hdr->nseg = nseg;
       a.hdr->n_chunks = nchunks;
       a.hdr->n_items_gu = nchunks * a.mtiles_gu * a.ksplit_gu;
-      a.hdr->n_items_dn = nchunks * a.mtiles_dn;
+      a.hdr->n_items_dn = nchunks * a.mtiles_dn * a.ksplit_dn;
       a.hdr->next_gu = 0;
       a.hdr->next_dn = 0;
     }
-    if (a.split_cnt && a.ksplit_gu > 1)
-      for (int i = tid; i < nchunks * a.mtiles_gu; i += NT) a.split_cnt[i] = 0;
+    if (a.split_cnt)
+      for (int i = tid; i < nchunks * a.cnt_per_chunk; i += NT) a.split_cnt[i] = 0;
     return;
   }
   // Tensor-core path: tiles per segment = (token chunks) x (row tiles); prefix over segments.
@@ -340,16 +340,16 @@ __device__ void group_rows_small(const PermuteArgs& a, const int* ids, int* smem
     a.hdr->nseg = nseg;
     a.hdr->n_chunks = nchunks;
     a.hdr->n_items_gu = nchunks * a.mtiles_gu * a.ksplit_gu;
-    a.hdr->n_items_dn = nchunks * a.mtiles_dn;
+    a.hdr->n_items_dn = nchunks * a.mtiles_dn * a.ksplit_dn;
     a.hdr->next_gu = 0;
     a.hdr->next_dn = 0;
   }
 #pragma unroll 1
   for (int q = tid; q < sh_chunks; q += NT)
     a.chunk_list[q] = make_int4(E, R + q * a.tokc, min(a.tokc, a.T - q * a.tokc), 0);
-  if (a.split_cnt && a.ksplit_gu > 1) {
+  if (a.split_cnt) {
 #pragma unroll 1
-    for (int i = tid; i < nchunks * a.mtiles_gu; i += NT) a.split_cnt[i] = 0;
+    for (int i = tid; i < nchunks * a.cnt_per_chunk; i += NT) a.split_cnt[i] = 0;
   }
   __syncthreads();
   // positions: expert offset + marked rows of that expert below r (stable by token)

@@ -22,7 +22,9 @@ struct PermuteArgs {
   int mtiles_gu;     // gate/up row tiles per expert
   int mtiles_dn;     // down row tiles per expert
   int ksplit_gu;     // gate/up contraction splits per tile (1 = none)
-  int* split_cnt;    // [gate/up tiles] arrival counters of the split-K reduction, zeroed here
+  int ksplit_dn;     // down contraction splits per tile (1 = none)
+  int cnt_per_chunk; // split-K arrival counters per chunk (zeroed here)
+  int* split_cnt;    // arrival counters of the split-K reductions
   int4* chunk_list;  // warp path: {expert, first row, rows, 0} per tokc-row chunk (else null)
   WsHeader* hdr;
   uint32_t* status;
@@ -93,6 +95,12 @@ constexpr int kRouteSmallMaxT = 64;  // tokens handled by the fused decode route
 int route_small_epc(int E, int num_sms);
 cudaError_t launch_route_small(const RouteSmallArgs& a, cudaStream_t stream);
 cudaError_t launch_gemm_warp(const GemmArgs& a, bool gate_up, int num_sms, cudaStream_t stream);
+// CTA-staged warp GEMM (gemm_cta.cu): row blocks of cta_gemm_block_rows() weight rows per item.
+int cta_gemm_block_rows(bool gate_up);
+int cta_gemm_warps();
+int cta_gemm_ksplit(int64_t items, int64_t K, int num_sms);
+cudaError_t launch_gemm_cta(const GemmArgs& a, bool gate_up, int64_t experts, int num_sms,
+                            cudaStream_t stream);
 int warp_ksplit(int64_t T, int E, int k, int shared, int64_t I, int64_t H);
 constexpr int kTcRows = 256;  // token rows per tensor-core tile
 cudaError_t launch_gemm_tc(const TcArgs& a, bool gate_up, const void* b_rows, int64_t rows,

@@ -29,86 +29,134 @@ __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Softmax + top-k of one token's E (<= 1024) logits by one warp. Lane l keeps the keys of experts
-// e = l + 32 i (i < NPL) in registers, with its best remaining key. Each of the k rounds takes the
-// warp-wide largest best key with one redux.sync; the lane holding it is found with a ballot (a
-// second redux picks the lowest expert id when several lanes hold an equal key), and only that lane
-// drops the key and rescans its registers. Gates are computed by lanes 0..k-1 at the end.
-// kGlobal: lg is global memory written by other CTAs of this grid (read through L2).
-template <int NPL, bool kGlobal>
-__device__ __forceinline__ void warp_topk_regs(const float* lg, int E, int k, uint32_t flags,
-                                               int* ids, float* gates) {
-  const int lane = threadIdx.x & 31;
-  uint32_t key[NPL];
+// Best key of one lane's NPL keys and its slot, by a pairwise tree (ties keep the lower slot, which
+// is the lower expert id).
+// Slots whose bit is set in `taken` count as empty (a bit mask, not stores into key[]: an indexed
+// store would move the array to local memory).
+template <int N>
+__device__ __forceinline__ void lane_best(const uint32_t (&key)[N], uint32_t taken, uint32_t& bk,
+                                          int& bi) {
+  uint32_t k2[N];
+  int i2[N];
 #pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = lane + 32 * i;
-    float v = 0.f;
-    if (e < E) v = kGlobal ? __ldcg(lg + e) : lg[e];
-    key[i] = e < E ? float_key(v) : 0u;
+  for (int i = 0; i < N; ++i) { k2[i] = ((taken >> i) & 1u) ? 0u : key[i]; i2[i] = i; }
+#pragma unroll
+  for (int w = 1; w < N; w <<= 1) {
+#pragma unroll
+    for (int i = 0; i + w < N; i += 2 * w)
+      if (k2[i + w] > k2[i]) { k2[i] = k2[i + w]; i2[i] = i2[i + w]; }
   }
-  uint32_t bk = 0u;
-  int bi = 0;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i)
-    if (key[i] > bk) { bk = key[i]; bi = i; }  // ascending i: ties keep the lower expert id
-  const float mx = key_float(__reduce_max_sync(0xffffffffu, bk));
-  float sum = 0.f;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i)
-    if (lane + 32 * i < E) sum += expf(key_float(key[i]) - mx);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  bk = k2[0];
+  bi = i2[0];
+}
 
-  uint32_t my_key = 0u, my_id = 0u;
-#pragma unroll 1
-  for (int j = 0; j < k; ++j) {
-    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
-    const uint32_t cand = static_cast<uint32_t>(lane + 32 * bi);
-    const unsigned holders = __ballot_sync(0xffffffffu, bk == m);
-    uint32_t eb;
-    if ((holders & (holders - 1u)) == 0u)
-      eb = __shfl_sync(0xffffffffu, cand, __ffs(holders) - 1);
-    else
-      eb = __reduce_min_sync(0xffffffffu, bk == m ? cand : 0xFFFFFFFFu);
-    if (lane == j) { my_key = m; my_id = eb; }
-    if (cand == eb && bk == m) {  // this lane held the winner: drop it, rescan
+// Softmax + top-k of TPW tokens at once by one warp (their dependency chains interleave). Token j
+// is row t0 + j * tstride of lg (row stride ld) and is skipped if that is >= T; E <= 32 * NPL.
+// Lane l keeps the order-preserving keys of experts e = l + 32 i in registers with its best
+// remaining one. Each of the k rounds takes the warp-wide largest best key with one redux.sync and
+// the lowest expert id among the lanes holding it with a second; that lane marks the slot taken
+// and every lane re-takes its best. The rounds are branch-free, so the TPW chains interleave. Gates are computed by lanes 0..k-1 at the end.
+// kGlobal: lg is global memory written by other CTAs of this grid (read through L2).
+template <int NPL, int TPW, bool kGlobal>
+__device__ __forceinline__ void warp_topk_multi(const float* lg, int64_t ld, int t0, int tstride,
+                                                int T, int E, int k, uint32_t flags, int* ids,
+                                                float* gates) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[TPW][NPL];
+  // all loads first, unconditional (clamped address), so that they are in flight together
+  float v[TPW][NPL];
 #pragma unroll
-      for (int i = 0; i < NPL; ++i)
-        if (i == bi) key[i] = 0u;
-      bk = 0u;
-      bi = 0;
+  for (int j = 0; j < TPW; ++j) {
+    const int t = t0 + j * tstride;
+    const float* row = lg + static_cast<int64_t>(t < T ? t : 0) * ld;
 #pragma unroll
-      for (int i = 0; i < NPL; ++i)
-        if (key[i] > bk) { bk = key[i]; bi = i; }
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      const float* src = row + (e < E ? e : E - 1);
+      v[j][i] = kGlobal ? __ldcg(src) : *src;
     }
   }
-  const float g = lane < k ? expf(key_float(my_key) - mx) / sum : 0.f;
-  float gsum = g;
-  if (flags & STRATA_RENORM) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) gsum += __shfl_xor_sync(0xffffffffu, gsum, o);
+  for (int j = 0; j < TPW; ++j) {
+    const bool tok = t0 + j * tstride < T;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      key[j][i] = (tok && lane + 32 * i < E) ? float_key(v[j][i]) : 0u;
   }
-  if (lane < k) {
-    ids[lane] = static_cast<int>(my_id);
-    gates[lane] = (flags & STRATA_RENORM) ? g / gsum : g;
+  uint32_t bk[TPW], taken[TPW];
+  int bi[TPW];
+  float mx[TPW], sum[TPW];
+#pragma unroll
+  for (int j = 0; j < TPW; ++j) {
+    taken[j] = 0u;
+    lane_best<NPL>(key[j], 0u, bk[j], bi[j]);
+    mx[j] = key_float(__reduce_max_sync(0xffffffffu, bk[j]));
+  }
+#pragma unroll
+  for (int j = 0; j < TPW; ++j) {
+    float sj = 0.f;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (lane + 32 * i < E) sj += expf(key_float(key[j][i]) - mx[j]);
+    sum[j] = sj;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int j = 0; j < TPW; ++j) sum[j] += __shfl_xor_sync(0xffffffffu, sum[j], o);
+  }
+  uint32_t my_key[TPW], my_id[TPW];
+#pragma unroll
+  for (int j = 0; j < TPW; ++j) { my_key[j] = 0u; my_id[j] = 0u; }
+#pragma unroll 1
+  for (int r = 0; r < k; ++r) {
+    // one phase at a time over the TPW tokens: the warp-wide reductions are kept in program
+    // order, so interleaving them by hand is what lets the tokens' latencies overlap
+    uint32_t m[TPW], cand[TPW], eb[TPW];
+#pragma unroll
+    for (int j = 0; j < TPW; ++j) m[j] = __reduce_max_sync(0xffffffffu, bk[j]);
+#pragma unroll
+    for (int j = 0; j < TPW; ++j) {
+      cand[j] = static_cast<uint32_t>(lane + 32 * bi[j]);
+      eb[j] = __reduce_min_sync(0xffffffffu, bk[j] == m[j] ? cand[j] : 0xFFFFFFFFu);
+    }
+#pragma unroll
+    for (int j = 0; j < TPW; ++j) {
+      if (lane == r) { my_key[j] = m[j]; my_id[j] = eb[j]; }
+      if (cand[j] == eb[j] && bk[j] == m[j]) taken[j] |= 1u << bi[j];
+      lane_best<NPL>(key[j], taken[j], bk[j], bi[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < TPW; ++j) {
+    const int t = t0 + j * tstride;
+    const float g = lane < k ? expf(key_float(my_key[j]) - mx[j]) / sum[j] : 0.f;
+    float gsum = g;
+    if (flags & STRATA_RENORM) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) gsum += __shfl_xor_sync(0xffffffffu, gsum, o);
+    }
+    if (t < T && lane < k) {
+      ids[static_cast<int64_t>(t) * k + lane] = static_cast<int>(my_id[j]);
+      gates[static_cast<int64_t>(t) * k + lane] = (flags & STRATA_RENORM) ? g / gsum : g;
+    }
   }
 }
 
-template <bool kGlobal>
-__device__ void warp_softmax_topk(const float* lg, int E, int k, uint32_t flags, int* ids,
-                                  float* gates) {
+template <int TPW, bool kGlobal>
+__device__ void warp_softmax_topk(const float* lg, int64_t ld, int t0, int tstride, int T, int E,
+                                  int k, uint32_t flags, int* ids, float* gates) {
   const int npl = (E + 31) / 32;
-  if (npl <= 1) warp_topk_regs<1, kGlobal>(lg, E, k, flags, ids, gates);
-  else if (npl <= 2) warp_topk_regs<2, kGlobal>(lg, E, k, flags, ids, gates);
-  else if (npl <= 4) warp_topk_regs<4, kGlobal>(lg, E, k, flags, ids, gates);
-  else if (npl <= 6) warp_topk_regs<6, kGlobal>(lg, E, k, flags, ids, gates);
-  else if (npl <= 8) warp_topk_regs<8, kGlobal>(lg, E, k, flags, ids, gates);
-  else if (npl <= 10) warp_topk_regs<10, kGlobal>(lg, E, k, flags, ids, gates);
-  else if (npl <= 12) warp_topk_regs<12, kGlobal>(lg, E, k, flags, ids, gates);
-  else if (npl <= 16) warp_topk_regs<16, kGlobal>(lg, E, k, flags, ids, gates);
-  else if (npl <= 24) warp_topk_regs<24, kGlobal>(lg, E, k, flags, ids, gates);
-  else warp_topk_regs<32, kGlobal>(lg, E, k, flags, ids, gates);
+#define STRATA_TOPK_CASE(N) \
+  warp_topk_multi<N, TPW, kGlobal>(lg, ld, t0, tstride, T, E, k, flags, ids, gates)
+  if (npl <= 1) STRATA_TOPK_CASE(1);
+  else if (npl <= 2) STRATA_TOPK_CASE(2);
+  else if (npl <= 4) STRATA_TOPK_CASE(4);
+  else if (npl <= 8) STRATA_TOPK_CASE(8);
+  else if (npl <= 10) STRATA_TOPK_CASE(10);
+  else if (npl <= 16 || TPW > 2) STRATA_TOPK_CASE(16);  // callers keep E <= 512 for TPW > 2
+  else STRATA_TOPK_CASE(32);
+#undef STRATA_TOPK_CASE
 }
 
 // ----------------------------------------------------------------------------- decode: fused
@@ -234,11 +282,17 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
 
   int* s_ids = reinterpret_cast<int*>(rs_smem + route_small_ids_off(a));
   float* s_gates = reinterpret_cast<float*>(s_ids + T * a.k);
-  // one token per warp, its logits read from L2 straight into registers
+  // tokens warp, warp + 8, ... (up to 4 at once per warp), logits read from L2 into registers
+  const int tpw = T <= kRsWarps ? 1 : (T <= 2 * kRsWarps || E > 512) ? 2 : 4;
 #pragma unroll 1
-  for (int t = warp; t < T; t += kRsWarps)
-    warp_softmax_topk<true>(a.logits + static_cast<int64_t>(t) * E, E, a.k, a.flags,
-                            s_ids + t * a.k, s_gates + t * a.k);
+  for (int t0 = warp; t0 < T; t0 += kRsWarps * tpw) {
+    if (tpw == 1)
+      warp_softmax_topk<1, true>(a.logits, E, t0, kRsWarps, T, E, a.k, a.flags, s_ids, s_gates);
+    else if (tpw == 2)
+      warp_softmax_topk<2, true>(a.logits, E, t0, kRsWarps, T, E, a.k, a.flags, s_ids, s_gates);
+    else
+      warp_softmax_topk<4, true>(a.logits, E, t0, kRsWarps, T, E, a.k, a.flags, s_ids, s_gates);
+  }
   __syncthreads();
   for (int i = threadIdx.x; i < T * a.k; i += blockDim.x) {
     a.ids[i] = s_ids[i];
@@ -495,8 +549,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
     lg[e] = v;
   }
   __syncwarp();
-  warp_softmax_topk<false>(lg, E, k, flags, ids + static_cast<int64_t>(t) * k,
-                           gates + static_cast<int64_t>(t) * k);
+  warp_softmax_topk<1, false>(lg, E, 0, 1, 1, E, k, flags, ids + static_cast<int64_t>(t) * k,
+                              gates + static_cast<int64_t>(t) * k);
 }
 
 int router_num_splits(int64_t T, int64_t H, int E, int num_sms) {

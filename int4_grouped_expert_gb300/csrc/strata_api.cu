@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cstring>
 
+#include <algorithm>
+
 #include "kernels.cuh"
 
 namespace strata {
@@ -41,9 +43,19 @@ struct FwdLayout {
   RouteLayout r;
   size_t seg_expert, seg_row0, seg_rows, seg_item_gu, seg_item_dn, chunk_list, h, y, xp,
       split_part, split_cnt, total;
-  int ksplit;
-  bool tc;  // tensor-core path for the grouped GEMMs
+  int ksplit;     // gate/up contraction splits (warp paths)
+  int ksplit_dn;  // down contraction splits (CTA-staged warp path)
+  int nblk_gu, nblk_dn;  // CTA-staged warp path: row blocks per expert
+  bool tc;   // tensor-core path for the grouped GEMMs
+  bool cta;  // CTA-staged warp GEMM (else the per-warp one)
 };
+
+#ifndef STRATA_WARP_GEMM_LEGACY
+#define STRATA_WARP_GEMM_LEGACY 0
+#endif
+// SM count the work split is sized for (the same on every device, so the workspace size and the
+// launch agree); it only steers how many contraction splits small batches get.
+constexpr int kSizingSms = 152;
 
 // Tensor-core path for batches with enough rows per expert to fill 128 x N tiles.
 static bool use_tc_path(const strata_moe_layer* L, int64_t T) {
@@ -69,11 +81,30 @@ static FwdLayout fwd_layout(const strata_moe_layer* L, int64_t T) {
   F.h = o; o = up(o + sizeof(uint16_t) * rows * L->I);
   F.y = o; o = up(o + sizeof(float) * rows * L->H);
   F.xp = o; o = up(o + sizeof(uint16_t) * rows * L->H);  // gathered / pair-interleaved x
-  F.ksplit = F.tc ? 1 : warp_ksplit(T, L->E, L->k, L->has_shared, L->I, L->H);
-  // split-K scratch: tiles <= chunks * (I / 16)
-  const int64_t ntile = F.ksplit > 1 ? max_chunks * (L->I / 16) : 0;
-  F.split_part = o; o = up(o + sizeof(float) * 256 * F.ksplit * ntile);
-  F.split_cnt = o; o = up(o + sizeof(int) * ntile);
+  // the CTA-staged kernel reads scale pairs with 4-byte copies: even group counts only
+  F.cta = !F.tc && !STRATA_WARP_GEMM_LEGACY && (L->H / 128) % 2 == 0 && (L->I / 128) % 2 == 0 &&
+          aligned(L->gate_scales, 4) && aligned(L->up_scales, 4) && aligned(L->down_scales, 4);
+  F.ksplit = 1;
+  F.ksplit_dn = 1;
+  int64_t part_floats = 0, ncnt = 0;
+  if (F.cta) {
+    F.nblk_gu = static_cast<int>((L->I + cta_gemm_block_rows(true) - 1) / cta_gemm_block_rows(true));
+    F.nblk_dn = static_cast<int>((L->H + cta_gemm_block_rows(false) - 1) / cta_gemm_block_rows(false));
+    F.ksplit = cta_gemm_ksplit(segs * F.nblk_gu, L->H, kSizingSms);
+    F.ksplit_dn = cta_gemm_ksplit(segs * F.nblk_dn, L->I, kSizingSms);
+    // per split tile: one 256-float partial per consumer warp
+    const int64_t tgu = F.ksplit > 1 ? max_chunks * F.nblk_gu * cta_gemm_warps() : 0;
+    const int64_t tdn = F.ksplit_dn > 1 ? max_chunks * F.nblk_dn * cta_gemm_warps() : 0;
+    part_floats = std::max(tgu * F.ksplit, tdn * F.ksplit_dn) * 256;
+    ncnt = std::max(tgu, tdn);
+  } else if (!F.tc) {
+    F.ksplit = warp_ksplit(T, L->E, L->k, L->has_shared, L->I, L->H);
+    // split-K scratch: tiles <= chunks * (I / 16)
+    ncnt = F.ksplit > 1 ? max_chunks * (L->I / 16) : 0;
+    part_floats = 256 * F.ksplit * ncnt;
+  }
+  F.split_part = o; o = up(o + sizeof(float) * part_floats);
+  F.split_cnt = o; o = up(o + sizeof(int) * ncnt);
   F.total = o;
   return F;
 }
@@ -174,20 +205,32 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
   pa.seg_rows = reinterpret_cast<int*>(base + F.seg_rows);
   pa.seg_item_gu = reinterpret_cast<int*>(base + F.seg_item_gu);
   pa.seg_item_dn = reinterpret_cast<int*>(base + F.seg_item_dn);
+  pa.ksplit_dn = 1;
+  pa.cnt_per_chunk = 0;
   if (F.tc) {
     pa.tokc = kTcRows;
     pa.mtiles_gu = static_cast<int>(L->I / 128);
     pa.mtiles_dn = static_cast<int>(L->H / 128);
     pa.ksplit_gu = 1;
     pa.chunk_list = nullptr;
+  } else if (F.cta) {
+    pa.tokc = 8;
+    pa.mtiles_gu = F.nblk_gu;
+    pa.mtiles_dn = F.nblk_dn;
+    pa.ksplit_gu = F.ksplit;
+    pa.ksplit_dn = F.ksplit_dn;
+    pa.cnt_per_chunk = (F.ksplit > 1 || F.ksplit_dn > 1)
+                           ? std::max(F.nblk_gu, F.nblk_dn) * cta_gemm_warps() : 0;
+    pa.chunk_list = reinterpret_cast<int4*>(base + F.chunk_list);
   } else {
     pa.tokc = 8;
     pa.mtiles_gu = static_cast<int>(L->I / 16);
     pa.mtiles_dn = static_cast<int>(L->H / 32);
     pa.ksplit_gu = F.ksplit;
+    pa.cnt_per_chunk = F.ksplit > 1 ? pa.mtiles_gu : 0;
     pa.chunk_list = reinterpret_cast<int4*>(base + F.chunk_list);
   }
-  pa.split_cnt = F.ksplit > 1 ? reinterpret_cast<int*>(base + F.split_cnt) : nullptr;
+  pa.split_cnt = pa.cnt_per_chunk > 0 ? reinterpret_cast<int*>(base + F.split_cnt) : nullptr;
   pa.hdr = hdr;
   pa.status = &hdr->status;
 
@@ -272,7 +315,8 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     g.ksplit = F.ksplit;
     g.split_part = reinterpret_cast<float*>(base + F.split_part);
     g.split_cnt = pa.split_cnt;
-    e = launch_gemm_warp(g, true, sms, st);
+    const int64_t experts = E + S;
+    e = F.cta ? launch_gemm_cta(g, true, experts, sms, st) : launch_gemm_warp(g, true, sms, st);
     if (e != cudaSuccess || !mark(3)) return STRATA_ERR_CUDA;
     GemmArgs d = g;
     d.codes0 = L->down_codes;
@@ -284,8 +328,8 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     d.out = base + F.y;
     d.K = static_cast<int>(L->I);
     d.N = static_cast<int>(L->H);
-    d.ksplit = 1;
-    e = launch_gemm_warp(d, false, sms, st);
+    d.ksplit = F.cta ? F.ksplit_dn : 1;
+    e = F.cta ? launch_gemm_cta(d, false, experts, sms, st) : launch_gemm_warp(d, false, sms, st);
     if (e != cudaSuccess || !mark(4)) return STRATA_ERR_CUDA;
   }
 
