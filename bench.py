@@ -293,6 +293,20 @@ def kernels_per_forward(T):
     return 4 if T <= 64 else 7
 
 
+def measured_traffic(key):
+    """DRAM bytes per launch of a kernel from a committed ncu capture (profiles/dram_traffic.json),
+    or None when the kernel's source has changed since the capture."""
+    import hashlib
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))[key]
+        src = open(os.path.join(ROOT, rec["source"]), "rb").read()
+        if hashlib.sha256(src).hexdigest() != rec["source_sha256"]:
+            return None
+        return float(rec["bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def peak_numbers():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -379,7 +393,8 @@ def run_strata(args):
         "roofline": {"kernel": "gate_up_gemm (grouped W4A16 GEMM + SiLU)", "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "algorithmic_bytes_per_launch": gu_bytes, "traffic": None},
+                     "algorithmic_bytes_per_launch": gu_bytes,
+                     "traffic": measured_traffic("decode_gate_up")},
         "layer_hbm": {"achieved_gbs": layer_gbs, "frac": layer_gbs / peak,
                       "bytes_per_step": n_exp * eb, "experts_per_step": n_exp},
         "stages_us": {k: v * 1e3 for k, v in stages.items()},
@@ -490,7 +505,9 @@ def run_prefill(args):
            "roofline": {"kernel": "gate_up_gemm (tcgen05 grouped W4A16 GEMM + SiLU)",
                         "bound": "tensor", "achieved": gu_tf, "peak": peak_tf, "unit": "TFLOP/s",
                         "frac": gu_tf / peak_tf, "peak_kind": "measured sustained",
-                        "traffic": None},
+                        "traffic": (measured_traffic("prefill_gate_up_c5")
+                                    if args.workload == "c5" and not args.experts
+                                    and not args.tokens else None)},
            "layer_tflops": layer_tf, "layer_frac": layer_tf / peak_tf, "down_tflops": dn_tf,
            "stages_us": {k: v * 1e3 for k, v in stages.items()}, "quantize": quant,
            "gpu_launches": kernels_per_forward(T) * steps, "clocks": clk}
