@@ -515,6 +515,37 @@ def run_prefill(args):
         print(json.dumps(rec), flush=True)
 
 
+def stack_graph_us(structs, xs_dev, T, out, ws, need, steps, warmup):
+    """The same stack call captured once in a CUDA graph and replayed (no per-launch host work):
+    mean microseconds per replay, or None if capture is not possible here."""
+    import torch
+    import int4_grouped_expert_gb300 as st
+    try:
+        xg = xs_dev[0].clone()
+        side = torch.cuda.Stream()
+        with torch.cuda.stream(side):  # first call outside the capture (one-time host set-up)
+            st.check(st.strata_moe_stack_forward(structs, xg, T, out, ws, need, side), "stack")
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            s = torch.cuda.current_stream()
+            st.check(st.strata_moe_stack_forward(structs, xg, T, out, ws, need, s), "stack")
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps * 1e3
+    except Exception as exc:  # noqa: BLE001 - reported, not fatal
+        print(f"stack graph capture unavailable: {exc}", file=sys.stderr)
+        return None
+
+
 def run_stack(args):
     """The 8-layer decode stack (hidden 4096, expert inter 2048, 128 experts top-4 + shared, a
     Zipf router per layer, residual add between layers) through strata_moe_stack_forward, for
@@ -581,6 +612,7 @@ def run_stack(args):
             torch.cuda.synchronize()
             barrier()
         ms = max_over_ranks(e0.elapsed_time(e1)) / steps
+        graph_us = stack_graph_us(structs, xs_dev, T, out, ws, need, steps, args.warmup)
         # per-stage times of single layers (events between the kernels), same inputs and layers
         wsl = torch.empty(max(L.workspace_size(T) for L in layers), dtype=torch.uint8, device="cuda")
         _, stages = time_steps(layers, xs_dev, T, min(steps, 400), args.warmup, stream, wsl,
@@ -591,6 +623,7 @@ def run_stack(args):
                          "us_per_stack": ms * 1e3, "us_per_layer": ms * 1e3 / wl.layers,
                          "experts_per_layer": float(np.mean(n_exp)),
                          "hbm_gbs": st_bytes / (ms / 1e3) / 1e9, "steps": steps,
+                         "us_per_stack_graph": graph_us,
                          "stages_us": {k: v * 1e3 for k, v in stages.items()}}
     clk = clocks.stop()
     peak, peak_kind = peak_numbers()
