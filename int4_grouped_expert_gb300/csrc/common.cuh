@@ -22,7 +22,8 @@ struct WsHeader {
   int32_t next_dn;      // dynamic scheduler: next down item
   uint32_t route_done;  // CTAs of the fused router that finished their logits
   int32_t n_chunks;     // warp path: 8-row chunks in the chunk list
-  int32_t pad[56];
+  uint32_t topk_done;   // CTAs of the fused router that finished their share of the top-k
+  int32_t pad[55];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

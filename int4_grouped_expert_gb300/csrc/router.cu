@@ -185,7 +185,6 @@ __host__ __device__ static size_t route_small_smem(const RouteSmallArgs& a) {
 __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   extern __shared__ __align__(16) unsigned char rs_smem[];
   __shared__ float red[kRsWarps][kRouteSmallMaxT];
-  __shared__ int is_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = a.T, H = a.H, E = a.E;
   griddep_launch();  // the gate/up GEMM may launch now; it waits for this grid before reading
@@ -193,19 +192,6 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   const int slot = warp / wpe, part = warp - slot * wpe;
   const int e = blockIdx.x * a.epc + slot;
 
-  // the decode grouped GEMM reads x with every 8-wide chunk pair-interleaved; the CTAs share the copy
-  if (a.x_perm) {
-    const int nv = T * (H / 8);
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += gridDim.x * blockDim.x) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
-      uint4 o;
-      o.x = prmt(v.x, v.z, 0x5410);
-      o.y = prmt(v.x, v.z, 0x7632);
-      o.z = prmt(v.y, v.w, 0x5410);
-      o.w = prmt(v.y, v.w, 0x7632);
-      reinterpret_cast<uint4*>(a.x_perm)[i] = o;
-    }
-  }
   // logits: each warp dots its H slice of one router row with every token, 4 tokens x 4 vectors
   // of 8 columns per lane and pass, all loads of a pass in flight together
   const int nvec = H / 8;
@@ -268,37 +254,90 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
     if (a.bias) v += a.bias[ee];
     a.logits[static_cast<int64_t>(t) * E + ee] = v;
   }
+  // the decode grouped GEMM reads x with every 8-wide chunk pair-interleaved; the CTAs share the copy
+  // (after the logits: only the GEMMs, which wait for this grid, read it)
+  if (a.x_perm) {
+    const int nv = T * (H / 8);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += gridDim.x * blockDim.x) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
+      uint4 o;
+      o.x = prmt(v.x, v.z, 0x5410);
+      o.y = prmt(v.x, v.z, 0x7632);
+      o.z = prmt(v.y, v.w, 0x5410);
+      o.w = prmt(v.y, v.w, 0x7632);
+      reinterpret_cast<uint4*>(a.x_perm)[i] = o;
+    }
+  }
 
-  // last CTA: softmax + top-k of every token, then the grouping
+  // The last G CTAs to finish their logits (G = one warp per token, 8 tokens per CTA) wait for
+  // the others, take the top-k of their tokens, and the last of them groups the rows. With one
+  // such CTA (T <= 8) the ids stay in its shared memory.
+  __shared__ int role_s;
+  const int G = min(static_cast<int>(gridDim.x), (T + kRsWarps - 1) / kRsWarps);
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned prev = atomicAdd(&a.grp.hdr->route_done, 1u);
-    is_last = (prev == gridDim.x - 1) ? 1 : 0;
+    int r = static_cast<int>(prev) - (static_cast<int>(gridDim.x) - G);
+    if (r >= 0 && prev != gridDim.x - 1) {
+      // wait (bounded, ~1 s) for the CTAs still writing logits: all of them run already (this
+      // grid's dependents launch only once every CTA of it has started)
+      const long long t0 = clock64();
+      while (*reinterpret_cast<volatile unsigned*>(&a.grp.hdr->route_done) < gridDim.x) {
+        __nanosleep(64);
+        if (clock64() - t0 > 2000000000ll) {
+          set_status(a.grp.status, STRATA_DEV_TIMEOUT);
+          r = -1;  // give up: no top-k from this CTA, the status tells the host
+          break;
+        }
+      }
+    }
+    role_s = r;
   }
   __syncthreads();
-  if (!is_last) return;
+  const int role = role_s;
+  if (role < 0) return;
   __threadfence();
 
   int* s_ids = reinterpret_cast<int*>(rs_smem + route_small_ids_off(a));
   float* s_gates = reinterpret_cast<float*>(s_ids + T * a.k);
-  // tokens warp, warp + 8, ... (up to 4 at once per warp), logits read from L2 into registers
-  const int tpw = T <= kRsWarps ? 1 : (T <= 2 * kRsWarps || E > 512) ? 2 : 4;
+  if (G == 1) {
+    // tokens warp, warp + 8, ... (up to 4 at once per warp), logits read from L2 into registers
+    const int tpw = T <= kRsWarps ? 1 : (T <= 2 * kRsWarps || E > 512) ? 2 : 4;
 #pragma unroll 1
-  for (int t0 = warp; t0 < T; t0 += kRsWarps * tpw) {
-    if (tpw == 1)
-      warp_softmax_topk<1, true>(a.logits, E, t0, kRsWarps, T, E, a.k, a.flags, s_ids, s_gates);
-    else if (tpw == 2)
-      warp_softmax_topk<2, true>(a.logits, E, t0, kRsWarps, T, E, a.k, a.flags, s_ids, s_gates);
-    else
-      warp_softmax_topk<4, true>(a.logits, E, t0, kRsWarps, T, E, a.k, a.flags, s_ids, s_gates);
+    for (int t0 = warp; t0 < T; t0 += kRsWarps * tpw) {
+      if (tpw == 1)
+        warp_softmax_topk<1, true>(a.logits, E, t0, kRsWarps, T, E, a.k, a.flags, s_ids, s_gates);
+      else if (tpw == 2)
+        warp_softmax_topk<2, true>(a.logits, E, t0, kRsWarps, T, E, a.k, a.flags, s_ids, s_gates);
+      else
+        warp_softmax_topk<4, true>(a.logits, E, t0, kRsWarps, T, E, a.k, a.flags, s_ids, s_gates);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < T * a.k; i += blockDim.x) {
+      a.ids[i] = s_ids[i];
+      a.gates[i] = s_gates[i];
+    }
+  } else {
+    // one token per warp: token role * 8 + warp, results straight to global memory
+    const int t = role * kRsWarps + warp;
+    if (t < T) warp_softmax_topk<1, true>(a.logits, E, t, 1, T, E, a.k, a.flags, a.ids, a.gates);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const unsigned prev = atomicAdd(&a.grp.hdr->topk_done, 1u);
+      role_s = (prev == static_cast<unsigned>(G) - 1u) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!role_s) return;
+    __threadfence();
+    for (int i = threadIdx.x; i < T * a.k; i += blockDim.x) s_ids[i] = __ldcg(a.ids + i);
+    __syncthreads();
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < T * a.k; i += blockDim.x) {
-    a.ids[i] = s_ids[i];
-    a.gates[i] = s_gates[i];
+  if (threadIdx.x == 0) {
+    a.grp.hdr->route_done = 0;
+    a.grp.hdr->topk_done = 0;
   }
-  if (threadIdx.x == 0) a.grp.hdr->route_done = 0;
   if (a.do_group) {
     if (route_small_compact_group(a))
       group_rows_small<kRsWarps>(a.grp, s_ids, reinterpret_cast<int*>(rs_smem));
