@@ -13,30 +13,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const __nv_bfloat16* __restrict__ x, int T,
                                                       int H, int k, int has_shared, int R,
                                                       int residual, __nv_bfloat16* __restrict__ out) {
+  griddep_wait();  // y comes from the down GEMM
   const int t = blockIdx.x;
   const int64_t H4 = H / 4;
-  const int64_t tk = static_cast<int64_t>(t) * k;
-  // gates and rows come from the router (finished long before): read them before waiting
-  constexpr int kPre = 8;
-  float gpre[kPre];
-  int rpre[kPre];
-#pragma unroll
-  for (int j = 0; j < kPre; ++j) {
-    gpre[j] = j < k ? __ldg(gates + tk + j) : 0.f;
-    rpre[j] = j < k ? __ldg(inv + tk + j) : 0;
-  }
-  griddep_wait();  // y comes from the down GEMM
   for (int64_t c = blockIdx.y * blockDim.x + threadIdx.x; c < H4; c += gridDim.y * blockDim.x) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int j = 0; j < kPre; ++j) {
-      if (j >= k) break;
-      const float4 v =
-          __ldcg(reinterpret_cast<const float4*>(y + static_cast<int64_t>(rpre[j]) * H) + c);
-      acc.x = fmaf(gpre[j], v.x, acc.x); acc.y = fmaf(gpre[j], v.y, acc.y);
-      acc.z = fmaf(gpre[j], v.z, acc.z); acc.w = fmaf(gpre[j], v.w, acc.w);
-    }
-    for (int j = kPre; j < k; ++j) {
+    const int64_t tk = static_cast<int64_t>(t) * k;
+    // rows and gates first, then all row loads: the k loads are independent
+#pragma unroll 8
+    for (int j = 0; j < k; ++j) {
       const float g = gates[tk + j];
       const int row = inv[tk + j];
       const float4 v = __ldcg(reinterpret_cast<const float4*>(y + static_cast<int64_t>(row) * H) + c);

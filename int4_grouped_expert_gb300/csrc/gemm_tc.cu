@@ -9,9 +9,12 @@
 //   warp 1       MMA issuer: one thread issues tcgen05.mma (M=128, N=rows, K=16) into TMEM
 //   warp 2       owns the TMEM allocation
 //   warps 4..11  dequant producers: int4 codes (global) -> bf16(q*s) written in the same swizzled
-//                K-major layout (the A operand), then the epilogue: TMEM -> registers -> global
-// D[weight row][token] accumulates in TMEM (gate at column 0, up at column 256). Gate/up writes
-// h = silu(gate) * up as bf16; down writes y in fp32 for the combine.
+//                K-major layout (the A operand)
+//   warps 12..15 epilogue: TMEM -> registers -> global
+// D[weight row][token] accumulates in TMEM: gate/up in one 512-column buffer (gate, then up);
+// down in two 256-column buffers, so its MMAs for the next tile run while the epilogue drains
+// this one. While the epilogue runs, the dequant warps already fill the next tile's stages.
+// Gate/up writes h = silu(gate) * up as bf16; down writes y in fp32 for the combine.
 //
 // Contraction order: inside every 8-wide chunk the K order is (0,4,1,5,2,6,3,7). That is the
 // order in which one LOP3 per pair unpacks the codes, so the activations are stored in it too (by
@@ -31,8 +34,8 @@ namespace strata {
 
 constexpr int kTcBM = 128;       // weight rows per tile (MMA M)
 constexpr int kTcBK = 64;        // contraction per stage: one 128-byte swizzle row of bf16
-constexpr int kTcNMax = 256;     // token rows per tile (MMA N)
-constexpr int kTcThreads = 384;  // 12 warps
+constexpr int kTcNMax = kTcRows;  // token rows per tile (MMA N)
+constexpr int kTcThreads = 512;   // 16 warps
 constexpr int kTcBoxRows = 128;  // TMA box: 128 token rows x 64 columns (16 KB)
 constexpr int kTcBoxBytes = kTcBoxRows * kTcBK * 2;
 
@@ -43,7 +46,9 @@ struct TcCfg {
   static constexpr int B_BYTES = kTcNMax * kTcBK * 2;  // 32 KB
   static constexpr int NMAT = kGateUp ? 2 : 1;
   static constexpr int STAGE_BYTES = NMAT * A_BYTES + B_BYTES;
-  static constexpr uint32_t TMEM_COLS = kGateUp ? 512 : 256;
+  static constexpr uint32_t ACC_COLS = NMAT * kTcNMax;  // one accumulator buffer
+  static constexpr int NBUF = kGateUp ? 1 : 2;          // accumulator buffers (512 columns)
+  static constexpr uint32_t TMEM_COLS = NBUF * ACC_COLS;
   static constexpr size_t SMEM = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + 256;
 };
 
@@ -107,9 +112,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* full_a = bars;
   uint64_t* full_b = bars + ST;
   uint64_t* empty = bars + 2 * ST;
-  uint64_t* acc_full = bars + 3 * ST;
-  uint64_t* acc_empty = bars + 3 * ST + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * ST + 2);
+  uint64_t* acc_full = bars + 3 * ST;       // [2]
+  uint64_t* acc_empty = bars + 3 * ST + 2;  // [2]
+  uint64_t* drain = bars + 3 * ST + 4;      // abort path: completion of the issued MMAs
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * ST + 5);
   __shared__ int abort_flag_s;
   volatile int* abort_flag = &abort_flag_s;
 
@@ -120,8 +126,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::mbar_init(full_b + s, 1);
       tc::mbar_init(empty + s, 1);
     }
-    tc::mbar_init(acc_full, 1);
-    tc::mbar_init(acc_empty, 8);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(acc_full + b, 1);
+      tc::mbar_init(acc_empty + b, 4);  // the 4 epilogue warps
+    }
+    tc::mbar_init(drain, 1);
     tc::fence_barrier_init();
     abort_flag_s = 0;
   }
@@ -175,7 +184,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         TcTile t;
         tc_decode(a, item, nseg, mtiles, t);
         const uint32_t idesc = tc::idesc_bf16(kTcBM, t.nmma);
-        if (tcount > 0 && !tc::mbar_wait(acc_empty, (tcount - 1) & 1, abort_flag, a.status)) {
+        const int buf = tcount % C::NBUF;
+        const uint32_t dtm = tmem + buf * C::ACC_COLS;
+        // the epilogue has drained this buffer (the tile NBUF back)
+        if (tcount >= C::NBUF && !tc::mbar_wait(acc_empty + buf, ((tcount / C::NBUF) - 1) & 1,
+                                                abort_flag, a.status)) {
           ok = false;
           break;
         }
@@ -196,22 +209,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int kk = 0; kk < kTcBK / 16; ++kk) {
             const uint32_t acc = (kb | kk) ? 1u : 0u;
             // +32 bytes per 16-wide K step inside the swizzle row (address field is in 16 B)
-            tc::mma_bf16_ss(tmem, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-            if (kGateUp) tc::mma_bf16_ss(tmem + 256, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+            tc::mma_bf16_ss(dtm, da0 + 2 * kk, db + 2 * kk, idesc, acc);
+            if (kGateUp) tc::mma_bf16_ss(dtm + kTcNMax, da1 + 2 * kk, db + 2 * kk, idesc, acc);
           }
           tc::mma_commit(empty + s);
         }
         if (!ok) break;
-        tc::mma_commit(acc_full);
+        tc::mma_commit(acc_full + buf);
       }
       if (!ok) {  // drain every MMA issued so far before TMEM is released
-        tc::mma_commit(acc_empty);
-        tc::mbar_wait_drain(acc_empty, tcount & 1);
+        tc::mma_commit(drain);
+        tc::mbar_wait_drain(drain, 0);
       }
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------------ dequant + epilogue
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------------ dequant producers
     const int pt = threadIdx.x - 128;  // 0..255
     const int mat = kGateUp ? (pt >> 7) : 0;
     const int half = kGateUp ? 0 : (pt >> 7);
@@ -220,11 +233,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const __half* scales = mat ? a.scales1 : a.scales0;
     const int64_t row_bytes = a.K / 2;
     const int64_t srow = a.K / kGroup;
-    const int q4 = warp & 3;       // TMEM lane quarter of this warp
-    const int wg = (warp - 4) >> 2;  // epilogue: warpgroup 0 / 1 take alternating column blocks
-    int it = 0, tcount = 0;
+    int it = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++tcount) {
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       TcTile t;
       tc_decode(a, item, nseg, mtiles, t);
       const int64_t wrow = static_cast<int64_t>(t.e) * a.Nw + t.mt * kTcBM + r;
@@ -287,17 +298,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       if (!ok) break;
-      // epilogue
-      if (!tc::mbar_wait(acc_full, tcount & 1, abort_flag, a.status)) { ok = false; break; }
+    }
+    __syncwarp();
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------------ epilogue
+    const int q4 = warp & 3;  // TMEM lane quarter of this warp
+    int tcount = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++tcount) {
+      TcTile t;
+      tc_decode(a, item, nseg, mtiles, t);
+      const int buf = tcount % C::NBUF;
+      if (!tc::mbar_wait(acc_full + buf, (tcount / C::NBUF) & 1, abort_flag, a.status)) {
+        ok = false;
+        break;
+      }
       tc::tc_fence_after();
       const int irow = t.mt * kTcBM + q4 * 32 + lane;  // weight row = output column
-      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
-      for (int c = wg * 32; c < t.nmma; c += 64) {
+      const uint32_t lane_addr = tmem + buf * C::ACC_COLS + (static_cast<uint32_t>(q4 * 32) << 16);
+      for (int c = 0; c < t.nmma; c += 32) {
         uint32_t g[32];
         tc::tmem_ld32(lane_addr + c, g);
         if (kGateUp) {
           uint32_t u[32];
-          tc::tmem_ld32(lane_addr + 256 + c, u);
+          tc::tmem_ld32(lane_addr + kTcNMax + c, u);
           tc::tmem_ld_wait();
           __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.out);
           const int col = (irow & ~7) | pair_pos(irow & 7);
@@ -321,7 +345,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(acc_empty);
+      if (lane == 0) tc::mbar_arrive(acc_empty + buf);
     }
   }
   tc::tc_fence_before();
