@@ -481,7 +481,9 @@ def run_prefill(args):
     stream = torch.cuda.Stream()
     steps = args.steps
     clocks = ClockSampler(local)
+    torch.cuda.nvtx.range_push("timed")
     elapsed_ms, _ = time_steps([L], xs_dev, T, steps, args.warmup, stream, ws, ws_bytes, out)
+    torch.cuda.nvtx.range_pop()
     clk = clocks.stop()
     _, stages = time_steps([L], xs_dev, T, steps, args.warmup, stream, ws, ws_bytes, out,
                            profiled=True)

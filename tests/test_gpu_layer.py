@@ -47,8 +47,10 @@ def test_c1_single_layer_64_tokens():
     check_layer(wl, L, wr, b, gen.activations(64, wl.H, wl.seed))
 
 
-@pytest.mark.parametrize("T", [1, 7, 63, 200])
+@pytest.mark.parametrize("T", [1, 7, 63, 100, 200])
 def test_c1_ragged_batches(T):
+    # 1..64: one-launch router + CTA-staged GEMM; 100: multi-launch router, row gather, CTA-staged
+    # GEMM; 200: tensor-core GEMM
     wl, L, wr, b = layer_for("c1")
     check_layer(wl, L, wr, b, gen.activations(T, wl.H, wl.seed, name=f"ragged{T}"))
 
@@ -86,6 +88,15 @@ def test_dense_equivalence_on_gpu():
     wr = np.zeros((wl.E, wl.H), np.float32)
     L, wr, b = build_gpu_layer(wl, w_router=wr)
     check_layer(wl, L, wr, b, gen.activations(9, wl.H, 4))
+
+
+def test_largest_expert_count_and_top_k():
+    """1023 routed experts + the shared one (the library's maximum) and k = 32, 64 tokens: 2048
+    routed rows, more than the compact grouping handles, so the general grouping runs."""
+    wl = Workload("tmax", "max", H=256, I=128, E=1023, k=32, shared=1, batches=(64,),
+                  router="uniform")
+    L, wr, b = build_gpu_layer(wl)
+    check_layer(wl, L, wr, b, gen.activations(64, wl.H, 11), rows=[0, 1, 31, 63])
 
 
 def test_all_tokens_one_expert():
