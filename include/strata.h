@@ -218,6 +218,18 @@ strata_status strata_moe_forward_ex(const strata_moe_layer* layer, const void* x
                                     void* workspace, size_t ws_bytes, strata_stream stream);
 
 /*
+ * strata_moe_forward_stats — strata_moe_forward that also accumulates expert-activation statistics
+ * (the hot-expert list of "Strata" 3090 tuning, xdnf.cn/news/329730, §5.5): expert_rows[e] +=
+ * rows routed to expert e in this batch, and expert_rows[E] += T for the shared expert.
+ * expert_rows: [E + has_shared] uint64, device, 8-byte aligned, caller-owned and caller-zeroed;
+ * calls on several streams may accumulate into the same array (atomic adds). Results and errors
+ * are those of strata_moe_forward; STRATA_ERR_INVALID_ARG if expert_rows is NULL or unaligned.
+ */
+strata_status strata_moe_forward_stats(const strata_moe_layer* layer, const void* x_bf16,
+                                       int64_t T, void* out_bf16, uint64_t* expert_rows,
+                                       void* workspace, size_t ws_bytes, strata_stream stream);
+
+/*
  * strata_moe_forward_profiled — strata_moe_forward that also records caller-created CUDA events
  * (cudaEvent_t, passed as void*) on `stream` at the stage boundaries, for per-kernel timing:
  *   events[0] before the router, [1] after the router (logits + top-k), [2] after the grouping,

@@ -67,6 +67,8 @@ _SIGNATURES = {
     "strata_moe_forward": (ctypes.c_int, [ctypes.POINTER(strata_moe_layer), _P, _I64, _P, _P, _SZ, _P]),
     "strata_moe_forward_ex": (ctypes.c_int, [ctypes.POINTER(strata_moe_layer), _P, _I64, _P,
                                              _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "strata_moe_forward_stats": (ctypes.c_int, [ctypes.POINTER(strata_moe_layer), _P, _I64, _P, _P,
+                                                 _P, _SZ, _P]),
     "strata_moe_forward_profiled": (ctypes.c_int, [ctypes.POINTER(strata_moe_layer), _P, _I64, _P, _P,
                                                    _SZ, _P, ctypes.POINTER(_P), _I32]),
     "strata_moe_stack_workspace_size": (_SZ, [ctypes.POINTER(strata_moe_layer), _I32, _I64]),
@@ -168,6 +170,11 @@ def strata_moe_workspace_size(layer: strata_moe_layer, T_max: int) -> int:
 def strata_moe_forward(layer, x, T, out, workspace, ws_bytes, stream=None):
     return lib().strata_moe_forward(ctypes.byref(layer), ptr(x), T, ptr(out), ptr(workspace),
                                     ws_bytes, stream_handle(stream))
+
+
+def strata_moe_forward_stats(layer, x, T, out, expert_rows, workspace, ws_bytes, stream=None):
+    return lib().strata_moe_forward_stats(ctypes.byref(layer), ptr(x), T, ptr(out), ptr(expert_rows),
+                                          ptr(workspace), ws_bytes, stream_handle(stream))
 
 
 def strata_moe_forward_ex(layer, x, T, out, ids=None, gates=None, counts=None, offsets=None,

@@ -117,8 +117,11 @@ __device__ void group_rows(const PermuteArgs& a, const int* ids, GroupSmem sm) {
     sm.off[e] = run;
     a.counts[e] = c;
     a.offsets[e] = run;
+    if (a.hits && c > 0) atomicAdd(a.hits + e, static_cast<unsigned long long>(c));
     run += c;
   }
+  if (a.hits && a.has_shared && tid == 0 && a.T > 0)
+    atomicAdd(a.hits + E, static_cast<unsigned long long>(a.T));
   if (tid == 0) {
     a.offsets[E] = total;
     sm.off[E] = total;
@@ -317,6 +320,7 @@ __device__ void group_rows_small(const PermuteArgs& a, const int* ids, int* smem
     off[e] = row0;
     a.counts[e] = c;
     a.offsets[e] = row0;
+    if (a.hits && c > 0) atomicAdd(a.hits + e, static_cast<unsigned long long>(c));
     if (c > 0) {
       const int sidx = static_cast<int>((run >> 21) & 0x1FFFFF) + sh;
       a.seg_expert[sidx] = e;
@@ -331,6 +335,7 @@ __device__ void group_rows_small(const PermuteArgs& a, const int* ids, int* smem
     }
   }
   if (tid == 0) {
+    if (a.hits && sh) atomicAdd(a.hits + E, static_cast<unsigned long long>(a.T));
     a.offsets[E] = static_cast<int>(tot & 0x1FFFFF);
     if (sh) {
       a.seg_expert[0] = E;

@@ -25,6 +25,7 @@ struct PermuteArgs {
   int ksplit_dn;     // down contraction splits per tile (1 = none)
   int cnt_per_chunk; // split-K arrival counters per chunk (zeroed here)
   int* split_cnt;    // arrival counters of the split-K reductions
+  unsigned long long* hits;  // optional [E + has_shared]: += rows routed to each expert (statistics)
   int4* chunk_list;  // warp path: {expert, first row, rows, 0} per tokc-row chunk (else null)
   WsHeader* hdr;
   uint32_t* status;

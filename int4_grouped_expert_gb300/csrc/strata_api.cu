@@ -153,7 +153,8 @@ struct Taps {
 
 static strata_status run_forward(const strata_moe_layer* L, const void* x, int64_t T, void* out,
                                  const Taps* taps, void* ws, size_t ws_bytes, cudaStream_t st,
-                                 void* const* events = nullptr, bool keep_status = false) {
+                                 void* const* events = nullptr, bool keep_status = false,
+                                 unsigned long long* hits = nullptr) {
   auto mark = [&](int i) -> bool {
     if (!events || !events[i]) return true;
     return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
@@ -231,6 +232,7 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     pa.chunk_list = reinterpret_cast<int4*>(base + F.chunk_list);
   }
   pa.split_cnt = pa.cnt_per_chunk > 0 ? reinterpret_cast<int*>(base + F.split_cnt) : nullptr;
+  pa.hits = hits;
   pa.hdr = hdr;
   pa.status = &hdr->status;
 
@@ -467,6 +469,15 @@ strata_status strata_moe_forward_ex(const strata_moe_layer* layer, const void* x
   Taps t{ids, gates, counts, offsets, perm, inv};
   return run_forward(layer, x_bf16, T, out_bf16, &t, workspace, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+strata_status strata_moe_forward_stats(const strata_moe_layer* layer, const void* x_bf16,
+                                       int64_t T, void* out_bf16, uint64_t* expert_rows,
+                                       void* workspace, size_t ws_bytes, strata_stream stream) {
+  if (!expert_rows || !aligned(expert_rows, 8)) return STRATA_ERR_INVALID_ARG;
+  return run_forward(layer, x_bf16, T, out_bf16, nullptr, workspace, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream), nullptr, false,
+                     reinterpret_cast<unsigned long long*>(expert_rows));
 }
 
 strata_status strata_moe_forward_profiled(const strata_moe_layer* layer, const void* x_bf16,

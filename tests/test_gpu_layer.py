@@ -11,8 +11,8 @@ import numpy as np
 import pytest
 
 import oracle
-from helpers import (OracleExperts, bf16_tensor, build_gpu_layer, compare_output, compare_routing,
-                     run_forward)
+from helpers import (OracleExperts, bf16_tensor, bf16_to_np_bits, build_gpu_layer, compare_output,
+                     compare_routing, run_forward)
 from workloads import CONFIGS, Workload, gen
 
 pytestmark = pytest.mark.gpu
@@ -168,3 +168,52 @@ def test_tc_path_shared_expert_and_long_segments():
     wl = Workload("t2", "tc-edge", H=384, I=256, E=6, k=6, shared=1, batches=(600,), router="uniform")
     L, wr, b = build_gpu_layer(wl, flags=st.STRATA_FORCE_TC_PATH)
     check_layer(wl, L, wr, b, gen.activations(600, wl.H, 8))
+
+
+def test_expert_statistics_accumulate_across_calls():
+    """strata_moe_forward_stats adds each batch's routed rows per expert (and T for the shared
+    expert) into a caller-owned counter array; the output equals strata_moe_forward's."""
+    import torch
+    import int4_grouped_expert_gb300 as st
+    wl, L, wr, b = layer_for("c2")
+    hits = torch.zeros(wl.E + wl.shared, dtype=torch.int64, device="cuda")
+    expect = np.zeros(wl.E + wl.shared, np.int64)
+    for T, name in ((16, "stats16"), (5, "stats5"), (64, "stats64")):
+        xb = gen.activations(T, wl.H, wl.seed, name=name)
+        x = bf16_tensor(xb)
+        out = torch.empty_like(x)
+        ws = torch.empty(L.workspace_size(T), dtype=torch.uint8, device="cuda")
+        st.check(st.strata_moe_forward_stats(L.struct(), x, T, out, hits, ws, ws.numel()), "stats")
+        ref = run_forward(L, xb, taps=True)
+        np.testing.assert_array_equal(bf16_to_np_bits(out), ref["out"])
+        expect[:wl.E] += ref["counts"]
+        expect[wl.E] += T
+    np.testing.assert_array_equal(hits.cpu().numpy(), expect)
+
+
+def test_forward_replays_from_a_cuda_graph():
+    """The forward captured once in a CUDA graph (fixed buffers, PDL chain inside) and replayed on
+    new inputs copied into the captured input buffer gives the direct call's results."""
+    import torch
+    import int4_grouped_expert_gb300 as st
+    wl, L, wr, b = layer_for("c2")
+    T = 8
+    x_static = torch.empty(T, wl.H, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(x_static)
+    ws = torch.empty(L.workspace_size(T), dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    x_static.copy_(bf16_tensor(gen.activations(T, wl.H, wl.seed, name="graph0")))
+    with torch.cuda.stream(side):  # first call outside the capture (one-time host set-up)
+        st.check(st.strata_moe_forward(L.struct(), x_static, T, out, ws, ws.numel(), side), "fwd")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        s = torch.cuda.current_stream()
+        st.check(st.strata_moe_forward(L.struct(), x_static, T, out, ws, ws.numel(), s), "capture")
+    for name in ("graph1", "graph2"):
+        xb = gen.activations(T, wl.H, wl.seed, name=name)
+        x_static.copy_(bf16_tensor(xb))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = run_forward(L, xb)
+        np.testing.assert_array_equal(bf16_to_np_bits(out), ref["out"])
