@@ -156,7 +156,8 @@ def layer_copies(L0, n):
     out = [L0]
     for _ in range(n - 1):
         L = MoELayer(L0.H, L0.I, L0.E, L0.k, L0.shared)
-        L.w_router.copy_(L0.w_router)
+        L.w_router = L0.w_router.clone()
+        L.flags = L0.flags
         L.bias = L0.bias
         L.copy_expert_from(L0)
         out.append(L)
@@ -326,6 +327,8 @@ def run_strata(args):
     wl = CONFIGS[WORKLOAD]
     T = args.batch
     L0 = build_layer(wl)
+    if args.router_fp16:
+        L0.set_router(gen.router_weight(wl), gen.router_bias(wl), fp16=True)
     layers = layer_copies(L0, max(1, args.copies))
     stream = torch.cuda.Stream()
     xs_host, xs_dev = token_batches(wl, T, N_TOKEN_BATCHES)
@@ -387,6 +390,7 @@ def run_strata(args):
         "config": {"workload": wl.name, "tokens_per_step": T, "H": wl.H, "I": wl.I, "E": wl.E,
                    "k": wl.k, "shared": wl.shared, "router": "zipf(s=1.1), top-20% take 80%",
                    "weights": "int4 g128 codes + fp16 scales, quantized on device",
+                   "router_weights": "fp16" if args.router_fp16 else "fp32",
                    "l2": f"inputs larger than L2: {N_LAYER_COPIES} expert-storage copies x "
                          f"{N_TOKEN_BATCHES} token batches rotated per step",
                    "parallelism": f"replicas x{ws_n}"},
@@ -718,6 +722,8 @@ def main(argv=None):
                    help="c2: the decode layer (default, the headline); c3 / c5: prefill layers; "
                         "c4: the 8-layer decode stack")
     p.add_argument("--router", choices=["uniform", "zipf"], default=None)
+    p.add_argument("--router-fp16", action="store_true",
+                   help="decode: store the router weights as fp16 (STRATA_ROUTER_FP16)")
     p.add_argument("--experts", type=int, default=0, help="prefill: override the routed expert count")
     p.add_argument("--tokens", type=int, default=0,
                    help="prefill: override the batch; c4: run this batch only")

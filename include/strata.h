@@ -61,6 +61,9 @@ typedef enum {
 #define STRATA_RENORM 0x1u       /* renormalise the k gates of a token to sum to 1 (off by default:
                                     the pages never renormalise) */
 #define STRATA_ADD_RESIDUAL 0x2u /* moe_forward only: out = bf16(x + MoE(x)), one rounding */
+#define STRATA_ROUTER_FP16 0x4u  /* the router weights are fp16 [E, H] instead of fp32 ("Strata" MoE
+                                    tuning notes, lpnh.cn/news/2730718, §2.1: the router kept in
+                                    fp16); logits still accumulate in fp32 over exact products */
 /* Kernel-path selection of moe_forward (results agree within the layer tolerance; default: the
    tensor-core path from 128 tokens up, the warp path below). For tests and tuning. */
 #define STRATA_FORCE_WARP_PATH 0x100u /* mma.sync warp GEMMs, B from registers */
@@ -115,7 +118,8 @@ strata_status strata_quantize_groups(const void* w_fp16, int64_t n, int64_t k, i
  * ordered by (expert, token):
  *   counts[e]   rows routed to expert e;  offsets[e] = sum_{e'<e} counts[e'], offsets[E] = T*k
  *   perm[r]     token of row r;           inv[t,j] = row of (t, ids[t,j])
- * x_bf16 [T,H] bf16; w_router [E,H] fp32; bias [E] fp32 or NULL.
+ * x_bf16 [T,H] bf16; w_router [E,H] fp32 (fp16 when flags & STRATA_ROUTER_FP16: cast the
+ * pointer); bias [E] fp32 or NULL. flags: STRATA_RENORM | STRATA_ROUTER_FP16.
  * ids [T,k] int32, gates [T,k] fp32 (required); counts [E], offsets [E+1], perm [T*k],
  * inv [T,k] int32 (optional as a group: all four or none).
  * Limits: H % 128 == 0, 1 <= k <= min(E, 32), E <= 1024, T >= 0 (T == 0 writes counts/offsets
@@ -167,8 +171,9 @@ typedef struct {
   int32_t E;             /* routed experts, 1..1024 */
   int32_t k;             /* experts per token, 1..min(E, 32) */
   int32_t has_shared;    /* 0 or 1: expert E is always on, gate 1 */
-  uint32_t flags;        /* STRATA_RENORM | STRATA_ADD_RESIDUAL | STRATA_FORCE_*_PATH */
-  const float* w_router; /* [E, H] fp32 */
+  uint32_t flags;        /* STRATA_RENORM | STRATA_ADD_RESIDUAL | STRATA_ROUTER_FP16 |
+                            STRATA_FORCE_*_PATH */
+  const float* w_router; /* [E, H] fp32, or fp16 with STRATA_ROUTER_FP16 (cast the pointer) */
   const float* bias;     /* [E] fp32 or NULL */
   const uint8_t* gate_codes; const void* gate_scales; /* [E+S, I, H/2] u8, [E+S, I, H/128] fp16 */
   const uint8_t* up_codes;   const void* up_scales;   /* same shapes */

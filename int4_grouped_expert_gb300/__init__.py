@@ -20,6 +20,7 @@ STATUS_NAMES = ["STRATA_OK", "STRATA_ERR_INVALID_ARG", "STRATA_ERR_SHAPE", "STRA
                 "STRATA_ERR_TIMEOUT"]
 STRATA_RENORM = 0x1
 STRATA_ADD_RESIDUAL = 0x2
+STRATA_ROUTER_FP16 = 0x4
 STRATA_FORCE_WARP_PATH = 0x100
 STRATA_FORCE_TC_PATH = 0x200
 STRATA_DEV_NONFINITE = 0x1

@@ -72,7 +72,8 @@ struct TcArgs {
 // top-k for every token and groups the rows.
 struct RouteSmallArgs {
   const __nv_bfloat16* x;  // [T, H]
-  const float* wr;         // [E, H]
+  const void* wr;          // [E, H] fp32, or fp16 with wr_fp16
+  bool wr_fp16;
   const float* bias;       // [E] or null
   int T, H, E, k;
   uint32_t flags;
@@ -88,7 +89,7 @@ struct RouteSmallArgs {
 cudaError_t launch_quantize(const void* w, int64_t n, int64_t k, uint8_t* codes, void* scales,
                             uint32_t* status, cudaStream_t stream, int num_sms);
 int router_num_splits(int64_t T, int64_t H, int E, int num_sms);
-cudaError_t launch_router(const void* x, const float* wr, const float* bias, int64_t T, int64_t H,
+cudaError_t launch_router(const void* x, const void* wr, const float* bias, int64_t T, int64_t H,
                           int E, int k, uint32_t flags, int nsplit, float* partial, int* ids,
                           float* gates, cudaStream_t stream);
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t stream);

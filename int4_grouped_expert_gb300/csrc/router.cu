@@ -182,6 +182,7 @@ __host__ __device__ static size_t route_small_smem(const RouteSmallArgs& a) {
   return route_small_ids_off(a) + static_cast<size_t>(a.T) * a.k * 8;
 }
 
+template <bool kF16>
 __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   extern __shared__ __align__(16) unsigned char rs_smem[];
   __shared__ float red[kRsWarps][kRouteSmallMaxT];
@@ -196,7 +197,9 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   // of 8 columns per lane and pass, all loads of a pass in flight together
   const int nvec = H / 8;
   const int vb = part * nvec / wpe, ve = (part + 1) * nvec / wpe;
-  const float4* wrow = reinterpret_cast<const float4*>(a.wr + static_cast<int64_t>(e < E ? e : 0) * H);
+  const int64_t wro = static_cast<int64_t>(e < E ? e : 0) * H;
+  const float4* wrow = reinterpret_cast<const float4*>(static_cast<const float*>(a.wr) + wro);
+  const uint4* wrow16 = reinterpret_cast<const uint4*>(static_cast<const __half*>(a.wr) + wro);
   const uint4* xv = reinterpret_cast<const uint4*>(a.x);
   constexpr int TB = 8;  // tokens per pass: every load of a pass is in flight together
   for (int t0 = 0; t0 < T; t0 += TB) {
@@ -209,8 +212,17 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
         for (int i = 0; i < 4; ++i) {
           const int v = v0 + 32 * i;
           if (v < ve) {
-            w[i][0] = __ldg(wrow + 2 * v);
-            w[i][1] = __ldg(wrow + 2 * v + 1);
+            if (kF16) {
+              const uint4 hv = __ldg(wrow16 + v);
+              const __half2* h2 = reinterpret_cast<const __half2*>(&hv);
+              const float2 f0 = __half22float2(h2[0]), f1 = __half22float2(h2[1]);
+              const float2 f2 = __half22float2(h2[2]), f3 = __half22float2(h2[3]);
+              w[i][0] = make_float4(f0.x, f0.y, f1.x, f1.y);
+              w[i][1] = make_float4(f2.x, f2.y, f3.x, f3.y);
+            } else {
+              w[i][0] = __ldg(wrow + 2 * v);
+              w[i][1] = __ldg(wrow + 2 * v + 1);
+            }
 #pragma unroll
             for (int tt = 0; tt < TB; ++tt)
               if (t0 + tt < T) xr[tt][i] = __ldg(xv + static_cast<int64_t>(t0 + tt) * nvec + v);
@@ -351,103 +363,26 @@ cudaError_t launch_route_small(const RouteSmallArgs& a, cudaStream_t stream) {
   const dim3 grid((a.E + a.epc - 1) / a.epc);
   const size_t smem = route_small_smem(a);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(route_small_kernel,
+    cudaError_t e = cudaFuncSetAttribute(route_small_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(route_small_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  route_small_kernel<<<grid, kRsWarps * 32, smem, stream>>>(a);
+  if (a.wr_fp16)
+    route_small_kernel<true><<<grid, kRsWarps * 32, smem, stream>>>(a);
+  else
+    route_small_kernel<false><<<grid, kRsWarps * 32, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
 // ----------------------------------------------------------------------------- large batches
 
-constexpr int kRouterBT = 32;  // tokens per CTA tile
-constexpr int kRouterBE = 64;  // experts per CTA tile
-constexpr int kRouterKC = 32;  // H chunk staged in shared memory
-
-__global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16* __restrict__ x,
-                                                            const float* __restrict__ wr, int T,
-                                                            int H, int E, int h_per_split,
-                                                            float* __restrict__ partial) {
-  __shared__ float xs[kRouterKC][kRouterBT + 1];
-  __shared__ float ws[kRouterKC][kRouterBE + 4];
-  const int tid = threadIdx.x;
-  const int e0 = blockIdx.x * kRouterBE;
-  const int t0 = blockIdx.y * kRouterBT;
-  const int split = blockIdx.z;
-  const int hbeg = split * h_per_split;
-  const int hend = min(H, hbeg + h_per_split);
-  const int tx = tid & 15;  // experts tx*4 .. tx*4+3
-  const int ty = tid >> 4;  // tokens ty*2, ty*2+1
-  float acc[2][4] = {}, comp[2][4] = {};
-
-  for (int hc = hbeg; hc < hend; hc += kRouterKC) {
-    {  // x tile: 32 tokens x 32 h, 4 bf16 per thread
-      const int tok = tid >> 3, kq = (tid & 7) * 4;
-      const int t = t0 + tok;
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (t < T) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(x + static_cast<int64_t>(t) * H + hc + kq);
-        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&raw);
-        float2 a = __bfloat1622float2(p[0]), b = __bfloat1622float2(p[1]);
-        v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) xs[kq + c][tok] = v[c];
-    }
-    {  // router tile: 64 experts x 32 h fp32, 8 floats per thread
-      const int er = tid >> 2, kq = (tid & 3) * 8;
-      const int e = e0 + er;
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-      if (e < E) {
-        const float4* p = reinterpret_cast<const float4*>(wr + static_cast<int64_t>(e) * H + hc + kq);
-        a = __ldg(p);
-        b = __ldg(p + 1);
-      }
-      ws[kq + 0][er] = a.x; ws[kq + 1][er] = a.y; ws[kq + 2][er] = a.z; ws[kq + 3][er] = a.w;
-      ws[kq + 4][er] = b.x; ws[kq + 5][er] = b.y; ws[kq + 6][er] = b.z; ws[kq + 7][er] = b.w;
-    }
-    __syncthreads();
-    float part[2][4] = {};
-#pragma unroll 8
-    for (int kk = 0; kk < kRouterKC; ++kk) {
-      const float a0 = xs[kk][ty * 2], a1 = xs[kk][ty * 2 + 1];
-      const float4 b = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
-      part[0][0] = fmaf(a0, b.x, part[0][0]); part[0][1] = fmaf(a0, b.y, part[0][1]);
-      part[0][2] = fmaf(a0, b.z, part[0][2]); part[0][3] = fmaf(a0, b.w, part[0][3]);
-      part[1][0] = fmaf(a1, b.x, part[1][0]); part[1][1] = fmaf(a1, b.y, part[1][1]);
-      part[1][2] = fmaf(a1, b.z, part[1][2]); part[1][3] = fmaf(a1, b.w, part[1][3]);
-    }
-    // chunk sums enter the running total with compensated (Kahan) addition, so the rounding
-    // error stays at the level of one 32-term chunk instead of growing with H
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float y = part[i][j] - comp[i][j];
-        const float t = acc[i][j] + y;
-        comp[i][j] = (t - acc[i][j]) - y;
-        acc[i][j] = t;
-      }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int t = t0 + ty * 2 + i;
-    if (t >= T) continue;
-    float* out = partial + (static_cast<int64_t>(split) * T + t) * E;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + tx * 4 + j;
-      if (e < E) out[e] = acc[i][j];
-    }
-  }
-}
-
 // Large batches on tensor cores: logits = x Wr^T with Wr split exactly into three bf16 parts
-// (hi + mid + lo == the fp32 value), so every product x*part is exact and the mma.sync fp32
-// accumulation matches an fp32 GEMM. Tile 64 tokens x 64 experts, 8 warps (2 x 4), warp tile
+// (hi + mid + lo == the fp32 value; two parts for an fp16 router: 8 + 3 significant bits), so
+// every product x*part is exact and the mma.sync fp32 accumulation matches an fp32 GEMM. Tile 64 tokens x 64 experts, 8 warps (2 x 4), warp tile
 // 32 x 16; contraction staged 32 columns at a time (double-buffered cp.async for x, registers for
 // the fp32 router tile, split on the way into shared memory); every 256 columns the chunk sum joins
 // the running total with compensated (Kahan) addition. Split along H (blockIdx.z) like the SIMT
@@ -465,10 +400,12 @@ __device__ __forceinline__ void ldmatrix_x2(uint32_t (&r)[2], const void* p) {
                : "=r"(r[0]), "=r"(r[1]) : "r"(a));
 }
 
+template <bool kF16>
 __global__ void __launch_bounds__(256) router_logits_tc_kernel(const __nv_bfloat16* __restrict__ x,
-                                                               const float* __restrict__ wr, int T,
+                                                               const void* __restrict__ wr_, int T,
                                                                int H, int E, int h_per_split,
                                                                float* __restrict__ partial) {
+  constexpr int NSPLIT = kF16 ? 2 : 3;
   __shared__ __align__(16) __nv_bfloat16 xs[2][kRtT][kRtPad];
   __shared__ __align__(16) __nv_bfloat16 ws[3][kRtE][kRtPad];  // hi, mid, lo
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -486,15 +423,27 @@ __global__ void __launch_bounds__(256) router_logits_tc_kernel(const __nv_bfloat
   // router tile: 64 experts x 32 fp32 = 8 floats per thread
   const int wrr = tid >> 2, wc = (tid & 3) * 8;
   const bool wok = e0 + wrr < E;
-  const float* wsrc = wr + static_cast<int64_t>(wok ? e0 + wrr : 0) * H + wc;
+  const int64_t woff = static_cast<int64_t>(wok ? e0 + wrr : 0) * H + wc;
 
   auto stage_x = [&](int buf, int hc) { cp_async16(&xs[buf][xr][xc], xsrc + hc, xok); };
   auto stage_w = [&](int hc) {
     float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (wok) {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(wsrc + hc));
-      const float4 b = __ldg(reinterpret_cast<const float4*>(wsrc + hc) + 1);
-      f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+      if (kF16) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const __half*>(wr_) + woff + hc));
+        const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 ff = __half22float2(h2[i]);
+          f[2 * i] = ff.x;
+          f[2 * i + 1] = ff.y;
+        }
+      } else {
+        const float* wsrc = static_cast<const float*>(wr_) + woff + hc;
+        const float4 a = __ldg(reinterpret_cast<const float4*>(wsrc));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(wsrc) + 1);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+      }
     }
     __nv_bfloat16 hi[8], mid[8], lo[8];
 #pragma unroll
@@ -506,7 +455,7 @@ __global__ void __launch_bounds__(256) router_logits_tc_kernel(const __nv_bfloat
     }
     *reinterpret_cast<uint4*>(&ws[0][wrr][wc]) = *reinterpret_cast<uint4*>(hi);
     *reinterpret_cast<uint4*>(&ws[1][wrr][wc]) = *reinterpret_cast<uint4*>(mid);
-    *reinterpret_cast<uint4*>(&ws[2][wrr][wc]) = *reinterpret_cast<uint4*>(lo);
+    if (!kF16) *reinterpret_cast<uint4*>(&ws[2][wrr][wc]) = *reinterpret_cast<uint4*>(lo);
   };
 
   int buf = 0;
@@ -526,7 +475,7 @@ __global__ void __launch_bounds__(256) router_logits_tc_kernel(const __nv_bfloat
       for (int mi = 0; mi < 2; ++mi)
         ldmatrix_x4(a[mi], &xs[buf][wt + mi * 16 + (lane & 15)][ks + (lane >> 4) * 8]);
 #pragma unroll
-      for (int sp = 0; sp < 3; ++sp) {
+      for (int sp = 0; sp < NSPLIT; ++sp) {
 #pragma unroll
         for (int ni = 0; ni < 2; ++ni) {
           uint32_t b[2];
@@ -602,7 +551,7 @@ int router_num_splits(int64_t T, int64_t H, int E, int num_sms) {
   return static_cast<int>(want);
 }
 
-cudaError_t launch_router(const void* x, const float* wr, const float* bias, int64_t T, int64_t H,
+cudaError_t launch_router(const void* x, const void* wr, const float* bias, int64_t T, int64_t H,
                           int E, int k, uint32_t flags, int nsplit, float* partial, int* ids,
                           float* gates, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
@@ -612,9 +561,16 @@ cudaError_t launch_router(const void* x, const float* wr, const float* bias, int
   const int h_per_split = static_cast<int>(gps * 128);
   const int used = static_cast<int>((groups + gps - 1) / gps);
   dim3 grid((E + kRtE - 1) / kRtE, static_cast<unsigned>((T + kRtT - 1) / kRtT), used);
-  router_logits_tc_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), wr,
-                                                    static_cast<int>(T), static_cast<int>(H), E,
-                                                    h_per_split, partial);
+  if (flags & STRATA_ROUTER_FP16)
+    router_logits_tc_kernel<true><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x),
+                                                            wr, static_cast<int>(T),
+                                                            static_cast<int>(H), E, h_per_split,
+                                                            partial);
+  else
+    router_logits_tc_kernel<false><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x),
+                                                             wr, static_cast<int>(T),
+                                                             static_cast<int>(H), E, h_per_split,
+                                                             partial);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const size_t smem = static_cast<size_t>(8) * E * sizeof(float);

@@ -127,7 +127,7 @@ static strata_status check_layer(const strata_moe_layer* L) {
   if (L->has_shared != 0 && L->has_shared != 1) return STRATA_ERR_INVALID_ARG;
   if (L->E < 1 || L->E + L->has_shared > STRATA_MAX_EXPERTS) return STRATA_ERR_UNSUPPORTED;
   if (L->k < 1 || L->k > L->E || L->k > STRATA_MAX_TOPK) return STRATA_ERR_INVALID_ARG;
-  if (L->flags & ~(STRATA_RENORM | STRATA_ADD_RESIDUAL | STRATA_FORCE_WARP_PATH |
+  if (L->flags & ~(STRATA_RENORM | STRATA_ADD_RESIDUAL | STRATA_ROUTER_FP16 | STRATA_FORCE_WARP_PATH |
                    STRATA_FORCE_TC_PATH))
     return STRATA_ERR_INVALID_ARG;
   if ((L->flags & STRATA_FORCE_WARP_PATH) && (L->flags & STRATA_FORCE_TC_PATH))
@@ -240,6 +240,7 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     RouteSmallArgs ra{};
     ra.x = static_cast<const __nv_bfloat16*>(x);
     ra.wr = L->w_router;
+    ra.wr_fp16 = (L->flags & STRATA_ROUTER_FP16) != 0;
     ra.bias = L->bias;
     ra.T = static_cast<int>(T);
     ra.H = static_cast<int>(L->H);
@@ -257,7 +258,8 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     if (e != cudaSuccess || !mark(1) || !mark(2)) return STRATA_ERR_CUDA;
   } else {
     const int nsplit = router_num_splits(T, L->H, E, sms);
-    e = launch_router(x, L->w_router, L->bias, T, L->H, E, k, L->flags & STRATA_RENORM, nsplit,
+    e = launch_router(x, L->w_router, L->bias, T, L->H, E, k,
+                      L->flags & (STRATA_RENORM | STRATA_ROUTER_FP16), nsplit,
                       reinterpret_cast<float*>(base + F.r.partial), ids, gates, st);
     if (e != cudaSuccess || !mark(1)) return STRATA_ERR_CUDA;
     e = launch_permute(pa, st);
@@ -404,7 +406,7 @@ strata_status strata_route_topk(const void* x_bf16, const float* w_router, const
   if (T < 0 || T > kMaxTokens || H <= 0 || H > kMaxDim || H % STRATA_GROUP) return STRATA_ERR_SHAPE;
   if (E < 1 || E > STRATA_MAX_EXPERTS) return STRATA_ERR_UNSUPPORTED;
   if (k < 1 || k > E || k > STRATA_MAX_TOPK) return STRATA_ERR_INVALID_ARG;
-  if (flags & ~STRATA_RENORM) return STRATA_ERR_INVALID_ARG;
+  if (flags & ~(STRATA_RENORM | STRATA_ROUTER_FP16)) return STRATA_ERR_INVALID_ARG;
   const bool any_group = counts || offsets || perm || inv;
   const bool all_group = counts && offsets && perm && inv;
   if (any_group && !all_group) return STRATA_ERR_INVALID_ARG;

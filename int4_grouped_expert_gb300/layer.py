@@ -32,9 +32,16 @@ class MoELayer:
         self._stage = None
 
     # ---------------------------------------------------------------- weights
-    def set_router(self, w_router, bias=None):
+    def set_router(self, w_router, bias=None, fp16: bool = False):
+        """Router weights [E,H]: fp32, or stored as fp16 (STRATA_ROUTER_FP16) when fp16=True."""
         import torch
-        self.w_router.copy_(torch.as_tensor(w_router, dtype=torch.float32))
+        from . import STRATA_ROUTER_FP16
+        if fp16:
+            self.w_router = torch.as_tensor(w_router).to(torch.float16).to(self.device)
+            self.flags |= STRATA_ROUTER_FP16
+        else:
+            self.w_router = torch.as_tensor(w_router, dtype=torch.float32).to(self.device)
+            self.flags &= ~STRATA_ROUTER_FP16
         self.bias = None if bias is None else torch.as_tensor(bias, dtype=torch.float32).to(self.device)
 
     def load_expert_fp16(self, e: int, gate, up, down, stream=None):

@@ -105,7 +105,7 @@ def test_route_host_checks(st):
     assert st.strata_route_topk(A, A, None, 8, 1000, 16, 2, 0, A, A, workspace=A, ws_bytes=ws) == 2
     assert st.strata_route_topk(A, A, None, 8, 1024, 16, 17, 0, A, A, workspace=A, ws_bytes=ws) == 1
     assert st.strata_route_topk(A, A, None, 8, 1024, 2000, 2, 0, A, A, workspace=A, ws_bytes=ws) == 3
-    assert st.strata_route_topk(A, A, None, 8, 1024, 16, 2, 4, A, A, workspace=A, ws_bytes=ws) == 1
+    assert st.strata_route_topk(A, A, None, 8, 1024, 16, 2, 8, A, A, workspace=A, ws_bytes=ws) == 1
     assert st.strata_route_topk(A, A, None, 8, 1024, 16, 2, 0, A, A, counts=A, workspace=A,
                                 ws_bytes=ws) == 1                          # partial grouping set
     assert st.strata_route_topk(A, A, None, 8, 1024, 16, 2, 0, A, A, workspace=A, ws_bytes=ws - 1) == 4

@@ -217,3 +217,14 @@ def test_forward_replays_from_a_cuda_graph():
         torch.cuda.synchronize()
         ref = run_forward(L, xb)
         np.testing.assert_array_equal(bf16_to_np_bits(out), ref["out"])
+
+
+@pytest.mark.parametrize("T", [16, 200])
+def test_fp16_router_layer(T):
+    """A layer whose router weights are stored as fp16: 16 tokens take the one-launch decode
+    router, 200 the tensor-core router and GEMMs."""
+    wl = CONFIGS["c1"]
+    wr16 = gen.router_weight(wl).astype(np.float16).astype(np.float32)
+    L, _, b = build_gpu_layer(wl, w_router=wr16)
+    L.set_router(wr16, b, fp16=True)
+    check_layer(wl, L, wr16, b, gen.activations(T, wl.H, wl.seed, name=f"r16_{T}"))

@@ -22,7 +22,8 @@ def gpu_route(x_bits, wr, bias, k, flags=0, group=True):
     T, H = x_bits.shape
     E = wr.shape[0]
     x = bf16_tensor(x_bits) if T else torch.zeros(1, H, dtype=torch.bfloat16, device="cuda")
-    w = torch.from_numpy(np.ascontiguousarray(wr, dtype=np.float32)).cuda()
+    wdt = np.float16 if flags & st.STRATA_ROUTER_FP16 else np.float32
+    w = torch.from_numpy(np.ascontiguousarray(wr, dtype=wdt)).cuda()
     b = None if bias is None else torch.from_numpy(np.asarray(bias, np.float32)).cuda()
     o = dict(ids=torch.full((max(T, 1), k), -1, dtype=torch.int32, device="cuda"),
              gates=torch.zeros(max(T, 1), k, dtype=torch.float32, device="cuda"))
@@ -104,3 +105,14 @@ def test_renorm_flag():
 def test_empty_batch():
     g = gpu_route(np.zeros((0, 128), np.uint16), np.zeros((4, 128), np.float32), None, 2)
     assert (g["counts"] == 0).all() and (g["offsets"] == 0).all()
+
+
+@pytest.mark.parametrize("key,T", [("c2", 16), ("c5", 1024)])
+def test_fp16_router(key, T):
+    """STRATA_ROUTER_FP16: the router weights stored as fp16 (the oracle gets the same fp16
+    values); logits still come from exact products summed in fp32."""
+    import int4_grouped_expert_gb300 as st
+    wl = CONFIGS[key]
+    x = gen.activations(T, wl.H, 0, name=f"route16/{key}")
+    wr16 = gen.router_weight(wl).astype(np.float16).astype(np.float32)
+    check(x, wr16, gen.router_bias(wl), wl.k, flags=st.STRATA_ROUTER_FP16)
