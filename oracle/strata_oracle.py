@@ -30,7 +30,9 @@ from __future__ import annotations
 
 import numpy as np
 
-GROUP = 128          # [tuning-moe] §2.1: 128 weights per group, 64 and 256 rejected
+GROUP = 128          # [tuning-moe] §2.1: 128 weights per group (the pages' choice)
+GROUPS = (64, 128, 256)  # the sketch takes group_size as a parameter; 64 and 256 are the sizes
+                         # the pages weighed against 128, kept as variants
 QMIN, QMAX = -8, 7   # [tuning-moe] §2.1: clamp(-8, 7) for bits = 4
 QDIV = 7.0           # [tuning-moe] §2.1: scale = absmax / (2**(bits-1) - 1)
 
@@ -69,8 +71,8 @@ def _check_weight(w16, group):
     w = np.asarray(w16)
     if w.dtype != np.float16 or w.ndim != 2:
         raise TypeError("weight must be a 2-D float16 array [out, in]")
-    if group != GROUP:
-        raise ValueError("group size must be 128")
+    if group not in GROUPS:
+        raise ValueError("group size must be 64, 128 or 256")
     if w.shape[1] % group:
         raise ValueError("in_features must be a multiple of the group size")
     if not np.all(np.isfinite(w)):
@@ -81,10 +83,10 @@ def _check_weight(w16, group):
 def quantize_groups(w16: np.ndarray, group: int = GROUP):
     """Symmetric int4 group quantization, [tuning-moe] §2.1 (group_quantize sketch).
 
-    weight [out, in] is viewed as [out, in/128, 128]; per group
+    weight [out, in] is viewed as [out, in/G, G] (G = group, 128 unless given); per group
       scale = absmax / 7, stored as fp16 (nearest-even),
       q     = clamp(round_half_even(w / scale), -8, 7)  with the exact quotient.
-    Returns (codes uint8 [out, in/2], scales float16 [out, in/128]).
+    Returns (codes uint8 [out, in/2], scales float16 [out, in/G]).
     """
     w = _check_weight(w16, group)
     n, kdim = w.shape
@@ -118,10 +120,12 @@ def quantize_groups_f16_quotient(w16: np.ndarray, group: int = GROUP):
     return pack_codes(q), scale16
 
 
-def dequantize(codes: np.ndarray, scales: np.ndarray, group: int = GROUP) -> np.ndarray:
-    """q * scale in fp64, [out, in]."""
+def dequantize(codes: np.ndarray, scales: np.ndarray, group: int = None) -> np.ndarray:
+    """q * scale in fp64, [out, in]; the group size follows from the shapes unless given."""
     q = unpack_codes(codes).astype(np.float64)
     n, kdim = q.shape
+    if group is None:
+        group = kdim // np.asarray(scales).shape[1]
     s = np.asarray(scales, dtype=np.float16).astype(np.float64)
     return (q.reshape(n, kdim // group, group) * s[..., None]).reshape(n, kdim)
 

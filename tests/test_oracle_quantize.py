@@ -73,9 +73,9 @@ def brute_quantize_group(ws):
     return s, qs
 
 
-def _groups_from(w16, n_groups, rng):
+def _groups_from(w16, n_groups, rng, group=128):
     rows = rng.integers(0, w16.shape[0], n_groups)
-    gs = rng.integers(0, w16.shape[1] // 128, n_groups)
+    gs = rng.integers(0, w16.shape[1] // group, n_groups)
     return [(int(r), int(g)) for r, g in zip(rows, gs)]
 
 
@@ -177,7 +177,48 @@ def test_shape_and_finiteness_errors():
     with pytest.raises(ValueError):
         oracle.quantize_groups(bad)
     with pytest.raises(ValueError):
-        oracle.quantize_groups(np.zeros((1, 128), dtype=np.float16), group=64)
+        oracle.quantize_groups(np.zeros((1, 128), dtype=np.float16), group=32)
+    with pytest.raises(ValueError):
+        oracle.quantize_groups(np.zeros((1, 128), dtype=np.float16), group=256)  # 128 % 256
+
+
+# ---------------------------------------------------------------- other group sizes
+
+@pytest.mark.parametrize("group", [64, 256])
+def test_other_group_sizes_brute_force(group):
+    """The group size is a parameter of the sketch: every group of G weights gets its own
+    absmax / 7 scale; checked group by group by exact rational search."""
+    rng = np.random.default_rng(7 + group)
+    w = gen.expert_weight(0, 0, 2, "down", 8, 1024)
+    codes, scales = oracle.quantize_groups(w, group=group)
+    assert scales.shape == (8, 1024 // group) and codes.shape == (8, 512)
+    q = oracle.unpack_codes(codes)
+    for r, g in _groups_from(w, 8, rng, group):
+        s, qs = brute_quantize_group(w[r, g * group:(g + 1) * group])
+        assert Fraction(float(scales[r, g])) == s
+        np.testing.assert_array_equal(q[r, g * group:(g + 1) * group], qs)
+
+
+@pytest.mark.parametrize("group", [64, 256])
+def test_other_group_sizes_round_trip_and_dequantize(group):
+    w = gen.expert_weight(0, 0, 3, "gate", 16, 512)
+    codes, scales = oracle.quantize_groups(w, group=group)
+    d = oracle.dequantize(codes, scales)             # the group size follows from the shapes
+    s = np.repeat(scales.astype(np.float64), group, axis=1)
+    assert np.all(np.abs(w.astype(np.float64) - d) <= s / 2)
+    # a 64-group split of the same row refines the 128-group scales: each 64-scale <= its 128-scale
+    if group == 64:
+        _, s128 = oracle.quantize_groups(w)
+        assert np.all(scales.astype(np.float64).reshape(16, -1, 2).max(-1) == s128.astype(np.float64))
+
+
+def test_dequantize_layout_by_hand_group_64():
+    # 1 row x 128 in two 64-groups: codes 3 then -1, scales 0.5 and 4
+    q = np.zeros((1, 128), dtype=np.int8)
+    q[0, :64], q[0, 64:] = 3, -1
+    sc = np.array([[0.5, 4.0]], dtype=np.float16)
+    d = oracle.dequantize(oracle.pack_codes(q), sc)
+    assert d[0, 0] == 1.5 and d[0, 63] == 1.5 and d[0, 64] == -4.0 and d[0, 127] == -4.0
 
 
 def test_fp16_quotient_reading_differs_rarely():
