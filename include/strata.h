@@ -50,7 +50,7 @@ typedef enum {
   STRATA_OK = 0,
   STRATA_ERR_INVALID_ARG = 1,   /* null pointer, bad flag, k > E, ... */
   STRATA_ERR_SHAPE = 2,         /* a dimension is not a multiple of 128, or out of range */
-  STRATA_ERR_UNSUPPORTED = 3,   /* group size other than 128, or a size above a limit */
+  STRATA_ERR_UNSUPPORTED = 3,   /* group size not 64/128/256, or a size above a limit */
   STRATA_ERR_WORKSPACE = 4,     /* workspace null, misaligned or smaller than required */
   STRATA_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
   STRATA_ERR_DEVICE_STATUS = 6, /* the device status word reported a data fault */
@@ -88,15 +88,16 @@ int strata_version(void);
 /*
  * strata_quantize_groups — symmetric int4 group quantization, [tuning-moe] §2.1.
  *
- * For each row i of w and each group g of 128 consecutive columns:
- *   scale[i,g] = fp16_round_nearest_even(absmax(w[i, 128g : 128g+128]) / 7)
+ * For each row i of w and each group g of G = group_size consecutive columns:
+ *   scale[i,g] = fp16_round_nearest_even(absmax(w[i, Gg : Gg+G]) / 7)
  *   q[i,c]     = clamp(round_half_even(w[i,c] / scale[i,g]), -8, 7)   (exact quotient)
  *   a group whose stored scale is 0 gets q = 0.
  * w_fp16      [n, k] fp16, row-major (device).
  * codes       [n, k/2] uint8 (device, written): byte c of row i holds q[i,2c] in bits 0-3 and
  *             q[i,2c+1] in bits 4-7, as 4-bit two's complement.
- * scales_fp16 [n, k/128] fp16 (device, written).
- * group_size  must be 128 (STRATA_ERR_UNSUPPORTED otherwise); k % 128 != 0 -> STRATA_ERR_SHAPE;
+ * scales_fp16 [n, k/group_size] fp16 (device, written).
+ * group_size  128 (the pages' choice) or 64 / 256 (the sizes they weigh against it);
+ *             anything else -> STRATA_ERR_UNSUPPORTED; k % group_size != 0 -> STRATA_ERR_SHAPE;
  *             n == 0 is a no-op.
  * dev_status  optional device uint32 (NULL to skip): STRATA_DEV_NONFINITE is OR-ed in when a
  *             group holds inf/nan; such a group gets scale NaN and codes 0.
@@ -178,6 +179,9 @@ typedef struct {
   const uint8_t* gate_codes; const void* gate_scales; /* [E+S, I, H/2] u8, [E+S, I, H/128] fp16 */
   const uint8_t* up_codes;   const void* up_scales;   /* same shapes */
   const uint8_t* down_codes; const void* down_scales; /* [E+S, H, I/2] u8, [E+S, H, I/128] fp16 */
+  int32_t group_size;    /* scale group of all three projections: 128 (0 means 128), 64 or 256;
+                            the scales above are then [.., K/group_size]. 256 on the decode path
+                            needs H % 512 == 0 and I % 512 == 0 */
 } strata_moe_layer;
 
 /* Workspace bytes strata_moe_forward needs for up to T_max tokens (0 if the layer is invalid). */

@@ -45,6 +45,7 @@ class strata_moe_layer(ctypes.Structure):
         ("gate_codes", ctypes.c_void_p), ("gate_scales", ctypes.c_void_p),
         ("up_codes", ctypes.c_void_p), ("up_scales", ctypes.c_void_p),
         ("down_codes", ctypes.c_void_p), ("down_scales", ctypes.c_void_p),
+        ("group_size", ctypes.c_int32),
     ]
 
 

@@ -48,6 +48,7 @@ constexpr int kStageBytes = 19584;         // 128-byte multiple >= kHdrOff + siz
 constexpr int kBarOff = kStages * kStageBytes;
 constexpr int kSmemBytes = kBarOff + 2 * kStages * 8 + 16;
 constexpr int kCtasPerSm = 2;
+constexpr int kBlockK = 128;               // contraction per stage
 
 struct StageHdr {
   int e, rbase, nvalid, blk, ks, cidx;  // item: expert, first GEMM row, rows, row block, split, chunk
@@ -78,10 +79,24 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
                : "memory");
 }
 
+// Group sizes: the weights of a stage are one 128-wide contraction block. With 128-wide or 256-wide
+// scale groups (kG) the block has one scale per row; with 64-wide groups it has two, and lane t then
+// takes codes 16t..16t+15 of each 64-half (instead of 32t..32t+31 of the block) so that MMAs j = 0,1
+// stay inside the first group and j = 2,3 inside the second.
+//
+// Activation piece (16 bytes = 8 values) that feeds MMA step j of lane t.
+template <int kG>
+__device__ __forceinline__ int act_piece(int t, int j) {
+  return kG == 64 ? (j < 2 ? 2 * t + j : 8 + 2 * t + (j - 2)) : 4 * t + j;
+}
 // Position of 16-byte piece q (0..15) of activation row n inside the row. A 128-bit shared load
-// is served 8 lanes at a time: lanes 8p..8p+7 read rows 2p, 2p+1, pieces 4t + c (t = 0..3, fixed
-// c). The map sends those 8 pieces to 8 different 16-byte bank groups, so no load conflicts.
-__device__ __forceinline__ int act_swz(int n, int q) { return q ^ ((q >> 3) & 1) ^ ((n & 1) << 1); }
+// is served 8 lanes at a time: lanes 8p..8p+7 read rows 2p, 2p+1, pieces act_piece(t, c) for
+// t = 0..3 and a fixed c. The map sends those 8 pieces to 8 different 16-byte bank groups, so
+// the loads do not conflict.
+template <int kG>
+__device__ __forceinline__ int act_swz(int n, int q) {
+  return kG == 64 ? q ^ (n & 1) : q ^ ((q >> 3) & 1) ^ ((n & 1) << 1);
+}
 
 struct CtaGemmParams {
   GemmArgs a;
@@ -89,7 +104,7 @@ struct CtaGemmParams {
   int RB;     // rows per block (gate/up: per matrix)
 };
 
-template <bool kGateUp>
+template <bool kGateUp, int kG>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     grouped_gemm_cta_kernel(const __grid_constant__ CUtensorMap map0,
                             const __grid_constant__ CUtensorMap map1, const CtaGemmParams p) {
@@ -110,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   __syncthreads();
 
-  const int ngroups = a.K / kGroup;
+  const int ngroups = a.K / kBlockK;
   const int KS = a.ksplit;
 
   if (warp == kCW) {
@@ -124,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int* const next_ctr = kGateUp ? &a.hdr->next_gu : &a.hdr->next_dn;
     const int n_items = kGateUp ? a.hdr->n_items_gu : a.hdr->n_items_dn;
     const int nchunks = a.hdr->n_chunks;
-    const int64_t srow = a.K / kGroup;            // scale row stride (fp16)
+    const int64_t srow = a.K / kG;                // scale row stride (fp16)
     const int q = lane & 15;                      // activation piece of this lane
     const uint32_t tx_bytes = kGateUp ? 2u * p.RB * 64u : static_cast<uint32_t>(p.RB) * 64u;
     int stage = 0;
@@ -163,7 +178,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             tc::tma_load_2d(st + p.RB * 64, &map1, g * 64, static_cast<int32_t>(wrow0), &full[stage]);
         }
         // scales: the 4-byte fp16 pair holding group g, 8 rows per lane
-        const int gp = g & ~1;
+        // 4-byte scale pair holding this block's scale(s): groups 2g, 2g+1 (kG = 64), g (128) or
+        // g / 2 (256), the pair starting at an even group
+        const int gp = kG == 64 ? 2 * g : kG == 128 ? (g & ~1) : ((g >> 1) & ~1);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int r = lane + 32 * i;  // stage scale row
@@ -193,8 +210,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int n = 2 * i + (lane >> 4);
-            const uint32_t dst = tc::smem_u32(sst + kActOff + n * 256 + (act_swz(n, q) << 4));
-            cp_async16s(dst, reinterpret_cast<const char*>(arow[i] + gg * kGroup) + q * 16,
+            const uint32_t dst = tc::smem_u32(sst + kActOff + n * 256 + (act_swz<kG>(n, q) << 4));
+            cp_async16s(dst, reinterpret_cast<const char*>(arow[i] + gg * kBlockK) + q * 16,
                         avalid[i]);
           }
           cp_async_arrive_noinc(bar);
@@ -252,15 +269,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // weights: tile 0 rows (gate: w*16.., down: w*32..), tile 1 (up rows w*16.. / down w*32+16..)
     const unsigned char* t0 = st + (kGateUp ? warp * 16 : warp * 32) * 64;
     const unsigned char* t1 = kGateUp ? t0 + p.RB * 64 : t0 + 16 * 64;
-    const uint4 a0l = *reinterpret_cast<const uint4*>(t0 + gq * 64 + t4 * 16);
-    const uint4 a0h = *reinterpret_cast<const uint4*>(t0 + (gq + 8) * 64 + t4 * 16);
-    const uint4 a1l = *reinterpret_cast<const uint4*>(t1 + gq * 64 + t4 * 16);
-    const uint4 a1h = *reinterpret_cast<const uint4*>(t1 + (gq + 8) * 64 + t4 * 16);
+    // 16 bytes of codes per row: one piece of 16, or (64-wide groups) 8 from each 32-byte half
+    auto ldw = [&](const unsigned char* row) {
+      if (kG == 64) {
+        const uint2 lo = *reinterpret_cast<const uint2*>(row + t4 * 8);
+        const uint2 hi = *reinterpret_cast<const uint2*>(row + 32 + t4 * 8);
+        return make_uint4(lo.x, lo.y, hi.x, hi.y);
+      }
+      return *reinterpret_cast<const uint4*>(row + t4 * 16);
+    };
+    const uint4 a0l = ldw(t0 + gq * 64);
+    const uint4 a0h = ldw(t0 + (gq + 8) * 64);
+    const uint4 a1l = ldw(t1 + gq * 64);
+    const uint4 a1h = ldw(t1 + (gq + 8) * 64);
     uint32_t X[16];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const int qq = t4 * 4 + c;
-      const uint4 b = *reinterpret_cast<const uint4*>(st + kActOff + gq * 256 + (act_swz(gq, qq) << 4));
+      const int qq = act_piece<kG>(t4, c);
+      const uint4 b = *reinterpret_cast<const uint4*>(st + kActOff + gq * 256 + (act_swz<kG>(gq, qq) << 4));
       X[4 * c] = b.x; X[4 * c + 1] = b.y; X[4 * c + 2] = b.z; X[4 * c + 3] = b.w;
     }
     // scale pairs of rows gq, gq+8 of both tiles
@@ -278,11 +304,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     const uint32_t w0l[4] = {a0l.x, a0l.y, a0l.z, a0l.w}, w0h[4] = {a0h.x, a0h.y, a0h.z, a0h.w};
     const uint32_t w1l[4] = {a1l.x, a1l.y, a1l.z, a1l.w}, w1h[4] = {a1h.x, a1h.y, a1h.z, a1h.w};
-    // two accumulator sets (even / odd j) halve the MMA dependency chains
+    // two accumulator sets halve the MMA dependency chains: even / odd j, or (64-wide groups) the
+    // block's first and second group
     float p0[2][4] = {}, p1[2][4] = {}, cr[2][4] = {};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int h = j & 1;
+      const int h = kG == 64 ? (j >> 1) : (j & 1);
       // activations are stored pair-interleaved: X[4j+m] = {x[8j+m], x[8j+m+4]}
       const uint32_t b00 = X[4 * j], b01 = X[4 * j + 1], b10 = X[4 * j + 2], b11 = X[4 * j + 3];
       mma_bf16_16816(cr[h], a136, b00, b01, cr[h]);
@@ -306,18 +333,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         mma_bf16_16816(p1[h], fb, b10, b11, p1[h]);
       }
     }
-    // the scale of group g is the low half of its pair for even g, the high half for odd g
-    const int sh = (hd.g & 1) * 16;
-    const float sa0 = __half2float(__ushort_as_half(static_cast<unsigned short>(s0a >> sh)));
-    const float sb0 = __half2float(__ushort_as_half(static_cast<unsigned short>(s0b >> sh)));
-    const float sa1 = __half2float(__ushort_as_half(static_cast<unsigned short>(s1a >> sh)));
-    const float sb1 = __half2float(__ushort_as_half(static_cast<unsigned short>(s1b >> sh)));
+    auto h2f = [](uint32_t v, int sh) {
+      return __half2float(__ushort_as_half(static_cast<unsigned short>(v >> sh)));
+    };
+    if (kG == 64) {
+      // the pair holds the scales of the block's two groups
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const float q0 = (p0[0][c] - cr[0][c]) + (p0[1][c] - cr[1][c]);
-      const float q1 = (p1[0][c] - cr[0][c]) + (p1[1][c] - cr[1][c]);
-      acc0[c] = fmaf(c < 2 ? sa0 : sb0, q0, acc0[c]);
-      acc1[c] = fmaf(c < 2 ? sa1 : sb1, q1, acc1[c]);
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t s0 = c < 2 ? s0a : s0b, s1 = c < 2 ? s1a : s1b;
+        acc0[c] = fmaf(h2f(s0, 0), p0[0][c] - cr[0][c], acc0[c]);
+        acc0[c] = fmaf(h2f(s0, 16), p0[1][c] - cr[1][c], acc0[c]);
+        acc1[c] = fmaf(h2f(s1, 0), p1[0][c] - cr[0][c], acc1[c]);
+        acc1[c] = fmaf(h2f(s1, 16), p1[1][c] - cr[1][c], acc1[c]);
+      }
+    } else {
+      // the block's group is the low half of its pair for an even group index, the high half else
+      const int sh = ((kG == 128 ? hd.g : hd.g >> 1) & 1) * 16;
+      const float sa0 = h2f(s0a, sh), sb0 = h2f(s0b, sh), sa1 = h2f(s1a, sh), sb1 = h2f(s1b, sh);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float q0 = (p0[0][c] - cr[0][c]) + (p0[1][c] - cr[1][c]);
+        const float q1 = (p1[0][c] - cr[0][c]) + (p1[1][c] - cr[1][c]);
+        acc0[c] = fmaf(c < 2 ? sa0 : sb0, q0, acc0[c]);
+        acc1[c] = fmaf(c < 2 ? sa1 : sb1, q1, acc1[c]);
+      }
     }
     if (hd.g != hd.gend - 1) continue;
 
@@ -406,7 +445,7 @@ static bool make_codes_tmap(CUtensorMap* m, const void* base, int64_t rows, int6
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kGateUp>
+template <bool kGateUp, int kG>
 cudaError_t launch_t(const GemmArgs& a, int64_t experts, int num_sms, cudaStream_t stream) {
   CtaGemmParams p;
   p.a = a;
@@ -417,10 +456,10 @@ cudaError_t launch_t(const GemmArgs& a, int64_t experts, int num_sms, cudaStream
   if (!make_codes_tmap(&m0, a.codes0, rows, a.K, p.RB)) return cudaErrorInvalidValue;
   if (!make_codes_tmap(&m1, kGateUp ? a.codes1 : a.codes0, rows, a.K, p.RB))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_cta_kernel<kGateUp>,
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_cta_kernel<kGateUp, kG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_kernel(grouped_gemm_cta_kernel<kGateUp>, dim3(num_sms * kCtasPerSm),
+  return launch_kernel(grouped_gemm_cta_kernel<kGateUp, kG>, dim3(num_sms * kCtasPerSm),
                        dim3(kThreads), kSmemBytes, stream, true, m0, m1, p);
 }
 
@@ -431,15 +470,24 @@ int cta_gemm_warps() { return kCW; }
 
 cudaError_t launch_gemm_cta(const GemmArgs& a, bool gate_up, int64_t experts, int num_sms,
                             cudaStream_t stream) {
-  return gate_up ? launch_t<true>(a, experts, num_sms, stream)
-                 : launch_t<false>(a, experts, num_sms, stream);
+  switch (a.group) {
+    case 64:
+      return gate_up ? launch_t<true, 64>(a, experts, num_sms, stream)
+                     : launch_t<false, 64>(a, experts, num_sms, stream);
+    case 256:
+      return gate_up ? launch_t<true, 256>(a, experts, num_sms, stream)
+                     : launch_t<false, 256>(a, experts, num_sms, stream);
+    default:
+      return gate_up ? launch_t<true, 128>(a, experts, num_sms, stream)
+                     : launch_t<false, 128>(a, experts, num_sms, stream);
+  }
 }
 
 // Contraction splits for a batch whose grouped GEMM has `items` (chunk x row block) work items:
 // enough for about two items per CTA, each split keeping at least two 128-wide groups.
 int cta_gemm_ksplit(int64_t items, int64_t K, int num_sms) {
   const int64_t want = 2 * static_cast<int64_t>(num_sms) * kCtasPerSm;
-  const int64_t groups = K / kGroup;
+  const int64_t groups = K / kBlockK;
   int ks = 1;
   while (items * ks < want && 2 * ks * 2 <= groups && ks < 16) ks *= 2;
   return ks;

@@ -232,7 +232,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint8_t* codes = mat ? a.codes1 : a.codes0;
     const __half* scales = mat ? a.scales1 : a.scales0;
     const int64_t row_bytes = a.K / 2;
-    const int64_t srow = a.K / kGroup;
+    const int64_t srow = a.K / a.group;
+    // scale of stage kb (64 codes): group (64 kb) / G
+    const int gs = a.group == 64 ? 0 : a.group == 128 ? 1 : 2;
     int it = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
@@ -246,9 +248,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // is unrolled by 4 so slot u is refilled for stage kb + 4 right after stage kb used it
       constexpr int PD = 4;
       uint4 cA[PD], cB[PD];
-      // scale of the group of stage kb (one per stage pair), kept as raw fp16 bits: converting on
-      // load would make the load complete right away
-      unsigned short sc[PD / 2];
+      // scale of stage kb's group, kept as raw fp16 bits: converting on load would make the load
+      // complete right away
+      unsigned short sc[PD];
       auto ld = [&](int kb, uint4& x0, uint4& x1) {
         if (kb < nk) {
           x0 = __ldg(reinterpret_cast<const uint4*>(cp + static_cast<int64_t>(kb) * 32));
@@ -258,7 +260,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int u = 0; u < PD; ++u) {
         ld(u, cA[u], cB[u]);
-        if ((u & 1) == 0 && u < nk) sc[u / 2] = __ldg(reinterpret_cast<const unsigned short*>(sp) + (u >> 1));
+        if (u < nk) sc[u] = __ldg(reinterpret_cast<const unsigned short*>(sp) + (u >> gs));
       }
       for (int kb0 = 0; ok && kb0 < nk; kb0 += PD) {
 #pragma unroll
@@ -268,15 +270,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int s = it % ST;
           const uint32_t ph = (it / ST) & 1;
           // scale of this stage's group as a bf16 pair split: s = s_hi + s_lo
-          const float sf = __half2float(__ushort_as_half(sc[u / 2]));
+          const float sf = __half2float(__ushort_as_half(sc[u]));
           const __nv_bfloat16 hb = __float2bfloat16_rn(sf);
           const __nv_bfloat16 lb = __float2bfloat16_rn(sf - __bfloat162float(hb));
           const __nv_bfloat162 s_hi = __halves2bfloat162(hb, hb);
           const __nv_bfloat162 s_lo = __halves2bfloat162(lb, lb);
           const uint4 x0 = cA[u], x1 = cB[u];
           ld(kb + PD, cA[u], cB[u]);
-          if ((u & 1) == 1 && kb + PD - 1 < nk)
-            sc[u / 2] = __ldg(reinterpret_cast<const unsigned short*>(sp) + ((kb + PD - 1) >> 1));
+          if (kb + PD < nk)
+            sc[u] = __ldg(reinterpret_cast<const unsigned short*>(sp) + ((kb + PD) >> gs));
           if (!tc::mbar_wait(empty + s, ph ^ 1, abort_flag, a.status)) { ok = false; break; }
           uint8_t* dst = A_of(s, mat) + soff;
           const uint32_t wds[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};

@@ -48,6 +48,7 @@ struct GemmArgs {
   const int* seg_item;       // exclusive prefix of work items per segment, [nseg + 1]
   const int4* chunk_list;    // {expert, first row, rows, 0} per 8-row chunk
   int ksplit;                // contraction splits per tile (gate/up only)
+  int group;                 // scale group size: 64, 128 or 256 (CTA-staged kernel; others 128)
   float* split_part;         // [tiles * ksplit * 256] partial sums of split tiles
   int* split_cnt;            // [tiles] arrival counters (zero on entry)
 };
@@ -60,6 +61,7 @@ struct TcArgs {
   const __half* scales1;
   void* out;              // gate/up: h bf16 [rows, Nw] (pair-interleaved columns); down: y fp32
   int K, Nw;              // contraction; weight rows per expert
+  int group;              // scale group size: 64, 128 or 256
   WsHeader* hdr;
   const int* seg_expert;
   const int* seg_row0;
@@ -86,8 +88,8 @@ struct RouteSmallArgs {
   bool do_group;
 };
 
-cudaError_t launch_quantize(const void* w, int64_t n, int64_t k, uint8_t* codes, void* scales,
-                            uint32_t* status, cudaStream_t stream, int num_sms);
+cudaError_t launch_quantize(const void* w, int64_t n, int64_t k, int group, uint8_t* codes,
+                            void* scales, uint32_t* status, cudaStream_t stream, int num_sms);
 int router_num_splits(int64_t T, int64_t H, int E, int num_sms);
 cudaError_t launch_router(const void* x, const void* wr, const float* bias, int64_t T, int64_t H,
                           int E, int k, uint32_t flags, int nsplit, float* partial, int* ids,

@@ -1,11 +1,11 @@
 // K1: symmetric int4 group quantization ("Strata" MoE tuning notes, lpnh.cn/news/2730718, §2.1
 // group_quantize sketch: scale = absmax / (2^(bits-1) - 1), codes = round(w / scale) clamped to
-// [-8, 7], 128 weights per group).
+// [-8, 7], 128 weights per group by default; 64 and 256 are accepted too).
 //
-// HBM-streaming pass: 16 threads own one 128-wide group (8 fp16 = one 16-byte load each), find
-// the group's absmax with four butterfly shuffles, and write 4 bytes of packed codes each (the
-// half-warp's 64 bytes are contiguous) plus one fp16 scale. Each thread walks its groups with a
-// grid-stride loop, four groups' loads in flight at a time.
+// HBM-streaming pass: G/8 threads own one G-wide group (8 fp16 = one 16-byte load each), find the
+// group's absmax with butterfly shuffles, and write 4 bytes of packed codes each (the group's
+// G/2 bytes are contiguous) plus one fp16 scale. Each thread walks its groups with a grid-stride
+// loop, four groups' loads in flight at a time.
 //
 // Exactness: absmax / 7.0f is an IEEE fp32 division rounded once more to fp16 (no double-rounding
 // hazard: a/7 has a period-3 binary expansion, never 12 equal bits in a row), and w / s is an IEEE
@@ -15,7 +15,8 @@
 
 namespace strata {
 
-// One group: 16 lanes of a half-warp hold 8 fp16 each.
+// One group: TPG lanes hold 8 fp16 each.
+template <int TPG>
 __device__ __forceinline__ void quantize_one(const uint4& v, unsigned half_mask, int sub, int64_t g,
                                              uint32_t* __restrict__ codes,
                                              __half* __restrict__ scales, uint32_t* status) {
@@ -26,7 +27,7 @@ __device__ __forceinline__ void quantize_one(const uint4& v, unsigned half_mask,
   const uint32_t m2 = __vmaxu2(m01, m23);
   uint32_t mbits = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll
-  for (int o = 8; o > 0; o >>= 1) mbits = max(mbits, __shfl_xor_sync(half_mask, mbits, o));
+  for (int o = TPG / 2; o > 0; o >>= 1) mbits = max(mbits, __shfl_xor_sync(half_mask, mbits, o));
   const bool finite = mbits < 0x7C00u;
   const float amax = finite ? __half2float(__ushort_as_half(static_cast<unsigned short>(mbits))) : 0.f;
   const __half* h = reinterpret_cast<const __half*>(&v);
@@ -45,48 +46,60 @@ __device__ __forceinline__ void quantize_one(const uint4& v, unsigned half_mask,
     s_h = __ushort_as_half(0x7E00);  // NaN scale marks the group
     if (sub == 0) set_status(status, STRATA_DEV_NONFINITE);
   }
-  __stcs(codes + g * 16 + sub, packed);
+  __stcs(codes + g * TPG + sub, packed);
   if (sub == 0) scales[g] = s_h;
 }
 
-// Each half-warp walks groups g, g + stride, ... with four groups' loads in flight at a time.
+// Each TPG-lane team walks groups g, g + stride, ... with four groups' loads in flight at a time.
+template <int TPG>
 __global__ void __launch_bounds__(256) quantize_groups_kernel(const uint4* __restrict__ w,
                                                               int64_t n_groups,
                                                               uint32_t* __restrict__ codes,
                                                               __half* __restrict__ scales,
                                                               uint32_t* status) {
-  const int sub = threadIdx.x & 15;  // position in the group
-  // the two half-warps may leave the loop at different times: shuffle within the half only
-  const unsigned half_mask = (threadIdx.x & 16) ? 0xFFFF0000u : 0x0000FFFFu;
-  const int64_t first = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
-  const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 4;
+  const int sub = threadIdx.x & (TPG - 1);  // position in the group
+  // the teams of a warp may leave the loop at different times: shuffle within the team only
+  const unsigned team_mask =
+      TPG == 32 ? 0xFFFFFFFFu : (((1u << TPG) - 1u) << (threadIdx.x & 31 & ~(TPG - 1)));
+  const int64_t first = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / TPG;
+  const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) / TPG;
   constexpr int U = 4;
   for (int64_t g0 = first; g0 < n_groups; g0 += U * stride) {
     uint4 v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t g = g0 + u * stride;
-      if (g < n_groups) v[u] = __ldcs(w + g * 16 + sub);  // streaming: every weight read once
+      if (g < n_groups) v[u] = __ldcs(w + g * TPG + sub);  // streaming: every weight read once
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t g = g0 + u * stride;
-      if (g < n_groups) quantize_one(v[u], half_mask, sub, g, codes, scales, status);
+      if (g < n_groups) quantize_one<TPG>(v[u], team_mask, sub, g, codes, scales, status);
     }
   }
 }
 
-cudaError_t launch_quantize(const void* w, int64_t n, int64_t k, uint8_t* codes, void* scales,
-                            uint32_t* status, cudaStream_t stream, int num_sms) {
-  const int64_t n_groups = n * (k / kGroup);
+cudaError_t launch_quantize(const void* w, int64_t n, int64_t k, int group, uint8_t* codes,
+                            void* scales, uint32_t* status, cudaStream_t stream, int num_sms) {
+  const int64_t n_groups = n * (k / group);
   if (n_groups == 0) return cudaSuccess;
-  const int threads = 256;                       // 16 groups per block and pass
-  int64_t blocks = (n_groups + 15) / 16;
+  const int threads = 256;
+  const int tpg = group / 8;                     // threads per group
+  int64_t blocks = (n_groups * tpg + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;  // ~8 resident blocks/SM, grid-stride
   if (blocks > cap) blocks = cap;
-  quantize_groups_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<const uint4*>(w), n_groups, reinterpret_cast<uint32_t*>(codes),
-      static_cast<__half*>(scales), status);
+  const uint4* wv = static_cast<const uint4*>(w);
+  uint32_t* cv = reinterpret_cast<uint32_t*>(codes);
+  __half* sv = static_cast<__half*>(scales);
+  const unsigned b = static_cast<unsigned>(blocks);
+  if (tpg == 8)
+    quantize_groups_kernel<8><<<b, threads, 0, stream>>>(wv, n_groups, cv, sv, status);
+  else if (tpg == 16)
+    quantize_groups_kernel<16><<<b, threads, 0, stream>>>(wv, n_groups, cv, sv, status);
+  else if (tpg == 32)
+    quantize_groups_kernel<32><<<b, threads, 0, stream>>>(wv, n_groups, cv, sv, status);
+  else
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 

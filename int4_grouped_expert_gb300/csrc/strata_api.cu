@@ -63,6 +63,10 @@ static bool use_tc_path(const strata_moe_layer* L, int64_t T) {
   if (L->flags & STRATA_FORCE_TC_PATH) return true;
   return T >= 128;
 }
+static int layer_group(const strata_moe_layer* L) {
+  return L->group_size == 0 ? STRATA_GROUP : L->group_size;
+}
+
 static FwdLayout fwd_layout(const strata_moe_layer* L, int64_t T) {
   FwdLayout F{};
   F.r = route_layout(T, L->H, L->E, L->k, L->has_shared);
@@ -82,7 +86,10 @@ static FwdLayout fwd_layout(const strata_moe_layer* L, int64_t T) {
   F.y = o; o = up(o + sizeof(float) * rows * L->H);
   F.xp = o; o = up(o + sizeof(uint16_t) * rows * L->H);  // gathered / pair-interleaved x
   // the CTA-staged kernel reads scale pairs with 4-byte copies: even group counts only
+  // (256-wide groups: the pair holding a block's scale starts at an even group: K / 256 even)
+  const int G = layer_group(L);
   F.cta = !F.tc && !STRATA_WARP_GEMM_LEGACY && (L->H / 128) % 2 == 0 && (L->I / 128) % 2 == 0 &&
+          (G != 256 || ((L->H / 256) % 2 == 0 && (L->I / 256) % 2 == 0)) &&
           aligned(L->gate_scales, 4) && aligned(L->up_scales, 4) && aligned(L->down_scales, 4);
   F.ksplit = 1;
   F.ksplit_dn = 1;
@@ -123,7 +130,9 @@ static int device_sms(int* out) {
 static strata_status check_layer(const strata_moe_layer* L) {
   if (!L) return STRATA_ERR_INVALID_ARG;
   if (L->H <= 0 || L->I <= 0 || L->H > kMaxDim || L->I > kMaxDim) return STRATA_ERR_SHAPE;
-  if (L->H % STRATA_GROUP || L->I % STRATA_GROUP) return STRATA_ERR_SHAPE;
+  const int G = layer_group(L);
+  if (G != 64 && G != 128 && G != 256) return STRATA_ERR_UNSUPPORTED;
+  if (L->H % STRATA_GROUP || L->I % STRATA_GROUP || L->H % G || L->I % G) return STRATA_ERR_SHAPE;
   if (L->has_shared != 0 && L->has_shared != 1) return STRATA_ERR_INVALID_ARG;
   if (L->E < 1 || L->E + L->has_shared > STRATA_MAX_EXPERTS) return STRATA_ERR_UNSUPPORTED;
   if (L->k < 1 || L->k > L->E || L->k > STRATA_MAX_TOPK) return STRATA_ERR_INVALID_ARG;
@@ -167,6 +176,8 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
   if (!aligned(x, 16) || !aligned(out, 16)) return STRATA_ERR_INVALID_ARG;
   if (x == out) return STRATA_ERR_INVALID_ARG;
   const FwdLayout F = fwd_layout(L, T);
+  // the per-warp decode kernel (odd group counts, 2-byte-aligned scales) has 128-wide groups only
+  if (!F.tc && !F.cta && layer_group(L) != STRATA_GROUP) return STRATA_ERR_UNSUPPORTED;
   if (!ws || !aligned(ws, kAlign)) return STRATA_ERR_WORKSPACE;
   if (ws_bytes < F.total) return STRATA_ERR_WORKSPACE;
 
@@ -271,6 +282,7 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     e = launch_gather_rows(x, perm, rows, L->H, base + F.xp, st);
     if (e != cudaSuccess) return STRATA_ERR_CUDA;
     TcArgs g{};
+    g.group = layer_group(L);
     g.codes0 = L->gate_codes;
     g.scales0 = static_cast<const __half*>(L->gate_scales);
     g.codes1 = L->up_codes;
@@ -299,6 +311,7 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     if (e != cudaSuccess || !mark(4)) return STRATA_ERR_CUDA;
   } else {
     GemmArgs g{};
+    g.group = layer_group(L);
     g.codes0 = L->gate_codes;
     g.scales0 = static_cast<const __half*>(L->gate_scales);
     g.codes1 = L->up_codes;
@@ -378,8 +391,8 @@ int strata_version(void) { return 100; }
 strata_status strata_quantize_groups(const void* w_fp16, int64_t n, int64_t k, int32_t group_size,
                                      uint8_t* codes, void* scales_fp16, uint32_t* dev_status,
                                      strata_stream stream) {
-  if (group_size != STRATA_GROUP) return STRATA_ERR_UNSUPPORTED;
-  if (n < 0 || k <= 0 || k % STRATA_GROUP) return STRATA_ERR_SHAPE;
+  if (group_size != 64 && group_size != 128 && group_size != 256) return STRATA_ERR_UNSUPPORTED;
+  if (n < 0 || k <= 0 || k % group_size) return STRATA_ERR_SHAPE;
   if (n > (int64_t(1) << 40) / k) return STRATA_ERR_SHAPE;
   if (n == 0) return STRATA_OK;
   if (!w_fp16 || !codes || !scales_fp16) return STRATA_ERR_INVALID_ARG;
@@ -388,7 +401,7 @@ strata_status strata_quantize_groups(const void* w_fp16, int64_t n, int64_t k, i
     return STRATA_ERR_INVALID_ARG;
   int sms = 0;
   if (device_sms(&sms) != 0) return STRATA_ERR_CUDA;
-  return cuda_fail(launch_quantize(w_fp16, n, k, codes, scales_fp16, dev_status,
+  return cuda_fail(launch_quantize(w_fp16, n, k, group_size, codes, scales_fp16, dev_status,
                                    reinterpret_cast<cudaStream_t>(stream), sms));
 }
 

@@ -14,20 +14,21 @@ from . import (GROUP, StrataError, check, ptr, strata_moe_layer, strata_moe_work
 
 class MoELayer:
     def __init__(self, H: int, I: int, E: int, k: int, shared: int, flags: int = 0,
-                 device: str = "cuda"):
+                 device: str = "cuda", group: int = GROUP):
         import torch
         self.H, self.I, self.E, self.k, self.shared, self.flags = H, I, E, k, shared, flags
+        self.group = group
         self.device = torch.device(device)
         n = E + shared
         u8, f16, f32 = torch.uint8, torch.float16, torch.float32
         self.w_router = torch.zeros(E, H, dtype=f32, device=self.device)
         self.bias = None
         self.gate_codes = torch.zeros(n, I, H // 2, dtype=u8, device=self.device)
-        self.gate_scales = torch.zeros(n, I, H // GROUP, dtype=f16, device=self.device)
+        self.gate_scales = torch.zeros(n, I, H // group, dtype=f16, device=self.device)
         self.up_codes = torch.zeros(n, I, H // 2, dtype=u8, device=self.device)
-        self.up_scales = torch.zeros(n, I, H // GROUP, dtype=f16, device=self.device)
+        self.up_scales = torch.zeros(n, I, H // group, dtype=f16, device=self.device)
         self.down_codes = torch.zeros(n, H, I // 2, dtype=u8, device=self.device)
-        self.down_scales = torch.zeros(n, H, I // GROUP, dtype=f16, device=self.device)
+        self.down_scales = torch.zeros(n, H, I // group, dtype=f16, device=self.device)
         self._status = torch.zeros(1, dtype=torch.int32, device=self.device)
         self._stage = None
 
@@ -58,7 +59,8 @@ class MoELayer:
             dst.copy_(src, non_blocking=False)
             rows, cols = src.shape
             check(strata_quantize_groups(dst, rows, cols, codes[e], scales[e], self._status,
-                                         stream=stream), "strata_quantize_groups")
+                                         group_size=self.group, stream=stream),
+                  "strata_quantize_groups")
 
     def check_status(self, stream=None):
         st, v = strata_read_status(self._status, stream)
@@ -81,6 +83,7 @@ class MoELayer:
         s.gate_codes, s.gate_scales = ptr(self.gate_codes), ptr(self.gate_scales)
         s.up_codes, s.up_scales = ptr(self.up_codes), ptr(self.up_scales)
         s.down_codes, s.down_scales = ptr(self.down_codes), ptr(self.down_scales)
+        s.group_size = self.group
         return s
 
     def workspace_size(self, T_max: int) -> int:
@@ -88,7 +91,7 @@ class MoELayer:
 
     def expert_bytes(self) -> int:
         n = 3 * self.H * self.I
-        return n // 2 + 2 * (n // GROUP)
+        return n // 2 + 2 * (n // self.group)
 
 
 __all__ = ["MoELayer", "ctypes"]

@@ -49,7 +49,9 @@ def test_status_strings(st):
 def test_quantize_host_checks(st):
     A = 1 << 12  # a 16-byte aligned fake address: never dereferenced, checks fail first
     assert st.strata_quantize_groups(A, 4, 100, A, A) == 2
-    assert st.strata_quantize_groups(A, 4, 256, A, A, group_size=64) == 3
+    assert st.strata_quantize_groups(A, 4, 256, A, A, group_size=32) == 3
+    assert st.strata_quantize_groups(A, 4, 256, A, A, group_size=512) == 3
+    assert st.strata_quantize_groups(A, 4, 320, A, A, group_size=256) == 2   # 320 % 256
     assert st.strata_quantize_groups(None, 4, 256, A, A) == 1
     assert st.strata_quantize_groups(A + 2, 4, 256, A, A) == 1
     assert st.strata_quantize_groups(A, -1, 256, A, A) == 2

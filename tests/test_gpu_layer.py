@@ -33,7 +33,8 @@ def check_layer(wl, L, wr, b, x, layer=0, residual=False, renorm=False, rows=Non
                 overrides=None):
     g = run_forward(L, x)
     tokens = np.arange(x.shape[0]) if rows is None else np.asarray(rows)
-    ref = oracle.moe_forward(x, wr, b, wl.k, OracleExperts(wl, layer, overrides), wl.E, wl.shared,
+    experts = OracleExperts(wl, layer, overrides, group=getattr(L, "group", 128))
+    ref = oracle.moe_forward(x, wr, b, wl.k, experts, wl.E, wl.shared,
                              renorm=renorm, residual=residual, tokens=tokens)
     full_ref = oracle.route_topk(x, wr, b, wl.k, renorm=renorm)
     diff, _ = compare_routing(g, full_ref, wl.E)
@@ -228,3 +229,14 @@ def test_fp16_router_layer(T):
     L, _, b = build_gpu_layer(wl, w_router=wr16)
     L.set_router(wr16, b, fp16=True)
     check_layer(wl, L, wr16, b, gen.activations(T, wl.H, wl.seed, name=f"r16_{T}"))
+
+
+@pytest.mark.parametrize("group", [64, 256])
+@pytest.mark.parametrize("T", [16, 100, 200])
+def test_other_group_sizes(group, T):
+    """Experts quantized with 64- or 256-wide groups (codes and scales from the device kernel,
+    bit-exact vs the oracle), the forward on the decode path (16: one-launch router; 100:
+    multi-launch router) and the tensor-core path (200)."""
+    wl = CONFIGS["c1"]
+    L, wr, b = build_gpu_layer(wl, group=group)
+    check_layer(wl, L, wr, b, gen.activations(T, wl.H, wl.seed, name=f"g{group}_{T}"))

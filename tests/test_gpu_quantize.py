@@ -16,21 +16,21 @@ pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "quantize_cases.json")
 
 
-def gpu_quantize(w16: np.ndarray, status=None):
+def gpu_quantize(w16: np.ndarray, status=None, group=128):
     import torch
     import int4_grouped_expert_gb300 as st
     n, k = w16.shape
     w = torch.from_numpy(w16).cuda()
     codes = torch.full((n, k // 2), 0xAB, dtype=torch.uint8, device="cuda")
-    scales = torch.full((n, k // 128), 7.0, dtype=torch.float16, device="cuda")
-    st.check(st.strata_quantize_groups(w, n, k, codes, scales, status), "quantize")
+    scales = torch.full((n, k // group), 7.0, dtype=torch.float16, device="cuda")
+    st.check(st.strata_quantize_groups(w, n, k, codes, scales, status, group_size=group), "quantize")
     torch.cuda.synchronize()
     return codes.cpu().numpy(), scales.cpu().numpy()
 
 
-def assert_same(w16):
-    c, s = gpu_quantize(w16)
-    rc, rs = oracle.quantize_groups(w16)
+def assert_same(w16, group=128):
+    c, s = gpu_quantize(w16, group=group)
+    rc, rs = oracle.quantize_groups(w16, group=group)
     np.testing.assert_array_equal(s.view(np.uint16), rs.view(np.uint16))
     np.testing.assert_array_equal(c, rc)
 
@@ -109,6 +109,15 @@ def test_argument_errors_on_device_pointers():
     c = torch.zeros(4, 128, dtype=torch.uint8, device="cuda")
     s = torch.zeros(4, 2, dtype=torch.float16, device="cuda")
     assert st.strata_quantize_groups(w, 4, 200, c, s) == 2                     # SHAPE
-    assert st.strata_quantize_groups(w, 4, 256, c, s, group_size=64) == 3      # UNSUPPORTED
+    assert st.strata_quantize_groups(w, 4, 256, c, s, group_size=32) == 3      # UNSUPPORTED
     assert st.strata_quantize_groups(w.view(-1)[1:].data_ptr(), 1, 128, c, s) == 1  # misaligned
     assert st.strata_quantize_groups(w, 0, 256, c, s) == 0                     # empty
+
+
+@pytest.mark.parametrize("group", [64, 256])
+@pytest.mark.parametrize("n,k", [(1, 256), (37, 1280), (5, 7168)])
+def test_other_group_sizes(group, n, k):
+    """Group sizes 64 and 256: codes and scales bit-exact against the oracle."""
+    w = gen.expert_weight(2, 0, n, "down", n, k).astype(np.float32)
+    w *= np.float32(2.0 ** (-6 if group == 64 else 2))
+    assert_same(w.astype(np.float16), group=group)
