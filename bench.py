@@ -233,6 +233,25 @@ def time_steps(layers, xs_dev, T, steps, warmup, stream, ws, ws_bytes, out, prof
     return elapsed_ms, stages
 
 
+def step_percentiles(layers, xs_dev, T, steps, stream, ws, ws_bytes, out):
+    """p10 / p50 / p90 of single-step device times (an event pair around every step)."""
+    import torch
+    import int4_grouped_expert_gb300 as st
+    structs = [L.struct() for L in layers]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i, (a, b) in enumerate(evs):
+            a.record(stream)
+            st.check(st.strata_moe_forward(structs[i % len(structs)], xs_dev[i % len(xs_dev)], T,
+                                           out, ws, ws_bytes, stream), "forward")
+            b.record(stream)
+        torch.cuda.synchronize()
+    us = np.array([a.elapsed_time(b) * 1e3 for a, b in evs])
+    return {"p10": float(np.percentile(us, 10)), "p50": float(np.percentile(us, 50)),
+            "p90": float(np.percentile(us, 90)), "steps": steps}
+
+
 def time_e2e(L, xs_host, T, steps, warmup, stream):
     """Through the C ABI with host buffers: H2D of x and D2H of out inside every call."""
     import torch
@@ -254,7 +273,18 @@ def time_e2e(L, xs_host, T, steps, warmup, stream):
     return dt, nbytes
 
 
-def cpu_baseline(wl, xs_host, T, budget_s=20.0):
+def oracle_one_thread(T):
+    """The same oracle sample in a child process with every BLAS pool limited to one thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", str(T)],
+                           env=env, capture_output=True, text=True, timeout=300)
+        return float(r.stdout.strip().splitlines()[-1])
+    except Exception:  # noqa: BLE001 - reported as missing, not fatal
+        return None
+
+
+def cpu_baseline(wl, xs_host, T, budget_s=20.0, one_thread=True):
     """The fp64 oracle on the host cores, on a bounded sample of the batch's tokens."""
     import oracle
     from workloads.gen import router_bias, router_weight
@@ -280,11 +310,14 @@ def cpu_baseline(wl, xs_host, T, budget_s=20.0):
             break
     dt = time.perf_counter() - t0
     threads = os.environ.get("OMP_NUM_THREADS") or os.environ.get("OPENBLAS_NUM_THREADS")
-    return {"value": tokens / dt, "unit": "tokens/s", "cores": int(threads) if threads else
-            (os.cpu_count() or 1), "kind": "oracle",
+    rec = {"value": tokens / dt, "unit": "tokens/s", "cores": int(threads) if threads else
+           (os.cpu_count() or 1), "kind": "oracle",
             "sample": f"{n_tok} token of the T={T} batch per pass ({tokens} tokens, {dt:.1f} s): "
                       f"fp64 routing over all {wl.E} experts, dequant + FFN of its "
                       f"{wl.k} routed experts and the shared one; experts pre-quantized"}
+    if one_thread:
+        rec["one_thread_value"] = oracle_one_thread(T)
+    return rec
 
 
 def kernels_per_forward(T):
@@ -351,6 +384,7 @@ def run_strata(args):
     # per-stage times from a second, profiled pass (events between the kernels)
     _, stages = time_steps(layers, xs_dev, T, min(args.steps, 2000), args.warmup, stream, ws,
                            ws_bytes, out, profiled=True)
+    step_pct = step_percentiles(layers, xs_dev, T, min(args.steps, 1000), stream, ws, ws_bytes, out)
     elapsed_s = elapsed_ms / 1e3
     value = aggregate_throughput(T * args.steps, elapsed_s, ws_n)
     ms_step = max_over_ranks(elapsed_ms) / args.steps
@@ -402,6 +436,7 @@ def run_strata(args):
         "layer_hbm": {"achieved_gbs": layer_gbs, "frac": layer_gbs / peak,
                       "bytes_per_step": n_exp * eb, "experts_per_step": n_exp},
         "stages_us": {k: v * 1e3 for k, v in stages.items()},
+        "step_us_percentiles": step_pct,
         "sweep": sweep,
         "e2e": e2e,
         "gpu_launches": kernels_per_forward(T) * args.steps,
@@ -729,7 +764,13 @@ def main(argv=None):
     p.add_argument("--experts", type=int, default=0, help="prefill: override the routed expert count")
     p.add_argument("--tokens", type=int, default=0,
                    help="prefill: override the batch; c4: run this batch only")
+    p.add_argument("--oracle-sample", type=int, default=0, help=argparse.SUPPRESS)
     args = p.parse_args(argv)
+    if args.oracle_sample:  # child of cpu_baseline: the oracle sample alone, tokens/s on stdout
+        wl = CONFIGS[WORKLOAD]
+        xs = [gen.activations(args.oracle_sample, wl.H, wl.seed, name=f"bench/{args.oracle_sample}/0")]
+        print(cpu_baseline(wl, xs, args.oracle_sample, one_thread=False)["value"])
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.steps is None:
