@@ -82,6 +82,23 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
+// L2 policy for data a kernel streams once per call (expert weights and scales, router weights):
+// evicted before normal lines, so that the layer's small reused state (code, activations,
+// routing buffers) stays in L2 while hundreds of MB of weights pass through it.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// 16-byte read-only load with an L2 policy.
+__device__ __forceinline__ uint4 ldg_hint(const uint4* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+
 // silu(u) = u * sigmoid(u) with the fast exp and divide intrinsics (a few ulp of fp32: the result
 // is rounded to bf16 right after). Large negative u: exp overflows to inf and the quotient is 0.
 __device__ __forceinline__ float silu_f(float u) { return __fdividef(u, 1.0f + __expf(-u)); }

@@ -65,9 +65,10 @@ __device__ __forceinline__ uint32_t codes_to_bf16_biased(uint32_t v) {
   return d;
 }
 
-__device__ __forceinline__ void cp_async4(uint32_t saddr, const void* gmem, bool pred) {
+__device__ __forceinline__ void cp_async4(uint32_t saddr, const void* gmem, bool pred, uint64_t pol) {
   const int sz = pred ? 4 : 0;
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(saddr), "l"(gmem), "r"(sz));
+  asm volatile("cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 4, %2, %3;\n" ::"r"(saddr),
+               "l"(gmem), "r"(sz), "l"(pol));
 }
 __device__ __forceinline__ void cp_async16s(uint32_t saddr, const void* gmem, bool pred) {
   const int sz = pred ? 16 : 0;
@@ -168,14 +169,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       for (int g = gbeg; g < gend; ++g) {
         if (!tc::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
         unsigned char* st = smem + stage * kStageBytes;
+        // weights and scales are read once per call: evict them from L2 first (made here, per
+        // stage, so that the policy holds no register across the loop)
+        const uint64_t pol = l2_evict_first_policy();
         if (lane == 0) {
           StageHdr* h = reinterpret_cast<StageHdr*>(st + kHdrOff);
           h->e = e; h->rbase = rbase; h->nvalid = nvalid; h->blk = blk; h->ks = ks; h->cidx = cidx;
           h->g = g; h->gbeg = gbeg; h->gend = gend; h->done = 0;
           tc::mbar_arrive_expect_tx(&full[stage], tx_bytes);
-          tc::tma_load_2d(st, &map0, g * 64, static_cast<int32_t>(wrow0), &full[stage]);
+          tc::tma_load_2d_hint(st, &map0, g * 64, static_cast<int32_t>(wrow0), &full[stage], pol);
           if (kGateUp)
-            tc::tma_load_2d(st + p.RB * 64, &map1, g * 64, static_cast<int32_t>(wrow0), &full[stage]);
+            tc::tma_load_2d_hint(st + p.RB * 64, &map1, g * 64, static_cast<int32_t>(wrow0),
+                                 &full[stage], pol);
         }
         // scales: the 4-byte fp16 pair holding group g, 8 rows per lane
         // 4-byte scale pair holding this block's scale(s): groups 2g, 2g+1 (kG = 64), g (128) or
@@ -194,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             row = wrow0 + r;
           }
           const bool in = kGateUp ? true : (blk * p.RB + r < a.N);
-          cp_async4(tc::smem_u32(st + kScOff + r * 4), sbase + (in ? row : wrow0) * srow + gp, in);
+          cp_async4(tc::smem_u32(st + kScOff + r * 4), sbase + (in ? row : wrow0) * srow + gp, in,
+                    pol);
         }
         if (g == gbeg) {
 #pragma unroll

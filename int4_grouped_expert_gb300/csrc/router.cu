@@ -201,6 +201,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   const float4* wrow = reinterpret_cast<const float4*>(static_cast<const float*>(a.wr) + wro);
   const uint4* wrow16 = reinterpret_cast<const uint4*>(static_cast<const __half*>(a.wr) + wro);
   const uint4* xv = reinterpret_cast<const uint4*>(a.x);
+  const uint64_t pol = l2_evict_first_policy();  // the router rows are read once per call
   constexpr int TB = 8;  // tokens per pass: every load of a pass is in flight together
   for (int t0 = 0; t0 < T; t0 += TB) {
     float acc[TB] = {};
@@ -213,15 +214,19 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
           const int v = v0 + 32 * i;
           if (v < ve) {
             if (kF16) {
-              const uint4 hv = __ldg(wrow16 + v);
+              const uint4 hv = ldg_hint(wrow16 + v, pol);
               const __half2* h2 = reinterpret_cast<const __half2*>(&hv);
               const float2 f0 = __half22float2(h2[0]), f1 = __half22float2(h2[1]);
               const float2 f2 = __half22float2(h2[2]), f3 = __half22float2(h2[3]);
               w[i][0] = make_float4(f0.x, f0.y, f1.x, f1.y);
               w[i][1] = make_float4(f2.x, f2.y, f3.x, f3.y);
             } else {
-              w[i][0] = __ldg(wrow + 2 * v);
-              w[i][1] = __ldg(wrow + 2 * v + 1);
+              const uint4 u0 = ldg_hint(reinterpret_cast<const uint4*>(wrow + 2 * v), pol);
+              const uint4 u1 = ldg_hint(reinterpret_cast<const uint4*>(wrow + 2 * v + 1), pol);
+              w[i][0] = make_float4(__uint_as_float(u0.x), __uint_as_float(u0.y),
+                                    __uint_as_float(u0.z), __uint_as_float(u0.w));
+              w[i][1] = make_float4(__uint_as_float(u1.x), __uint_as_float(u1.y),
+                                    __uint_as_float(u1.z), __uint_as_float(u1.w));
             }
 #pragma unroll
             for (int tt = 0; tt < TB; ++tt)
@@ -266,11 +271,12 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
     if (a.bias) v += a.bias[ee];
     a.logits[static_cast<int64_t>(t) * E + ee] = v;
   }
-  // the decode grouped GEMM reads x with every 8-wide chunk pair-interleaved; the CTAs share the copy
-  // (after the logits: only the GEMMs, which wait for this grid, read it)
-  if (a.x_perm) {
+  // The decode grouped GEMM reads x with every 8-wide chunk pair-interleaved. Only the GEMMs, which
+  // wait for this grid, read the copy, so the CTAs that do not take part in the top-k make it after
+  // signalling their logits (off the top-k's path); with no such CTA every CTA copies first.
+  auto copy_x = [&](int part, int nparts) {
     const int nv = T * (H / 8);
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += gridDim.x * blockDim.x) {
+    for (int i = part * blockDim.x + threadIdx.x; i < nv; i += nparts * blockDim.x) {
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
       uint4 o;
       o.x = prmt(v.x, v.z, 0x5410);
@@ -279,18 +285,21 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
       o.w = prmt(v.y, v.w, 0x7632);
       reinterpret_cast<uint4*>(a.x_perm)[i] = o;
     }
-  }
+  };
 
   // The last G CTAs to finish their logits (G = one warp per token, 8 tokens per CTA) wait for
   // the others, take the top-k of their tokens, and the last of them groups the rows. With one
   // such CTA (T <= 8) the ids stay in its shared memory.
-  __shared__ int role_s;
+  __shared__ int role_s, arrival_s;
   const int G = min(static_cast<int>(gridDim.x), (T + kRsWarps - 1) / kRsWarps);
+  const int ncopy = static_cast<int>(gridDim.x) - G;  // CTAs outside the top-k
+  if (a.x_perm && ncopy == 0) copy_x(blockIdx.x, gridDim.x);
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned prev = atomicAdd(&a.grp.hdr->route_done, 1u);
-    int r = static_cast<int>(prev) - (static_cast<int>(gridDim.x) - G);
+    arrival_s = static_cast<int>(prev);
+    int r = static_cast<int>(prev) - ncopy;
     if (r >= 0 && prev != gridDim.x - 1) {
       // wait (bounded, ~1 s) for the CTAs still writing logits: all of them run already (this
       // grid's dependents launch only once every CTA of it has started)
@@ -308,7 +317,11 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   }
   __syncthreads();
   const int role = role_s;
-  if (role < 0) return;
+  if (role < 0) {
+    // arrivals 0 .. ncopy-1 are exactly the CTAs outside the top-k: each copies its share of x
+    if (a.x_perm && arrival_s < ncopy) copy_x(arrival_s, ncopy);
+    return;
+  }
   __threadfence();
 
   int* s_ids = reinterpret_cast<int*>(rs_smem + route_small_ids_off(a));
