@@ -4,13 +4,19 @@
 // weights are dequantized on chip ("Strata" MoE tuning notes, lpnh.cn/news/2730718, §2.1 format:
 // 128 codes share one fp16 scale).
 //
-// Tile = (segment, 128 weight rows, up to 256 token rows), contraction in 64-wide stages.
+// Tile = (segment, 128 weight rows, up to kN token rows), contraction in 64-wide stages.
 //   warp 0       TMA producer: the stage's token rows (bf16, 128-byte swizzle) -> shared memory
 //   warp 1       MMA issuer: one thread issues tcgen05.mma (M=128, N=rows, K=16) into TMEM
 //   warp 2       owns the TMEM allocation
-//   warps 4..11  dequant producers: int4 codes (global) -> bf16(q*s) written in the same swizzled
-//                K-major layout (the A operand)
+//   warp 3       small tiles only: TMA producer of the int4 code tiles (a deep ring of stages)
+//   warps 4..11  dequant producers: int4 codes -> bf16(q*s) written in the same swizzled K-major
+//                layout (the A operand)
 //   warps 12..15 epilogue: TMEM -> registers -> global
+// Two tile widths: kN = 256 token rows for segments with many rows (the dequant warps load their
+// codes from global memory themselves, four stages ahead in registers), and kN = 64 for batches
+// with few rows per expert. There the shared memory the wide B tiles would take holds a ring of
+// code tiles filled by TMA (slots of four stages: 128-byte rows), so that enough weight bytes are
+// in flight to stream HBM while each dequantized tile serves only a few dozen tokens.
 // D[weight row][token] accumulates in TMEM: gate/up in one 512-column buffer (gate, then up);
 // down in two 256-column buffers, so its MMAs for the next tile run while the epilogue drains
 // this one. While the epilogue runs, the dequant warps already fill the next tile's stages.
@@ -34,28 +40,49 @@ namespace strata {
 
 constexpr int kTcBM = 128;       // weight rows per tile (MMA M)
 constexpr int kTcBK = 64;        // contraction per stage: one 128-byte swizzle row of bf16
-constexpr int kTcNMax = kTcRows;  // token rows per tile (MMA N)
-constexpr int kTcThreads = 512;   // 16 warps
-constexpr int kTcBoxRows = 128;  // TMA box: 128 token rows x 64 columns (16 KB)
-constexpr int kTcBoxBytes = kTcBoxRows * kTcBK * 2;
+constexpr int kTcThreads = 512;  // 16 warps
 
-template <bool kGateUp>
+#ifndef STRATA_TC_SMALL_STAGES_GU
+#define STRATA_TC_SMALL_STAGES_GU 3
+#endif
+#ifndef STRATA_TC_SMALL_RING_GU
+#define STRATA_TC_SMALL_RING_GU 3
+#endif
+#ifndef STRATA_TC_SMALL_STAGES_DN
+#define STRATA_TC_SMALL_STAGES_DN 4
+#endif
+#ifndef STRATA_TC_SMALL_RING_DN
+#define STRATA_TC_SMALL_RING_DN 4
+#endif
+template <bool kGateUp, int kN>
 struct TcCfg {
-  static constexpr int STAGES = kGateUp ? 3 : 4;
+  static constexpr bool RING = kN <= 64;               // code tiles through the TMA ring
+  static constexpr int STAGES = RING ? (kGateUp ? STRATA_TC_SMALL_STAGES_GU : STRATA_TC_SMALL_STAGES_DN)
+                                     : (kGateUp ? 3 : 4);
   static constexpr int A_BYTES = kTcBM * kTcBK * 2;    // 16 KB per weight matrix
-  static constexpr int B_BYTES = kTcNMax * kTcBK * 2;  // 32 KB
+  static constexpr int B_BYTES = kN * kTcBK * 2;       // 32 KB (kN = 256) or 8 KB (64)
+  static constexpr int BOX_ROWS = kN < 128 ? kN : 128;  // TMA box of token rows x 64 columns
+  static constexpr int BOX_BYTES = BOX_ROWS * kTcBK * 2;
   static constexpr int NMAT = kGateUp ? 2 : 1;
   static constexpr int STAGE_BYTES = NMAT * A_BYTES + B_BYTES;
-  static constexpr uint32_t ACC_COLS = NMAT * kTcNMax;  // one accumulator buffer
-  static constexpr int NBUF = kGateUp ? 1 : 2;          // accumulator buffers (512 columns)
+  // ring slot: the codes of SLOT_K consecutive stages (128 bytes of every weight row, one TMA box
+  // of 128 rows per matrix, 128-byte swizzle)
+  static constexpr int SLOT_K = 4;
+  static constexpr int CODE_BYTES = NMAT * kTcBM * 128;
+  static constexpr int RING_STAGES = RING ? (kGateUp ? STRATA_TC_SMALL_RING_GU : STRATA_TC_SMALL_RING_DN) : 0;
+  static constexpr uint32_t ACC_COLS = NMAT * kN;        // one accumulator buffer
+  static constexpr int NBUF = (kGateUp && !RING) ? 1 : 2;  // accumulator buffers (<= 512 columns)
   static constexpr uint32_t TMEM_COLS = NBUF * ACC_COLS;
-  static constexpr size_t SMEM = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + 256;
+  static constexpr size_t SMEM =
+      static_cast<size_t>(STAGES) * STAGE_BYTES + static_cast<size_t>(RING_STAGES) * CODE_BYTES +
+      1024 + 512;
 };
 
 struct TcTile {
   int e, mt, row0, nvalid, nmma;
 };
 
+template <int kN>
 __device__ __forceinline__ bool tc_decode(const TcArgs& a, int item, int nseg, int mtiles,
                                           TcTile& t) {
   int lo = 0, hi = nseg - 1;
@@ -67,8 +94,8 @@ __device__ __forceinline__ bool tc_decode(const TcArgs& a, int item, int nseg, i
   const int chunk = local / mtiles;
   t.mt = local - chunk * mtiles;
   t.e = a.seg_expert[lo];
-  t.row0 = a.seg_row0[lo] + chunk * kTcNMax;
-  t.nvalid = min(kTcNMax, a.seg_rows[lo] - chunk * kTcNMax);
+  t.row0 = a.seg_row0[lo] + chunk * kN;
+  t.nvalid = min(kN, a.seg_rows[lo] - chunk * kN);
   t.nmma = (t.nvalid + 15) & ~15;
   return true;
 }
@@ -100,22 +127,28 @@ __device__ __forceinline__ uint32_t scale_pair(uint32_t q, __nv_bfloat162 hi, __
 // Position of natural index i (0..7) inside a chunk stored in (0,4,1,5,2,6,3,7) order.
 __device__ __forceinline__ int pair_pos(int i) { return i < 4 ? 2 * i : 2 * (i - 4) + 1; }
 
-template <bool kGateUp>
+template <bool kGateUp, int kN>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, TcArgs a) {
-  using C = TcCfg<kGateUp>;
+    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_b,
+                           const __grid_constant__ CUtensorMap tmap_c0,
+                           const __grid_constant__ CUtensorMap tmap_c1, TcArgs a) {
+  using C = TcCfg<kGateUp, kN>;
   constexpr int ST = C::STAGES;
+  constexpr int RS = C::RING_STAGES > 0 ? C::RING_STAGES : 1;  // (1: unused without the ring)
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ST * C::STAGE_BYTES);
+  uint8_t* ring = smem + ST * C::STAGE_BYTES;  // [RS][matrix][128 rows][128 bytes] of codes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + C::RING_STAGES * C::CODE_BYTES);
   uint64_t* full_a = bars;
   uint64_t* full_b = bars + ST;
   uint64_t* empty = bars + 2 * ST;
   uint64_t* acc_full = bars + 3 * ST;       // [2]
   uint64_t* acc_empty = bars + 3 * ST + 2;  // [2]
   uint64_t* drain = bars + 3 * ST + 4;      // abort path: completion of the issued MMAs
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * ST + 5);
+  uint64_t* cfull = bars + 3 * ST + 5;      // [RS] code slot landed
+  uint64_t* cempty = cfull + RS;            // [RS] code slot read by the 8 dequant warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cempty + RS);
   __shared__ int abort_flag_s;
   volatile int* abort_flag = &abort_flag_s;
 
@@ -131,6 +164,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::mbar_init(acc_empty + b, 4);  // the 4 epilogue warps
     }
     tc::mbar_init(drain, 1);
+    for (int s = 0; s < C::RING_STAGES; ++s) {
+      tc::mbar_init(cfull + s, 1);
+      tc::mbar_init(cempty + s, 8);
+    }
     tc::fence_barrier_init();
     abort_flag_s = 0;
   }
@@ -158,16 +195,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         TcTile t;
-        tc_decode(a, item, nseg, mtiles, t);
-        const int nbox = t.nmma > kTcBoxRows ? 2 : 1;  // only the rows the MMA reads
+        tc_decode<kN>(a, item, nseg, mtiles, t);
+        const int nbox = t.nmma > C::BOX_ROWS ? 2 : 1;  // only the rows the MMA reads
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % ST;
           const uint32_t ph = (it / ST) & 1;
           if (!tc::mbar_wait(empty + s, ph ^ 1, abort_flag, a.status)) { ok = false; break; }
-          tc::mbar_arrive_expect_tx(full_b + s, nbox * kTcBoxBytes);
+          tc::mbar_arrive_expect_tx(full_b + s, nbox * C::BOX_BYTES);
           for (int bx = 0; bx < nbox; ++bx)
-            tc::tma_load_2d(B_of(s) + bx * kTcBoxBytes, &tmap_b, kb * kTcBK,
-                            t.row0 + bx * kTcBoxRows, full_b + s);
+            tc::tma_load_2d(B_of(s) + bx * C::BOX_BYTES, &tmap_b, kb * kTcBK,
+                            t.row0 + bx * C::BOX_ROWS, full_b + s);
         }
       }
       if (!ok)  // drain the copies that may still be in flight
@@ -182,7 +219,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++tcount) {
         TcTile t;
-        tc_decode(a, item, nseg, mtiles, t);
+        tc_decode<kN>(a, item, nseg, mtiles, t);
         const uint32_t idesc = tc::idesc_bf16(kTcBM, t.nmma);
         const int buf = tcount % C::NBUF;
         const uint32_t dtm = tmem + buf * C::ACC_COLS;
@@ -210,7 +247,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t acc = (kb | kk) ? 1u : 0u;
             // +32 bytes per 16-wide K step inside the swizzle row (address field is in 16 B)
             tc::mma_bf16_ss(dtm, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-            if (kGateUp) tc::mma_bf16_ss(dtm + kTcNMax, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+            if (kGateUp) tc::mma_bf16_ss(dtm + kN, da1 + 2 * kk, db + 2 * kk, idesc, acc);
           }
           tc::mma_commit(empty + s);
         }
@@ -221,6 +258,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::mma_commit(drain);
         tc::mbar_wait_drain(drain, 0);
       }
+    }
+    __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------------------ code ring producer
+    if (C::RING && lane == 0) {
+      tc::prefetch_tmap(&tmap_c0);
+      if (kGateUp) tc::prefetch_tmap(&tmap_c1);
+      int cit = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        TcTile t;
+        tc_decode<kN>(a, item, nseg, mtiles, t);
+        const int32_t wrow = t.e * a.Nw + t.mt * kTcBM;
+        for (int kb = 0; kb < nk; kb += C::SLOT_K, ++cit) {
+          const int cs = cit % RS;
+          if (!tc::mbar_wait(cempty + cs, ((cit / RS) & 1) ^ 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          // a slot past the end of the row (nk not a multiple of SLOT_K) reads zero fill
+          uint8_t* dst = ring + cs * C::CODE_BYTES;
+          tc::mbar_arrive_expect_tx(cfull + cs, C::CODE_BYTES);
+          tc::tma_load_2d(dst, &tmap_c0, kb * (kTcBK / 2), wrow, cfull + cs);
+          if (kGateUp)
+            tc::tma_load_2d(dst + C::CODE_BYTES / 2, &tmap_c1, kb * (kTcBK / 2), wrow, cfull + cs);
+        }
+      }
+      if (!ok)  // drain the copies that may still be in flight
+        for (int j = (cit > RS ? cit - RS : 0); j < cit; ++j)
+          tc::mbar_wait_drain(cfull + (j % RS), (j / RS) & 1);
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 12) {
@@ -235,11 +302,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int64_t srow = a.K / a.group;
     // scale of stage kb (64 codes): group (64 kb) / G
     const int gs = a.group == 64 ? 0 : a.group == 128 ? 1 : 2;
-    int it = 0;
+    // ring: this thread's weight row inside a slot; a stage is 32 bytes (two 16-byte chunks) of
+    // it, chunk c stored at c ^ (r % 8) (128-byte swizzle)
+    const int roff = (kGateUp ? mat * (C::CODE_BYTES / 2) : 0) + r * 128;
+    int it = 0, cit = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       TcTile t;
-      tc_decode(a, item, nseg, mtiles, t);
+      tc_decode<kN>(a, item, nseg, mtiles, t);
       const int64_t wrow = static_cast<int64_t>(t.e) * a.Nw + t.mt * kTcBM + r;
       const uint8_t* cp = codes + wrow * row_bytes + half * 16;
       const __half* sp = scales + wrow * srow;
@@ -252,7 +322,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // complete right away
       unsigned short sc[PD];
       auto ld = [&](int kb, uint4& x0, uint4& x1) {
-        if (kb < nk) {
+        if (!C::RING && kb < nk) {
           x0 = __ldg(reinterpret_cast<const uint4*>(cp + static_cast<int64_t>(kb) * 32));
           if (kGateUp) x1 = __ldg(reinterpret_cast<const uint4*>(cp + static_cast<int64_t>(kb) * 32 + 16));
         }
@@ -275,8 +345,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const __nv_bfloat16 lb = __float2bfloat16_rn(sf - __bfloat162float(hb));
           const __nv_bfloat162 s_hi = __halves2bfloat162(hb, hb);
           const __nv_bfloat162 s_lo = __halves2bfloat162(lb, lb);
-          const uint4 x0 = cA[u], x1 = cB[u];
-          ld(kb + PD, cA[u], cB[u]);
+          uint4 x0 = cA[u], x1 = cB[u];
+          if (C::RING) {
+            const int cs = cit % RS;
+            const int ks = kb % C::SLOT_K;
+            if (ks == 0 && !tc::mbar_wait(cfull + cs, (cit / RS) & 1, abort_flag, a.status)) {
+              ok = false;
+              break;
+            }
+            const uint8_t* src = ring + cs * C::CODE_BYTES + roff;
+            const int c0 = 2 * ks + (kGateUp ? 0 : half);
+            x0 = *reinterpret_cast<const uint4*>(src + ((c0 ^ (r & 7)) << 4));
+            if (kGateUp) x1 = *reinterpret_cast<const uint4*>(src + (((c0 + 1) ^ (r & 7)) << 4));
+            if (ks == C::SLOT_K - 1 || kb == nk - 1) {
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(cempty + cs);  // the slot's codes are all read
+              ++cit;
+            }
+          } else {
+            ld(kb + PD, cA[u], cB[u]);
+          }
           if (kb + PD < nk)
             sc[u] = __ldg(reinterpret_cast<const unsigned short*>(sp) + ((kb + PD) >> gs));
           if (!tc::mbar_wait(empty + s, ph ^ 1, abort_flag, a.status)) { ok = false; break; }
@@ -309,7 +397,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool ok = true;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++tcount) {
       TcTile t;
-      tc_decode(a, item, nseg, mtiles, t);
+      tc_decode<kN>(a, item, nseg, mtiles, t);
       const int buf = tcount % C::NBUF;
       if (!tc::mbar_wait(acc_full + buf, (tcount / C::NBUF) & 1, abort_flag, a.status)) {
         ok = false;
@@ -323,7 +411,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::tmem_ld32(lane_addr + c, g);
         if (kGateUp) {
           uint32_t u[32];
-          tc::tmem_ld32(lane_addr + kTcNMax + c, u);
+          tc::tmem_ld32(lane_addr + kN + c, u);
           tc::tmem_ld_wait();
           __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.out);
           const int col = (irow & ~7) | pair_pos(irow & 7);
@@ -404,37 +492,62 @@ static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
-// Row-major bf16 [rows, cols]: boxes of 128 rows x 64 columns, 128-byte swizzle, zero fill.
-static bool make_row_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+// Row-major bf16 [rows, cols]: boxes of box_rows rows x 64 columns, 128-byte swizzle, zero fill.
+static bool make_row_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
+                          int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {kTcBK, kTcBoxRows};
+  cuuint32_t box[2] = {kTcBK, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kGateUp>
-cudaError_t launch_gemm_tc_t(const TcArgs& a, const void* b_rows, int64_t rows, int num_sms,
-                             cudaStream_t stream) {
-  using C = TcCfg<kGateUp>;
-  CUtensorMap map;
-  if (!make_row_tmap(&map, b_rows, rows, a.K)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<kGateUp>,
+// Codes [rows, K/2] bytes: boxes of 128 bytes (four 64-wide stages) x 128 weight rows, 128-byte
+// swizzle, zero fill past the row end.
+static bool make_code_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t K) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+  cuuint32_t box[2] = {128, kTcBM};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kGateUp, int kN>
+cudaError_t launch_gemm_tc_t(const TcArgs& a, const void* b_rows, int64_t rows, int64_t experts,
+                             int num_sms, cudaStream_t stream) {
+  using C = TcCfg<kGateUp, kN>;
+  CUtensorMap map, c0, c1;
+  if (!make_row_tmap(&map, b_rows, rows, a.K, C::BOX_ROWS)) return cudaErrorInvalidValue;
+  c0 = map;
+  c1 = map;
+  if (C::RING) {
+    if (!make_code_tmap(&c0, a.codes0, experts * a.Nw, a.K)) return cudaErrorInvalidValue;
+    if (kGateUp && !make_code_tmap(&c1, a.codes1, experts * a.Nw, a.K)) return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<kGateUp, kN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
-  grouped_gemm_tc_kernel<kGateUp><<<num_sms, kTcThreads, C::SMEM, stream>>>(map, a);
+  grouped_gemm_tc_kernel<kGateUp, kN><<<num_sms, kTcThreads, C::SMEM, stream>>>(map, c0, c1, a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_tc(const TcArgs& a, bool gate_up, const void* b_rows, int64_t rows,
-                           int num_sms, cudaStream_t stream) {
-  return gate_up ? launch_gemm_tc_t<true>(a, b_rows, rows, num_sms, stream)
-                 : launch_gemm_tc_t<false>(a, b_rows, rows, num_sms, stream);
+                           int64_t experts, int tile_rows, int num_sms, cudaStream_t stream) {
+  if (tile_rows == kTcRowsSmall)
+    return gate_up ? launch_gemm_tc_t<true, kTcRowsSmall>(a, b_rows, rows, experts, num_sms, stream)
+                   : launch_gemm_tc_t<false, kTcRowsSmall>(a, b_rows, rows, experts, num_sms, stream);
+  if (tile_rows != kTcRows) return cudaErrorInvalidValue;
+  return gate_up ? launch_gemm_tc_t<true, kTcRows>(a, b_rows, rows, experts, num_sms, stream)
+                 : launch_gemm_tc_t<false, kTcRows>(a, b_rows, rows, experts, num_sms, stream);
 }
 
 }  // namespace strata

@@ -106,9 +106,12 @@ int cta_gemm_ksplit(int64_t items, int64_t K, int num_sms);
 cudaError_t launch_gemm_cta(const GemmArgs& a, bool gate_up, int64_t experts, int num_sms,
                             cudaStream_t stream);
 int warp_ksplit(int64_t T, int E, int k, int shared, int64_t I, int64_t H);
-constexpr int kTcRows = 256;  // token rows per tensor-core tile
+constexpr int kTcRows = 256;      // token rows per tensor-core tile
+constexpr int kTcRowsSmall = 64;  // the same for batches with few rows per expert
+// b_rows: the B operand rows [rows, K] bf16; experts: weight matrices per code tensor
+// (routed + shared); tile_rows: kTcRows or kTcRowsSmall (the grouping's chunk size)
 cudaError_t launch_gemm_tc(const TcArgs& a, bool gate_up, const void* b_rows, int64_t rows,
-                           int num_sms, cudaStream_t stream);
+                           int64_t experts, int tile_rows, int num_sms, cudaStream_t stream);
 cudaError_t launch_gather_rows(const void* x, const int* perm, int64_t rows, int64_t H, void* xp,
                                cudaStream_t stream);
 cudaError_t launch_combine(const float* y, const float* gates, const int* inv, const void* x,

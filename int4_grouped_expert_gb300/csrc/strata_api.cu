@@ -63,6 +63,11 @@ static bool use_tc_path(const strata_moe_layer* L, int64_t T) {
   if (L->flags & STRATA_FORCE_TC_PATH) return true;
   return T >= 128;
 }
+// Token rows per tensor-core tile: 64 when the routed experts average at most 48 rows (the
+// small-tile kernel streams its code tiles through a deep TMA ring), else 256.
+static int tc_tile_rows(const strata_moe_layer* L, int64_t T) {
+  return T * L->k <= 48 * static_cast<int64_t>(L->E) ? kTcRowsSmall : kTcRows;
+}
 static int layer_group(const strata_moe_layer* L) {
   return L->group_size == 0 ? STRATA_GROUP : L->group_size;
 }
@@ -220,7 +225,7 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
   pa.ksplit_dn = 1;
   pa.cnt_per_chunk = 0;
   if (F.tc) {
-    pa.tokc = kTcRows;
+    pa.tokc = tc_tile_rows(L, T);
     pa.mtiles_gu = static_cast<int>(L->I / 128);
     pa.mtiles_dn = static_cast<int>(L->H / 128);
     pa.ksplit_gu = 1;
@@ -296,7 +301,8 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     g.seg_rows = pa.seg_rows;
     g.seg_item = pa.seg_item_gu;
     g.status = &hdr->status;
-    e = launch_gemm_tc(g, true, base + F.xp, rows, sms, st);
+    const int64_t nexp = E + (S ? 1 : 0);
+    e = launch_gemm_tc(g, true, base + F.xp, rows, nexp, pa.tokc, sms, st);
     if (e != cudaSuccess || !mark(3)) return STRATA_ERR_CUDA;
     TcArgs d = g;
     d.codes0 = L->down_codes;
@@ -307,7 +313,7 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     d.K = static_cast<int>(L->I);
     d.Nw = static_cast<int>(L->H);
     d.seg_item = pa.seg_item_dn;
-    e = launch_gemm_tc(d, false, base + F.h, rows, sms, st);
+    e = launch_gemm_tc(d, false, base + F.h, rows, nexp, pa.tokc, sms, st);
     if (e != cudaSuccess || !mark(4)) return STRATA_ERR_CUDA;
   } else {
     GemmArgs g{};
