@@ -13,7 +13,8 @@ invariants, special cases and brute force (tests/test_oracle_*.py).
 
 Functions and their pins:
   quantize_groups   pinned: exact-rational brute force, |w - q s| <= s/2,
-                    absmax -> +-7, idempotence, hand-built .5 ties (golden).
+                    absmax -> +-7 (+-127 for 8 bits), idempotence, hand-built
+                    .5 ties (golden), for 4- and 8-bit codes.
   dequantize        pinned: hand-packed bytes (golden) and round trip.
   route_topk        pinned: pure-Python brute force, full sort, sum p = 1,
                     k = E, zero router -> uniform.

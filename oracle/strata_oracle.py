@@ -33,8 +33,20 @@ import numpy as np
 GROUP = 128          # [tuning-moe] §2.1: 128 weights per group (the pages' choice)
 GROUPS = (64, 128, 256)  # the sketch takes group_size as a parameter; 64 and 256 are the sizes
                          # the pages weighed against 128, kept as variants
-QMIN, QMAX = -8, 7   # [tuning-moe] §2.1: clamp(-8, 7) for bits = 4
-QDIV = 7.0           # [tuning-moe] §2.1: scale = absmax / (2**(bits-1) - 1)
+BITS = (4, 8)        # [tuning-moe] §2.1: the sketch takes bits as a parameter (4 for experts;
+                     # the pages keep attention projections at 8 bits)
+
+
+def code_range(bits: int):
+    """(qmin, qmax, divisor) of a bit width, [tuning-moe] §2.1.
+
+    scale = absmax / (2**(bits-1) - 1); the sketch's clamp(-8, 7) is the bits = 4 instance of
+    the two's-complement range [-2**(bits-1), 2**(bits-1) - 1], which is the range taken for 8.
+    """
+    if bits not in BITS:
+        raise ValueError("bits must be 4 or 8")
+    qmax = 2 ** (bits - 1) - 1
+    return -(qmax + 1), qmax, float(qmax)
 
 
 # ----------------------------------------------------------------------------- storage
@@ -80,49 +92,58 @@ def _check_weight(w16, group):
     return w
 
 
-def quantize_groups(w16: np.ndarray, group: int = GROUP):
-    """Symmetric int4 group quantization, [tuning-moe] §2.1 (group_quantize sketch).
+def quantize_groups(w16: np.ndarray, group: int = GROUP, bits: int = 4):
+    """Symmetric group quantization, [tuning-moe] §2.1 (group_quantize sketch).
 
     weight [out, in] is viewed as [out, in/G, G] (G = group, 128 unless given); per group
-      scale = absmax / 7, stored as fp16 (nearest-even),
-      q     = clamp(round_half_even(w / scale), -8, 7)  with the exact quotient.
-    Returns (codes uint8 [out, in/2], scales float16 [out, in/G]).
+      scale = absmax / (2**(bits-1) - 1)  (7 for 4 bits, 127 for 8), stored as fp16
+              (nearest-even),
+      q     = clamp(round_half_even(w / scale), qmin, qmax)  with the exact quotient.
+    Returns (codes, scales float16 [out, in/G]); codes are uint8 [out, in/2] (two 4-bit codes
+    per byte) for bits = 4 and int8 [out, in] (one code per byte) for bits = 8.
     """
+    qmin, qmax, qdiv = code_range(bits)
     w = _check_weight(w16, group)
     n, kdim = w.shape
     wg = w.astype(np.float64).reshape(n, kdim // group, group)
     absmax = np.abs(wg).max(axis=-1)                      # exact
-    # One rounding: the fp64 quotient absmax/7 never sits on an fp16 midpoint
-    # unless the exact one does (a/7 has a period-3 binary expansion).
-    scale16 = (absmax / QDIV).astype(np.float16)
+    # One rounding: the fp64 quotient absmax/7 (or /127) never sits on an fp16 midpoint unless
+    # the exact one does (the exact quotient of an 11-bit significand by 7 or 127 is either
+    # exact in fp16 or at least 2^-18 relative away from every midpoint).
+    scale16 = (absmax / qdiv).astype(np.float16)
     s = scale16.astype(np.float64)[..., None]
     with np.errstate(divide="ignore", invalid="ignore"):
         # fp64 quotient of two fp16 values decides every .5 tie exactly.
         r = np.where(s > 0, np.rint(wg / s), 0.0)
-    q = np.clip(r, QMIN, QMAX).astype(np.int8).reshape(n, kdim)
-    return pack_codes(q), scale16
+    q = np.clip(r, qmin, qmax).astype(np.int8).reshape(n, kdim)
+    return (pack_codes(q) if bits == 4 else q), scale16
 
 
-def quantize_groups_f16_quotient(w16: np.ndarray, group: int = GROUP):
+def quantize_groups_f16_quotient(w16: np.ndarray, group: int = GROUP, bits: int = 4):
     """The literal fp16 reading of the sketch: w / scale rounded to fp16 before round().
 
     Not the chosen reading; kept so the tests can count where the two differ.
     """
+    qmin, qmax, qdiv = code_range(bits)
     w = _check_weight(w16, group)
     n, kdim = w.shape
     wg = w.reshape(n, kdim // group, group)
     absmax = np.abs(wg.astype(np.float64)).max(axis=-1)
-    scale16 = (absmax / QDIV).astype(np.float16)
+    scale16 = (absmax / qdiv).astype(np.float16)
     with np.errstate(divide="ignore", invalid="ignore"):
         quot = (wg.astype(np.float64) / scale16.astype(np.float64)[..., None]).astype(np.float16)
         r = np.where(scale16[..., None] > 0, np.rint(quot.astype(np.float64)), 0.0)
-    q = np.clip(r, QMIN, QMAX).astype(np.int8).reshape(n, kdim)
-    return pack_codes(q), scale16
+    q = np.clip(r, qmin, qmax).astype(np.int8).reshape(n, kdim)
+    return (pack_codes(q) if bits == 4 else q), scale16
 
 
 def dequantize(codes: np.ndarray, scales: np.ndarray, group: int = None) -> np.ndarray:
-    """q * scale in fp64, [out, in]; the group size follows from the shapes unless given."""
-    q = unpack_codes(codes).astype(np.float64)
+    """q * scale in fp64, [out, in]; the group size follows from the shapes unless given.
+
+    codes: packed 4-bit (uint8 [out, in/2]) or 8-bit (int8 [out, in]), told apart by dtype.
+    """
+    c = np.asarray(codes)
+    q = (c if c.dtype == np.int8 else unpack_codes(c)).astype(np.float64)
     n, kdim = q.shape
     if group is None:
         group = kdim // np.asarray(scales).shape[1]

@@ -18,13 +18,13 @@ from oracle import strata_oracle as so
 from workloads import gen
 
 
-def make_layer(rng, E, H, I, shared, std=0.05):
+def make_layer(rng, E, H, I, shared, std=0.05, bits=4):
     ws = []
     for _ in range(E + shared):
         g = (rng.standard_normal((I, H)) * std).astype(np.float16)
         u = (rng.standard_normal((I, H)) * std).astype(np.float16)
         d = (rng.standard_normal((H, I)) * std).astype(np.float16)
-        ws.append(tuple(oracle.quantize_groups(m) for m in (g, u, d)))
+        ws.append(tuple(oracle.quantize_groups(m, bits=bits) for m in (g, u, d)))
     return ws
 
 
@@ -90,6 +90,21 @@ def test_single_expert_is_one_ffn():
     wr = (rng.standard_normal((1, H)) * 0.02).astype(np.float32)
     res = oracle.moe_forward(x, wr, None, 1, lambda e: ws[e], 1, 0)
     np.testing.assert_array_equal(res["route"]["gates"], 1.0)
+    xf = gen.bf16_bits_to_f32(x).astype(np.float64)
+    ref = torch_swiglu(xf, *[oracle.dequantize(c, s) for (c, s) in ws[0]])
+    np.testing.assert_allclose(res["out"], ref, rtol=1e-10, atol=1e-12)
+
+
+def test_single_expert_is_one_ffn_8bit():
+    """8-bit experts: E = k = 1 is one SwiGLU FFN of the dequantized weights, and those weights are
+    within half a (127x finer) step of the fp16 ones."""
+    H, I, T = 256, 128, 4
+    rng = np.random.default_rng(19)
+    ws = make_layer(rng, 1, H, I, 0, bits=8)
+    assert all(c.dtype == np.int8 and c.shape[1] == s.shape[1] * 128 for (c, s) in ws[0])
+    x = gen.activations(T, H, 6)
+    wr = (rng.standard_normal((1, H)) * 0.02).astype(np.float32)
+    res = oracle.moe_forward(x, wr, None, 1, lambda e: ws[e], 1, 0)
     xf = gen.bf16_bits_to_f32(x).astype(np.float64)
     ref = torch_swiglu(xf, *[oracle.dequantize(c, s) for (c, s) in ws[0]])
     np.testing.assert_allclose(res["out"], ref, rtol=1e-10, atol=1e-12)

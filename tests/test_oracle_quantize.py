@@ -54,18 +54,20 @@ def nearest_fp16_exact(x: Fraction) -> Fraction:
     return best[1]
 
 
-def brute_quantize_group(ws):
-    """Exact: scale = fp16-nearest(absmax/7); q = argmin |w - q s| over [-8,7], ties even."""
+def brute_quantize_group(ws, bits=4):
+    """Exact: scale = fp16-nearest(absmax/qmax); q = argmin |w - q s| over the code range,
+    ties even (qmax = 7, range [-8, 7] for 4 bits; 127 and [-128, 127] for 8)."""
+    qmax = 2 ** (bits - 1) - 1
     fr = [Fraction(float(w)) for w in ws]
     a = max(abs(v) for v in fr)
-    s = nearest_fp16_exact(a / 7)
+    s = nearest_fp16_exact(a / qmax)
     qs = []
     for v in fr:
         if s == 0:
             qs.append(0)
             continue
         best = None
-        for q in range(-8, 8):
+        for q in range(-qmax - 1, qmax + 1):
             key = (abs(v - q * s), q % 2)                    # prefer the even code on a tie
             if best is None or key < best[0]:
                 best = (key, q)
@@ -244,3 +246,99 @@ def test_planted_rounding_mistake_is_caught(monkeypatch):
     for i, c in g["codes_nonzero"]:
         expect[i] = c
     assert not np.array_equal(q, expect)
+
+
+# ---------------------------------------------------------------- 8-bit codes
+
+def test_golden_hand_built_groups_8bit():
+    cases = json.load(open(GOLDEN))
+    for g in cases["groups_8bit"]:
+        w = np.zeros((1, 128), dtype=np.float16)
+        for i, v in g["nonzero"]:
+            w[0, i] = v
+        codes, scales = oracle.quantize_groups(w, bits=8)
+        assert codes.dtype == np.int8 and codes.shape == (1, 128)
+        assert float(scales[0, 0]) == g["scale"], g["why"]
+        expect = np.zeros(128, dtype=np.int8)
+        for i, c in g["codes_nonzero"]:
+            expect[i] = c
+        np.testing.assert_array_equal(codes[0], expect, err_msg=g["why"])
+
+
+@pytest.mark.parametrize("scale_exp,group", [(0, 128), (-14, 128), (0, 64), (-6, 256)])
+def test_exact_brute_force_random_groups_8bit(scale_exp, group):
+    """8-bit codes: every sampled group equals the exact-rational search over [-128, 127]."""
+    rng = np.random.default_rng(300 + scale_exp + group)
+    w = gen.expert_weight(0, 0, 4, "up", 8, 1024)
+    w = (w.astype(np.float32) * np.float32(2.0 ** scale_exp)).astype(np.float16)
+    codes, scales = oracle.quantize_groups(w, group=group, bits=8)
+    for r, g in _groups_from(w, 6, rng, group):
+        s, qs = brute_quantize_group(w[r, g * group:(g + 1) * group], bits=8)
+        assert Fraction(float(scales[r, g])) == s
+        np.testing.assert_array_equal(codes[r, g * group:(g + 1) * group], qs)
+
+
+def test_round_trip_bound_and_absmax_8bit():
+    w = gen.expert_weight(0, 0, 5, "down", 32, 2048)
+    codes, scales = oracle.quantize_groups(w, bits=8)
+    q = codes.astype(np.int64).reshape(32, 16, 128)
+    s = scales.astype(np.float64)
+    wg = w.astype(np.float64).reshape(32, 16, 128)
+    assert np.all(np.abs(wg - q * s[..., None]) <= s[..., None] / 2)
+    am = np.abs(wg).argmax(axis=-1)
+    top = np.take_along_axis(q, am[..., None], axis=-1)[..., 0]
+    topw = np.take_along_axis(wg, am[..., None], axis=-1)[..., 0]
+    np.testing.assert_array_equal(np.abs(top), 127)
+    np.testing.assert_array_equal(np.sign(top), np.sign(topw))
+    assert q.min() >= -127                  # -128 never occurs
+    # 8-bit codes resolve the same weights ~18x finer than 4-bit ones (scale ratio 127 / 7)
+    _, s4 = oracle.quantize_groups(w)
+    ratio = s4.astype(np.float64) / s
+    assert np.all(np.abs(ratio - 127 / 7) < 127 / 7 * 2e-3)
+
+
+def test_idempotent_8bit():
+    """Quantizing w = q0*s0 (exact in fp16, one +-127 per group) returns (q0, s0)."""
+    rng = np.random.default_rng(12)
+    n, kdim = 16, 512
+    q0 = rng.integers(-127, 128, (n, kdim)).astype(np.int8)
+    q0[:, ::128] = rng.choice([-127, 127], (n, kdim // 128))
+    # scales with <= 4 significant bits: q*s (7 + 4 bits) is exact in fp16
+    mant = rng.integers(8, 16, (n, kdim // 128))
+    s0 = (mant * 2.0 ** rng.integers(-18, -10, (n, kdim // 128))).astype(np.float16)
+    w64 = q0.reshape(n, -1, 128) * s0.astype(np.float64)[..., None]
+    w = w64.reshape(n, kdim).astype(np.float16)
+    assert np.array_equal(w.astype(np.float64), w64.reshape(n, kdim))
+    codes, scales = oracle.quantize_groups(w, bits=8)
+    np.testing.assert_array_equal(scales, s0)
+    np.testing.assert_array_equal(codes, q0)
+
+
+def test_dequantize_layout_by_hand_8bit():
+    # int8 codes are one per byte, told apart from packed 4-bit codes by their dtype
+    q = np.zeros((1, 256), dtype=np.int8)
+    q[0, 0], q[0, 127], q[0, 128], q[0, 255] = -127, 3, 100, -1
+    sc = np.array([[0.5, 0.25]], dtype=np.float16)
+    d = oracle.dequantize(q, sc)
+    assert d[0, 0] == -63.5 and d[0, 127] == 1.5 and d[0, 128] == 25.0 and d[0, 255] == -0.25
+    assert d[0, 1] == 0.0
+
+
+def test_bits_argument_errors():
+    with pytest.raises(ValueError):
+        oracle.quantize_groups(np.zeros((1, 128), dtype=np.float16), bits=2)
+    with pytest.raises(ValueError):
+        oracle.quantize_groups(np.zeros((1, 128), dtype=np.float16), bits=16)
+
+
+def test_planted_divisor_mistake_is_caught_8bit(monkeypatch):
+    """Dividing the absmax by 128 instead of 127 (a plausible slip) must fail the golden groups."""
+    real = so.code_range
+    monkeypatch.setattr(so, "code_range", lambda bits: (real(bits)[0], real(bits)[1], 128.0)
+                        if bits == 8 else real(bits))
+    g = json.load(open(GOLDEN))["groups_8bit"][0]
+    w = np.zeros((1, 128), dtype=np.float16)
+    for i, v in g["nonzero"]:
+        w[0, i] = v
+    codes, scales = so.quantize_groups(w, bits=8)
+    assert float(scales[0, 0]) != g["scale"]
