@@ -108,6 +108,22 @@ strata_status strata_quantize_groups(const void* w_fp16, int64_t n, int64_t k, i
                                      strata_stream stream);
 
 /*
+ * strata_quantize_groups_bits — the same with the sketch's bit width as a parameter
+ * ([tuning-moe] §2.1: scale = absmax / (2^(bits-1) - 1); the pages keep experts at 4 bits and
+ * attention projections at 8).
+ * bits  4: exactly strata_quantize_groups.
+ *       8: scale[i,g] = fp16_round_nearest_even(absmax / 127),
+ *          q[i,c] = clamp(round_half_even(w[i,c] / scale[i,g]), -128, 127) (exact quotient);
+ *          codes [n, k] int8 (two's complement), one per byte, row-major.
+ *       anything else -> STRATA_ERR_UNSUPPORTED.
+ * Other arguments, errors and alignment as strata_quantize_groups.
+ */
+strata_status strata_quantize_groups_bits(const void* w_fp16, int64_t n, int64_t k,
+                                          int32_t group_size, int32_t bits, uint8_t* codes,
+                                          void* scales_fp16, uint32_t* dev_status,
+                                          strata_stream stream);
+
+/*
  * strata_route_topk — router GEMV + softmax + top-k + token grouping,
  * [tuning-moe] §2.3 point 1 and [tok-102] §3.2; grouping per [tuning-3090] §3.2.
  *
@@ -182,6 +198,11 @@ typedef struct {
   int32_t group_size;    /* scale group of all three projections: 128 (0 means 128), 64 or 256;
                             the scales above are then [.., K/group_size]. 256 on the decode path
                             needs H % 512 == 0 and I % 512 == 0 */
+  int32_t bits;          /* code width of all three projections: 4 (0 means 4) or 8. With 8 the
+                            codes are int8, one per byte (strata_quantize_groups_bits): gate/up
+                            [E+S, I, H], down [E+S, H, I]; such layers run on the tensor-core
+                            grouped GEMM at every batch size (STRATA_FORCE_WARP_PATH ->
+                            STRATA_ERR_UNSUPPORTED) */
 } strata_moe_layer;
 
 /* Workspace bytes strata_moe_forward needs for up to T_max tokens (0 if the layer is invalid). */

@@ -45,7 +45,7 @@ class strata_moe_layer(ctypes.Structure):
         ("gate_codes", ctypes.c_void_p), ("gate_scales", ctypes.c_void_p),
         ("up_codes", ctypes.c_void_p), ("up_scales", ctypes.c_void_p),
         ("down_codes", ctypes.c_void_p), ("down_scales", ctypes.c_void_p),
-        ("group_size", ctypes.c_int32),
+        ("group_size", ctypes.c_int32), ("bits", ctypes.c_int32),
     ]
 
 
@@ -60,6 +60,7 @@ _SIGNATURES = {
     "strata_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "strata_version": (ctypes.c_int, []),
     "strata_quantize_groups": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, _P, _P, _P]),
+    "strata_quantize_groups_bits": (ctypes.c_int, [_P, _I64, _I64, _I32, _I32, _P, _P, _P, _P]),
     "strata_route_workspace_size": (_SZ, [_I64, _I32, _I32]),
     "strata_route_topk": (ctypes.c_int, [_P, _P, _P, _I64, _I64, _I32, _I32, _U32,
                                          _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -141,6 +142,12 @@ def strata_version() -> int:
 def strata_quantize_groups(w, n, k, codes, scales, dev_status=None, group_size=GROUP, stream=None):
     return lib().strata_quantize_groups(ptr(w), n, k, group_size, ptr(codes), ptr(scales),
                                         ptr(dev_status), stream_handle(stream))
+
+
+def strata_quantize_groups_bits(w, n, k, codes, scales, dev_status=None, group_size=GROUP, bits=4,
+                                stream=None):
+    return lib().strata_quantize_groups_bits(ptr(w), n, k, group_size, bits, ptr(codes),
+                                             ptr(scales), ptr(dev_status), stream_handle(stream))
 
 
 def strata_route_workspace_size(T, E, k) -> int:

@@ -54,7 +54,7 @@ constexpr int kTcThreads = 512;  // 16 warps
 #ifndef STRATA_TC_SMALL_RING_DN
 #define STRATA_TC_SMALL_RING_DN 4
 #endif
-template <bool kGateUp, int kN>
+template <bool kGateUp, int kN, int kBits = 4>
 struct TcCfg {
   static constexpr bool RING = kN <= 64;               // code tiles through the TMA ring
   static constexpr int STAGES = RING ? (kGateUp ? STRATA_TC_SMALL_STAGES_GU : STRATA_TC_SMALL_STAGES_DN)
@@ -66,8 +66,9 @@ struct TcCfg {
   static constexpr int NMAT = kGateUp ? 2 : 1;
   static constexpr int STAGE_BYTES = NMAT * A_BYTES + B_BYTES;
   // ring slot: the codes of SLOT_K consecutive stages (128 bytes of every weight row, one TMA box
-  // of 128 rows per matrix, 128-byte swizzle)
-  static constexpr int SLOT_K = 4;
+  // of 128 rows per matrix, 128-byte swizzle): four stages of 4-bit codes or two of 8-bit ones
+  static constexpr int STAGE_CODE_BYTES = kTcBK * kBits / 8;  // bytes of one row per stage
+  static constexpr int SLOT_K = 128 / STAGE_CODE_BYTES;
   static constexpr int CODE_BYTES = NMAT * kTcBM * 128;
   static constexpr int RING_STAGES = RING ? (kGateUp ? STRATA_TC_SMALL_RING_GU : STRATA_TC_SMALL_RING_DN) : 0;
   static constexpr uint32_t ACC_COLS = NMAT * kN;        // one accumulator buffer
@@ -124,15 +125,32 @@ __device__ __forceinline__ uint32_t scale_pair(uint32_t q, __nv_bfloat162 hi, __
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+// Four int8 codes (bytes of w) times the scale, exactly, in fp32: the byte with its sign bit
+// flipped (q + 128) becomes the low mantissa bits of 2^23 (fp32 2^23 + q + 128), the offset is
+// subtracted exactly, and q * s has at most 8 + 11 significant bits.
+__device__ __forceinline__ void codes8_scaled(uint32_t w, float s, float* v) {
+  const uint32_t u = w ^ 0x80808080u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float f = __uint_as_float(prmt(u, 0x4B000000u, 0x7540u + i)) - 8388736.0f;
+    v[i] = f * s;
+  }
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 // Position of natural index i (0..7) inside a chunk stored in (0,4,1,5,2,6,3,7) order.
 __device__ __forceinline__ int pair_pos(int i) { return i < 4 ? 2 * i : 2 * (i - 4) + 1; }
 
-template <bool kGateUp, int kN>
+template <bool kGateUp, int kN, int kBits>
 __global__ void __launch_bounds__(kTcThreads, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_b,
                            const __grid_constant__ CUtensorMap tmap_c0,
                            const __grid_constant__ CUtensorMap tmap_c1, TcArgs a) {
-  using C = TcCfg<kGateUp, kN>;
+  using C = TcCfg<kGateUp, kN, kBits>;
+  static_assert(kBits == 4 || C::RING, "8-bit codes come through the code ring");
   constexpr int ST = C::STAGES;
   constexpr int RS = C::RING_STAGES > 0 ? C::RING_STAGES : 1;  // (1: unused without the ring)
   extern __shared__ uint8_t tc_smem_raw[];
@@ -280,9 +298,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // a slot past the end of the row (nk not a multiple of SLOT_K) reads zero fill
           uint8_t* dst = ring + cs * C::CODE_BYTES;
           tc::mbar_arrive_expect_tx(cfull + cs, C::CODE_BYTES);
-          tc::tma_load_2d(dst, &tmap_c0, kb * (kTcBK / 2), wrow, cfull + cs);
+          tc::tma_load_2d(dst, &tmap_c0, kb * C::STAGE_CODE_BYTES, wrow, cfull + cs);
           if (kGateUp)
-            tc::tma_load_2d(dst + C::CODE_BYTES / 2, &tmap_c1, kb * (kTcBK / 2), wrow, cfull + cs);
+            tc::tma_load_2d(dst + C::CODE_BYTES / 2, &tmap_c1, kb * C::STAGE_CODE_BYTES, wrow,
+                            cfull + cs);
         }
       }
       if (!ok)  // drain the copies that may still be in flight
@@ -346,6 +365,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const __nv_bfloat162 s_hi = __halves2bfloat162(hb, hb);
           const __nv_bfloat162 s_lo = __halves2bfloat162(lb, lb);
           uint4 x0 = cA[u], x1 = cB[u];
+          uint4 x8[4];  // 8-bit codes of the stage: gate/up 64 bytes of the row, down 32 of its half
           if (C::RING) {
             const int cs = cit % RS;
             const int ks = kb % C::SLOT_K;
@@ -354,9 +374,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               break;
             }
             const uint8_t* src = ring + cs * C::CODE_BYTES + roff;
-            const int c0 = 2 * ks + (kGateUp ? 0 : half);
-            x0 = *reinterpret_cast<const uint4*>(src + ((c0 ^ (r & 7)) << 4));
-            if (kGateUp) x1 = *reinterpret_cast<const uint4*>(src + (((c0 + 1) ^ (r & 7)) << 4));
+            if (kBits == 8) {
+#pragma unroll
+              for (int c = 0; c < (kGateUp ? 4 : 2); ++c) {
+                const int lc = 4 * ks + (kGateUp ? c : 2 * half + c);
+                x8[c] = *reinterpret_cast<const uint4*>(src + ((lc ^ (r & 7)) << 4));
+              }
+            } else {
+              const int c0 = 2 * ks + (kGateUp ? 0 : half);
+              x0 = *reinterpret_cast<const uint4*>(src + ((c0 ^ (r & 7)) << 4));
+              if (kGateUp) x1 = *reinterpret_cast<const uint4*>(src + (((c0 + 1) ^ (r & 7)) << 4));
+            }
             if (ks == C::SLOT_K - 1 || kb == nk - 1) {
               __syncwarp();
               if (lane == 0) tc::mbar_arrive(cempty + cs);  // the slot's codes are all read
@@ -369,6 +397,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             sc[u] = __ldg(reinterpret_cast<const unsigned short*>(sp) + ((kb + PD) >> gs));
           if (!tc::mbar_wait(empty + s, ph ^ 1, abort_flag, a.status)) { ok = false; break; }
           uint8_t* dst = A_of(s, mat) + soff;
+          if (kBits == 8) {
+            // 8 codes (bytes m0..m7, natural order) per chunk -> bf16 pairs (m0,m4) (m1,m5)
+            // (m2,m6) (m3,m7); q * s is exact in fp32 and rounded once to bf16
+            const uint32_t wds8[16] = {x8[0].x, x8[0].y, x8[0].z, x8[0].w, x8[1].x, x8[1].y,
+                                       x8[1].z, x8[1].w, x8[2].x, x8[2].y, x8[2].z, x8[2].w,
+                                       x8[3].x, x8[3].y, x8[3].z, x8[3].w};
+#pragma unroll
+            for (int j = 0; j < (kGateUp ? 8 : 4); ++j) {
+              float v[8];
+              codes8_scaled(wds8[2 * j], sf, v);
+              codes8_scaled(wds8[2 * j + 1], sf, v + 4);
+              uint4 o;
+              o.x = pack_bf16x2(v[0], v[4]);
+              o.y = pack_bf16x2(v[1], v[5]);
+              o.z = pack_bf16x2(v[2], v[6]);
+              o.w = pack_bf16x2(v[3], v[7]);
+              const int chunk = kGateUp ? j : (half * 4 + j);
+              *reinterpret_cast<uint4*>(dst + ((chunk ^ (r & 7)) << 4)) = o;
+            }
+          } else {
           const uint32_t wds[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
           for (int j = 0; j < (kGateUp ? 8 : 4); ++j) {
@@ -381,6 +429,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int chunk = kGateUp ? j : (half * 4 + j);
             *reinterpret_cast<uint4*>(dst + ((chunk ^ (r & 7)) << 4)) = o;
           }
+          }  // 4-bit
           tc::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(full_a + s);
@@ -506,13 +555,13 @@ static bool make_row_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Codes [rows, K/2] bytes: boxes of 128 bytes (four 64-wide stages) x 128 weight rows, 128-byte
-// swizzle, zero fill past the row end.
-static bool make_code_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t K) {
+// Codes [rows, row_bytes] (K/2 for 4-bit codes, K for 8-bit): boxes of 128 bytes x 128 weight
+// rows, 128-byte swizzle, zero fill past the row end.
+static bool make_code_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
   if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
   cuuint32_t box[2] = {128, kTcBM};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -520,34 +569,42 @@ static bool make_code_tmap(CUtensorMap* m, const void* base, int64_t rows, int64
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kGateUp, int kN>
+template <bool kGateUp, int kN, int kBits>
 cudaError_t launch_gemm_tc_t(const TcArgs& a, const void* b_rows, int64_t rows, int64_t experts,
                              int num_sms, cudaStream_t stream) {
-  using C = TcCfg<kGateUp, kN>;
+  using C = TcCfg<kGateUp, kN, kBits>;
   CUtensorMap map, c0, c1;
   if (!make_row_tmap(&map, b_rows, rows, a.K, C::BOX_ROWS)) return cudaErrorInvalidValue;
   c0 = map;
   c1 = map;
   if (C::RING) {
-    if (!make_code_tmap(&c0, a.codes0, experts * a.Nw, a.K)) return cudaErrorInvalidValue;
-    if (kGateUp && !make_code_tmap(&c1, a.codes1, experts * a.Nw, a.K)) return cudaErrorInvalidValue;
+    const int64_t row_bytes = static_cast<int64_t>(a.K) * kBits / 8;
+    if (!make_code_tmap(&c0, a.codes0, experts * a.Nw, row_bytes)) return cudaErrorInvalidValue;
+    if (kGateUp && !make_code_tmap(&c1, a.codes1, experts * a.Nw, row_bytes))
+      return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<kGateUp, kN>,
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<kGateUp, kN, kBits>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
-  grouped_gemm_tc_kernel<kGateUp, kN><<<num_sms, kTcThreads, C::SMEM, stream>>>(map, c0, c1, a);
+  grouped_gemm_tc_kernel<kGateUp, kN, kBits><<<num_sms, kTcThreads, C::SMEM, stream>>>(map, c0, c1,
+                                                                                         a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_tc(const TcArgs& a, bool gate_up, const void* b_rows, int64_t rows,
                            int64_t experts, int tile_rows, int num_sms, cudaStream_t stream) {
+  if (a.bits == 8) {  // 8-bit codes: 64-row tiles (the code ring) only
+    if (tile_rows != kTcRowsSmall) return cudaErrorInvalidValue;
+    return gate_up ? launch_gemm_tc_t<true, kTcRowsSmall, 8>(a, b_rows, rows, experts, num_sms, stream)
+                   : launch_gemm_tc_t<false, kTcRowsSmall, 8>(a, b_rows, rows, experts, num_sms, stream);
+  }
   if (tile_rows == kTcRowsSmall)
-    return gate_up ? launch_gemm_tc_t<true, kTcRowsSmall>(a, b_rows, rows, experts, num_sms, stream)
-                   : launch_gemm_tc_t<false, kTcRowsSmall>(a, b_rows, rows, experts, num_sms, stream);
+    return gate_up ? launch_gemm_tc_t<true, kTcRowsSmall, 4>(a, b_rows, rows, experts, num_sms, stream)
+                   : launch_gemm_tc_t<false, kTcRowsSmall, 4>(a, b_rows, rows, experts, num_sms, stream);
   if (tile_rows != kTcRows) return cudaErrorInvalidValue;
-  return gate_up ? launch_gemm_tc_t<true, kTcRows>(a, b_rows, rows, experts, num_sms, stream)
-                 : launch_gemm_tc_t<false, kTcRows>(a, b_rows, rows, experts, num_sms, stream);
+  return gate_up ? launch_gemm_tc_t<true, kTcRows, 4>(a, b_rows, rows, experts, num_sms, stream)
+                 : launch_gemm_tc_t<false, kTcRows, 4>(a, b_rows, rows, experts, num_sms, stream);
 }
 
 }  // namespace strata

@@ -62,6 +62,7 @@ struct TcArgs {
   void* out;              // gate/up: h bf16 [rows, Nw] (pair-interleaved columns); down: y fp32
   int K, Nw;              // contraction; weight rows per expert
   int group;              // scale group size: 64, 128 or 256
+  int bits;               // code width: 4 (codes [.., K/2]) or 8 (codes [.., K])
   WsHeader* hdr;
   const int* seg_expert;
   const int* seg_row0;
@@ -88,8 +89,9 @@ struct RouteSmallArgs {
   bool do_group;
 };
 
-cudaError_t launch_quantize(const void* w, int64_t n, int64_t k, int group, uint8_t* codes,
-                            void* scales, uint32_t* status, cudaStream_t stream, int num_sms);
+cudaError_t launch_quantize(const void* w, int64_t n, int64_t k, int group, int bits,
+                            uint8_t* codes, void* scales, uint32_t* status, cudaStream_t stream,
+                            int num_sms);
 int router_num_splits(int64_t T, int64_t H, int E, int num_sms);
 cudaError_t launch_router(const void* x, const void* wr, const float* bias, int64_t T, int64_t H,
                           int E, int k, uint32_t flags, int nsplit, float* partial, int* ids,

@@ -1,25 +1,29 @@
-// K1: symmetric int4 group quantization ("Strata" MoE tuning notes, lpnh.cn/news/2730718, §2.1
+// K1: symmetric group quantization ("Strata" MoE tuning notes, lpnh.cn/news/2730718, §2.1
 // group_quantize sketch: scale = absmax / (2^(bits-1) - 1), codes = round(w / scale) clamped to
-// [-8, 7], 128 weights per group by default; 64 and 256 are accepted too).
+// the code range, 128 weights per group by default; 64 and 256 are accepted too). bits = 4 (the
+// experts' width: range [-8, 7], two codes per byte, even k in the low nibble) or 8 (range
+// [-128, 127], one code per byte).
 //
 // HBM-streaming pass: G/8 threads own one G-wide group (8 fp16 = one 16-byte load each), find the
-// group's absmax with butterfly shuffles, and write 4 bytes of packed codes each (the group's
-// G/2 bytes are contiguous) plus one fp16 scale. Each thread walks its groups with a grid-stride
-// loop, four groups' loads in flight at a time.
+// group's absmax with butterfly shuffles, and write 4 bytes of packed codes (8 for 8-bit codes)
+// each (the group's codes are contiguous) plus one fp16 scale. Each thread walks its groups with
+// a grid-stride loop, four groups' loads in flight at a time.
 //
-// Exactness: absmax / 7.0f is an IEEE fp32 division rounded once more to fp16 (no double-rounding
-// hazard: a/7 has a period-3 binary expansion, never 12 equal bits in a row), and w / s is an IEEE
-// fp32 division of two fp16 values, so rintf() decides every half-way case like the exact
-// quotient (a spurious tie would need the 11-bit ratio to sit within 2^-21 of x.5).
+// Exactness: absmax / 7.0f (or / 127.0f) is an IEEE fp32 division rounded once more to fp16 (no
+// double-rounding hazard: the exact quotient of an 11-bit significand by 7 or 127 is either exact
+// in fp16 or at least 2^-18 relative away from every fp16 midpoint), and w / s is an IEEE fp32
+// division of two fp16 values, so rintf() decides every half-way case like the exact quotient (a
+// spurious tie would need the ratio to sit within 2^-18 relative of x.5).
 #include "kernels.cuh"
 
 namespace strata {
 
-// One group: TPG lanes hold 8 fp16 each.
-template <int TPG>
+// One group: TPG lanes hold 8 fp16 each. Codes: 4 bytes per lane (4-bit) or 8 (8-bit).
+template <int TPG, int kBits>
 __device__ __forceinline__ void quantize_one(const uint4& v, unsigned half_mask, int sub, int64_t g,
-                                             uint32_t* __restrict__ codes,
+                                             void* __restrict__ codes,
                                              __half* __restrict__ scales, uint32_t* status) {
+  constexpr float kQmax = kBits == 4 ? 7.0f : 127.0f;
   // |w| as fp16 bit patterns: their integer order is the order of the magnitudes, and any pattern
   // at or above 0x7C00 is inf or nan, so one integer max gives both absmax and finiteness
   const uint32_t m01 = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
@@ -31,30 +35,39 @@ __device__ __forceinline__ void quantize_one(const uint4& v, unsigned half_mask,
   const bool finite = mbits < 0x7C00u;
   const float amax = finite ? __half2float(__ushort_as_half(static_cast<unsigned short>(mbits))) : 0.f;
   const __half* h = reinterpret_cast<const __half*>(&v);
-  __half s_h = __float2half_rn(amax / 7.0f);
+  __half s_h = __float2half_rn(amax / kQmax);
   const float s = __half2float(s_h);
-  uint32_t packed = 0;
+  uint32_t packed = 0, lo = 0, hi = 0;  // 4-bit: 8 nibbles; 8-bit: 8 bytes in (lo, hi)
   if (finite && s > 0.0f) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       float q = rintf(__half2float(h[i]) / s);
-      q = fminf(fmaxf(q, -8.0f), 7.0f);
-      packed |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xFu) << (4 * i);
+      q = fminf(fmaxf(q, -kQmax - 1.0f), kQmax);
+      const uint32_t c = static_cast<uint32_t>(static_cast<int>(q));
+      if (kBits == 4)
+        packed |= (c & 0xFu) << (4 * i);
+      else if (i < 4)
+        lo |= (c & 0xFFu) << (8 * i);
+      else
+        hi |= (c & 0xFFu) << (8 * (i - 4));
     }
   }
   if (!finite) {
     s_h = __ushort_as_half(0x7E00);  // NaN scale marks the group
     if (sub == 0) set_status(status, STRATA_DEV_NONFINITE);
   }
-  __stcs(codes + g * TPG + sub, packed);
+  if (kBits == 4)
+    __stcs(static_cast<uint32_t*>(codes) + g * TPG + sub, packed);
+  else
+    __stcs(static_cast<uint2*>(codes) + g * TPG + sub, make_uint2(lo, hi));
   if (sub == 0) scales[g] = s_h;
 }
 
 // Each TPG-lane team walks groups g, g + stride, ... with four groups' loads in flight at a time.
-template <int TPG>
+template <int TPG, int kBits>
 __global__ void __launch_bounds__(256) quantize_groups_kernel(const uint4* __restrict__ w,
                                                               int64_t n_groups,
-                                                              uint32_t* __restrict__ codes,
+                                                              void* __restrict__ codes,
                                                               __half* __restrict__ scales,
                                                               uint32_t* status) {
   const int sub = threadIdx.x & (TPG - 1);  // position in the group
@@ -74,13 +87,14 @@ __global__ void __launch_bounds__(256) quantize_groups_kernel(const uint4* __res
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t g = g0 + u * stride;
-      if (g < n_groups) quantize_one<TPG>(v[u], team_mask, sub, g, codes, scales, status);
+      if (g < n_groups) quantize_one<TPG, kBits>(v[u], team_mask, sub, g, codes, scales, status);
     }
   }
 }
 
-cudaError_t launch_quantize(const void* w, int64_t n, int64_t k, int group, uint8_t* codes,
-                            void* scales, uint32_t* status, cudaStream_t stream, int num_sms) {
+cudaError_t launch_quantize(const void* w, int64_t n, int64_t k, int group, int bits,
+                            uint8_t* codes, void* scales, uint32_t* status, cudaStream_t stream,
+                            int num_sms) {
   const int64_t n_groups = n * (k / group);
   if (n_groups == 0) return cudaSuccess;
   const int threads = 256;
@@ -89,17 +103,23 @@ cudaError_t launch_quantize(const void* w, int64_t n, int64_t k, int group, uint
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;  // ~8 resident blocks/SM, grid-stride
   if (blocks > cap) blocks = cap;
   const uint4* wv = static_cast<const uint4*>(w);
-  uint32_t* cv = reinterpret_cast<uint32_t*>(codes);
   __half* sv = static_cast<__half*>(scales);
   const unsigned b = static_cast<unsigned>(blocks);
-  if (tpg == 8)
-    quantize_groups_kernel<8><<<b, threads, 0, stream>>>(wv, n_groups, cv, sv, status);
-  else if (tpg == 16)
-    quantize_groups_kernel<16><<<b, threads, 0, stream>>>(wv, n_groups, cv, sv, status);
-  else if (tpg == 32)
-    quantize_groups_kernel<32><<<b, threads, 0, stream>>>(wv, n_groups, cv, sv, status);
-  else
+#define STRATA_Q(T, B) quantize_groups_kernel<T, B><<<b, threads, 0, stream>>>(wv, n_groups, codes, sv, status)
+  if (bits == 4) {
+    if (tpg == 8) STRATA_Q(8, 4);
+    else if (tpg == 16) STRATA_Q(16, 4);
+    else if (tpg == 32) STRATA_Q(32, 4);
+    else return cudaErrorInvalidValue;
+  } else if (bits == 8) {
+    if (tpg == 8) STRATA_Q(8, 8);
+    else if (tpg == 16) STRATA_Q(16, 8);
+    else if (tpg == 32) STRATA_Q(32, 8);
+    else return cudaErrorInvalidValue;
+  } else {
     return cudaErrorInvalidValue;
+  }
+#undef STRATA_Q
   return cudaGetLastError();
 }
 

@@ -57,20 +57,25 @@ struct FwdLayout {
 // launch agree); it only steers how many contraction splits small batches get.
 constexpr int kSizingSms = 152;
 
-// Tensor-core path for batches with enough rows per expert to fill 128 x N tiles.
+// Tensor-core path for batches with enough rows per expert to fill 128 x N tiles, and for layers
+// with 8-bit codes at every batch size (the warp kernels read 4-bit codes only).
 static bool use_tc_path(const strata_moe_layer* L, int64_t T) {
+  if (L->bits == 8) return true;
   if (L->flags & STRATA_FORCE_WARP_PATH) return false;
   if (L->flags & STRATA_FORCE_TC_PATH) return true;
   return T >= 128;
 }
 // Token rows per tensor-core tile: 64 when the routed experts average at most 48 rows (the
-// small-tile kernel streams its code tiles through a deep TMA ring), else 256.
+// small-tile kernel streams its code tiles through a deep TMA ring) or the codes are 8-bit (they
+// go through that ring only), else 256.
 static int tc_tile_rows(const strata_moe_layer* L, int64_t T) {
+  if (L->bits == 8) return kTcRowsSmall;
   return T * L->k <= 48 * static_cast<int64_t>(L->E) ? kTcRowsSmall : kTcRows;
 }
 static int layer_group(const strata_moe_layer* L) {
   return L->group_size == 0 ? STRATA_GROUP : L->group_size;
 }
+static int layer_bits(const strata_moe_layer* L) { return L->bits == 0 ? 4 : L->bits; }
 
 static FwdLayout fwd_layout(const strata_moe_layer* L, int64_t T) {
   FwdLayout F{};
@@ -137,6 +142,7 @@ static strata_status check_layer(const strata_moe_layer* L) {
   if (L->H <= 0 || L->I <= 0 || L->H > kMaxDim || L->I > kMaxDim) return STRATA_ERR_SHAPE;
   const int G = layer_group(L);
   if (G != 64 && G != 128 && G != 256) return STRATA_ERR_UNSUPPORTED;
+  if (layer_bits(L) != 4 && layer_bits(L) != 8) return STRATA_ERR_UNSUPPORTED;
   if (L->H % STRATA_GROUP || L->I % STRATA_GROUP || L->H % G || L->I % G) return STRATA_ERR_SHAPE;
   if (L->has_shared != 0 && L->has_shared != 1) return STRATA_ERR_INVALID_ARG;
   if (L->E < 1 || L->E + L->has_shared > STRATA_MAX_EXPERTS) return STRATA_ERR_UNSUPPORTED;
@@ -183,6 +189,8 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
   const FwdLayout F = fwd_layout(L, T);
   // the per-warp decode kernel (odd group counts, 2-byte-aligned scales) has 128-wide groups only
   if (!F.tc && !F.cta && layer_group(L) != STRATA_GROUP) return STRATA_ERR_UNSUPPORTED;
+  // 8-bit codes run on the tensor-core kernel, which a forced warp path would bypass
+  if (layer_bits(L) == 8 && (L->flags & STRATA_FORCE_WARP_PATH)) return STRATA_ERR_UNSUPPORTED;
   if (!ws || !aligned(ws, kAlign)) return STRATA_ERR_WORKSPACE;
   if (ws_bytes < F.total) return STRATA_ERR_WORKSPACE;
 
@@ -288,6 +296,7 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     if (e != cudaSuccess) return STRATA_ERR_CUDA;
     TcArgs g{};
     g.group = layer_group(L);
+    g.bits = layer_bits(L);
     g.codes0 = L->gate_codes;
     g.scales0 = static_cast<const __half*>(L->gate_scales);
     g.codes1 = L->up_codes;
@@ -397,7 +406,16 @@ int strata_version(void) { return 100; }
 strata_status strata_quantize_groups(const void* w_fp16, int64_t n, int64_t k, int32_t group_size,
                                      uint8_t* codes, void* scales_fp16, uint32_t* dev_status,
                                      strata_stream stream) {
+  return strata_quantize_groups_bits(w_fp16, n, k, group_size, 4, codes, scales_fp16, dev_status,
+                                     stream);
+}
+
+strata_status strata_quantize_groups_bits(const void* w_fp16, int64_t n, int64_t k,
+                                          int32_t group_size, int32_t bits, uint8_t* codes,
+                                          void* scales_fp16, uint32_t* dev_status,
+                                          strata_stream stream) {
   if (group_size != 64 && group_size != 128 && group_size != 256) return STRATA_ERR_UNSUPPORTED;
+  if (bits != 4 && bits != 8) return STRATA_ERR_UNSUPPORTED;
   if (n < 0 || k <= 0 || k % group_size) return STRATA_ERR_SHAPE;
   if (n > (int64_t(1) << 40) / k) return STRATA_ERR_SHAPE;
   if (n == 0) return STRATA_OK;
@@ -407,7 +425,7 @@ strata_status strata_quantize_groups(const void* w_fp16, int64_t n, int64_t k, i
     return STRATA_ERR_INVALID_ARG;
   int sms = 0;
   if (device_sms(&sms) != 0) return STRATA_ERR_CUDA;
-  return cuda_fail(launch_quantize(w_fp16, n, k, group_size, codes, scales_fp16, dev_status,
+  return cuda_fail(launch_quantize(w_fp16, n, k, group_size, bits, codes, scales_fp16, dev_status,
                                    reinterpret_cast<cudaStream_t>(stream), sms));
 }
 

@@ -2,32 +2,35 @@
 
 Holds torch tensors (torch is used for device memory and streams only) and
 fills the C struct with their addresses. Expert weights arrive as fp16 host
-arrays and are quantized on the device by strata_quantize_groups.
+arrays and are quantized on the device by strata_quantize_groups_bits (4-bit
+codes, two per byte, by default; 8-bit codes, one per byte, with bits=8).
 """
 from __future__ import annotations
 
 import ctypes
 
 from . import (GROUP, StrataError, check, ptr, strata_moe_layer, strata_moe_workspace_size,
-               strata_quantize_groups, strata_read_status)
+               strata_quantize_groups_bits, strata_read_status)
 
 
 class MoELayer:
     def __init__(self, H: int, I: int, E: int, k: int, shared: int, flags: int = 0,
-                 device: str = "cuda", group: int = GROUP):
+                 device: str = "cuda", group: int = GROUP, bits: int = 4):
         import torch
         self.H, self.I, self.E, self.k, self.shared, self.flags = H, I, E, k, shared, flags
         self.group = group
+        self.bits = bits
+        per = 8 // bits  # codes per byte
         self.device = torch.device(device)
         n = E + shared
         u8, f16, f32 = torch.uint8, torch.float16, torch.float32
         self.w_router = torch.zeros(E, H, dtype=f32, device=self.device)
         self.bias = None
-        self.gate_codes = torch.zeros(n, I, H // 2, dtype=u8, device=self.device)
+        self.gate_codes = torch.zeros(n, I, H // per, dtype=u8, device=self.device)
         self.gate_scales = torch.zeros(n, I, H // group, dtype=f16, device=self.device)
-        self.up_codes = torch.zeros(n, I, H // 2, dtype=u8, device=self.device)
+        self.up_codes = torch.zeros(n, I, H // per, dtype=u8, device=self.device)
         self.up_scales = torch.zeros(n, I, H // group, dtype=f16, device=self.device)
-        self.down_codes = torch.zeros(n, H, I // 2, dtype=u8, device=self.device)
+        self.down_codes = torch.zeros(n, H, I // per, dtype=u8, device=self.device)
         self.down_scales = torch.zeros(n, H, I // group, dtype=f16, device=self.device)
         self._status = torch.zeros(1, dtype=torch.int32, device=self.device)
         self._stage = None
@@ -58,9 +61,10 @@ class MoELayer:
             dst = self._stage[:n_el].view(src.shape)
             dst.copy_(src, non_blocking=False)
             rows, cols = src.shape
-            check(strata_quantize_groups(dst, rows, cols, codes[e], scales[e], self._status,
-                                         group_size=self.group, stream=stream),
-                  "strata_quantize_groups")
+            check(strata_quantize_groups_bits(dst, rows, cols, codes[e], scales[e], self._status,
+                                              group_size=self.group, bits=self.bits,
+                                              stream=stream),
+                  "strata_quantize_groups_bits")
 
     def check_status(self, stream=None):
         st, v = strata_read_status(self._status, stream)
@@ -84,6 +88,7 @@ class MoELayer:
         s.up_codes, s.up_scales = ptr(self.up_codes), ptr(self.up_scales)
         s.down_codes, s.down_scales = ptr(self.down_codes), ptr(self.down_scales)
         s.group_size = self.group
+        s.bits = self.bits
         return s
 
     def workspace_size(self, T_max: int) -> int:
@@ -91,7 +96,7 @@ class MoELayer:
 
     def expert_bytes(self) -> int:
         n = 3 * self.H * self.I
-        return n // 2 + 2 * (n // self.group)
+        return n * self.bits // 8 + 2 * (n // self.group)
 
 
 __all__ = ["MoELayer", "ctypes"]

@@ -31,8 +31,8 @@ def bf16_to_np_bits(t) -> np.ndarray:
 class OracleExperts:
     """Oracle-side expert provider: regenerate the fp16 weights, quantize with the oracle."""
 
-    def __init__(self, wl, layer=0, overrides=None, group=128):
-        self.wl, self.layer, self.group = wl, layer, group
+    def __init__(self, wl, layer=0, overrides=None, group=128, bits=4):
+        self.wl, self.layer, self.group, self.bits = wl, layer, group, bits
         self.cache = {}
         self.overrides = overrides or {}
 
@@ -45,16 +45,17 @@ class OracleExperts:
         if e not in self.cache:
             if len(self.cache) > 4:
                 self.cache.clear()
-            self.cache[e] = tuple(oracle.quantize_groups(m, group=self.group) for m in self.fp16(e))
+            self.cache[e] = tuple(oracle.quantize_groups(m, group=self.group, bits=self.bits)
+                                  for m in self.fp16(e))
         return self.cache[e]
 
 
 def build_gpu_layer(wl, layer=0, router_kind=None, flags=0, bias=None, w_router=None,
-                    overrides=None, threads=0, experts=None, group=128):
+                    overrides=None, threads=0, experts=None, group=128, bits=4):
     """MoELayer with the workload's router and experts, quantized on the device."""
     from int4_grouped_expert_gb300 import MoELayer
     torch = torch_mod()
-    L = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared, flags=flags, group=group)
+    L = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared, flags=flags, group=group, bits=bits)
     wr = gen.router_weight(wl, layer) if w_router is None else w_router
     b = gen.router_bias(wl, layer, router_kind) if bias is None else bias
     L.set_router(wr, b)

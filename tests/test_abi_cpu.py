@@ -56,6 +56,12 @@ def test_quantize_host_checks(st):
     assert st.strata_quantize_groups(A + 2, 4, 256, A, A) == 1
     assert st.strata_quantize_groups(A, -1, 256, A, A) == 2
     assert st.strata_quantize_groups(A, 0, 256, A, A) == 0
+    assert st.strata_quantize_groups_bits(A, 4, 256, A, A, bits=2) == 3
+    assert st.strata_quantize_groups_bits(A, 4, 256, A, A, bits=16) == 3
+    assert st.strata_quantize_groups_bits(A, 4, 256, A, A, group_size=512, bits=8) == 3
+    assert st.strata_quantize_groups_bits(A, 4, 100, A, A, bits=8) == 2
+    assert st.strata_quantize_groups_bits(A + 2, 4, 256, A, A, bits=8) == 1
+    assert st.strata_quantize_groups_bits(A, 0, 256, A, A, bits=8) == 0
 
 
 def layer(st, **kw):
@@ -82,7 +88,8 @@ def test_workspace_sizes(st):
 @pytest.mark.parametrize("kw,expect", [(dict(H=1000), 2), (dict(I=100), 2), (dict(k=9, E=8), 1),
                                        (dict(k=33, E=64), 1), (dict(E=0), 3), (dict(flags=8), 1),
                                        (dict(has_shared=2), 1), (dict(gate_codes=None), 1),
-                                       (dict(up_codes=(1 << 12) + 8), 1)])
+                                       (dict(up_codes=(1 << 12) + 8), 1), (dict(bits=3), 3),
+                                       (dict(bits=8, flags=0x100), 3)])
 def test_forward_host_checks(st, kw, expect):
     A = 1 << 12
     assert st.strata_moe_forward(layer(st, **kw), A, 4, 2 * A, A, 1 << 30) == expect

@@ -33,7 +33,8 @@ def check_layer(wl, L, wr, b, x, layer=0, residual=False, renorm=False, rows=Non
                 overrides=None):
     g = run_forward(L, x)
     tokens = np.arange(x.shape[0]) if rows is None else np.asarray(rows)
-    experts = OracleExperts(wl, layer, overrides, group=getattr(L, "group", 128))
+    experts = OracleExperts(wl, layer, overrides, group=getattr(L, "group", 128),
+                            bits=getattr(L, "bits", 4))
     ref = oracle.moe_forward(x, wr, b, wl.k, experts, wl.E, wl.shared,
                              renorm=renorm, residual=residual, tokens=tokens)
     full_ref = oracle.route_topk(x, wr, b, wl.k, renorm=renorm)
@@ -240,3 +241,48 @@ def test_other_group_sizes(group, T):
     wl = CONFIGS["c1"]
     L, wr, b = build_gpu_layer(wl, group=group)
     check_layer(wl, L, wr, b, gen.activations(T, wl.H, wl.seed, name=f"g{group}_{T}"))
+
+
+@pytest.mark.parametrize("group,T", [(128, 1), (128, 16), (128, 63), (128, 100), (128, 200),
+                                     (64, 16), (64, 200), (256, 16), (256, 200)])
+def test_8bit_experts(group, T):
+    """Experts with 8-bit codes (one per byte, bit-exact vs the oracle's 8-bit quantizer) on the
+    tensor-core kernel's 8-bit dequant, with the one-launch decode router (T <= 64) and the
+    multi-launch router (100, 200)."""
+    wl = CONFIGS["c1"]
+    L, wr, b = build_gpu_layer(wl, group=group, bits=8)
+    check_layer(wl, L, wr, b, gen.activations(T, wl.H, wl.seed, name=f"b8_{group}_{T}"))
+
+
+def test_8bit_experts_decode_layer():
+    """8-bit experts at the headline decode shape (H4096 I1536, 288 experts top-8 + shared), T=16."""
+    wl = CONFIGS["c2"]
+    L, wr, b = build_gpu_layer(wl, bits=8)
+    check_layer(wl, L, wr, b, gen.activations(16, wl.H, wl.seed, name="b8_c2"))
+
+
+def test_8bit_layer_odd_group_counts_and_forced_warp_path():
+    """8-bit codes run on the tensor-core kernel at any shape (here H/128 = 3, a count the decode
+    kernel cannot take); forcing the warp path is refused."""
+    import int4_grouped_expert_gb300 as st
+    torch = __import__("torch")
+    wl = Workload("odd8", "odd-groups", H=384, I=256, E=4, k=2, shared=0, batches=(4,),
+                  router="uniform")
+    L, wr, b = build_gpu_layer(wl, bits=8)
+    check_layer(wl, L, wr, b, gen.activations(4, wl.H, 1, name="odd8"))
+    L.flags |= st.STRATA_FORCE_WARP_PATH
+    x = bf16_tensor(gen.activations(4, wl.H, 1, name="odd8"))
+    out = torch.empty_like(x)
+    ws = torch.empty(L.workspace_size(4), dtype=torch.uint8, device="cuda")
+    assert st.strata_moe_forward(L.struct(), x, 4, out, ws, ws.numel()) == 3   # UNSUPPORTED
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_tc_small_tiles_partial_code_slot(bits):
+    """The 64-row tensor-core tiles (few rows per expert) with a contraction of 6 stages: 4-bit
+    code slots hold 4 stages, so the second slot of each row is half past the row end (zero
+    fill); 8-bit slots hold 2."""
+    wl = Workload("slot", "partial-slot", H=384, I=256, E=16, k=2, shared=1, batches=(200,),
+                  router="uniform")
+    L, wr, b = build_gpu_layer(wl, bits=bits)
+    check_layer(wl, L, wr, b, gen.activations(200, wl.H, 3, name=f"slot{bits}"))

@@ -16,21 +16,27 @@ pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "quantize_cases.json")
 
 
-def gpu_quantize(w16: np.ndarray, status=None, group=128):
+def gpu_quantize(w16: np.ndarray, status=None, group=128, bits=4):
     import torch
     import int4_grouped_expert_gb300 as st
     n, k = w16.shape
     w = torch.from_numpy(w16).cuda()
-    codes = torch.full((n, k // 2), 0xAB, dtype=torch.uint8, device="cuda")
+    codes = torch.full((n, k * bits // 8), 0xAB, dtype=torch.uint8, device="cuda")
     scales = torch.full((n, k // group), 7.0, dtype=torch.float16, device="cuda")
-    st.check(st.strata_quantize_groups(w, n, k, codes, scales, status, group_size=group), "quantize")
+    if bits == 4:
+        st.check(st.strata_quantize_groups(w, n, k, codes, scales, status, group_size=group),
+                 "quantize")
+    else:
+        st.check(st.strata_quantize_groups_bits(w, n, k, codes, scales, status, group_size=group,
+                                                bits=bits), "quantize")
     torch.cuda.synchronize()
-    return codes.cpu().numpy(), scales.cpu().numpy()
+    c = codes.cpu().numpy()
+    return (c if bits == 4 else c.view(np.int8)), scales.cpu().numpy()
 
 
-def assert_same(w16, group=128):
-    c, s = gpu_quantize(w16, group=group)
-    rc, rs = oracle.quantize_groups(w16, group=group)
+def assert_same(w16, group=128, bits=4):
+    c, s = gpu_quantize(w16, group=group, bits=bits)
+    rc, rs = oracle.quantize_groups(w16, group=group, bits=bits)
     np.testing.assert_array_equal(s.view(np.uint16), rs.view(np.uint16))
     np.testing.assert_array_equal(c, rc)
 
@@ -121,3 +127,47 @@ def test_other_group_sizes(group, n, k):
     w = gen.expert_weight(2, 0, n, "down", n, k).astype(np.float32)
     w *= np.float32(2.0 ** (-6 if group == 64 else 2))
     assert_same(w.astype(np.float16), group=group)
+
+
+# ---------------------------------------------------------------- 8-bit codes
+
+def test_golden_groups_8bit():
+    for g in json.load(open(GOLDEN))["groups_8bit"]:
+        w = np.zeros((1, 128), dtype=np.float16)
+        for i, v in g["nonzero"]:
+            w[0, i] = v
+        c, s = gpu_quantize(w, bits=8)
+        assert float(s[0, 0]) == g["scale"], g["why"]
+        expect = np.zeros(128, dtype=np.int8)
+        for i, q in g["codes_nonzero"]:
+            expect[i] = q
+        np.testing.assert_array_equal(c[0], expect, err_msg=g["why"])
+
+
+@pytest.mark.parametrize("group", [64, 128, 256])
+@pytest.mark.parametrize("n,k", [(1, 256), (37, 1280), (5, 7168)])
+def test_8bit_codes_match_oracle(group, n, k):
+    """8-bit codes: scale = absmax / 127, one int8 code per byte; bit-exact against the oracle."""
+    w = gen.expert_weight(3, 0, n, "gate", n, k)
+    assert_same(w, group=group, bits=8)
+
+
+@pytest.mark.parametrize("scale_exp", [-20, -14, 0, 8])
+def test_8bit_extreme_scales(scale_exp):
+    w = gen.expert_weight(4, 0, 1, "up", 16, 1024).astype(np.float32)
+    w = (w * np.float32(2.0 ** scale_exp)).astype(np.float16)
+    assert_same(w, bits=8)
+
+
+def test_8bit_zero_groups_and_argument_errors():
+    import torch
+    import int4_grouped_expert_gb300 as st
+    w16 = np.zeros((3, 384), dtype=np.float16)
+    w16[1, 128:256] = np.float16(0.25)
+    assert_same(w16, bits=8)
+    w = torch.zeros(4, 256, dtype=torch.float16, device="cuda")
+    c = torch.zeros(4, 256, dtype=torch.uint8, device="cuda")
+    s = torch.zeros(4, 2, dtype=torch.float16, device="cuda")
+    assert st.strata_quantize_groups_bits(w, 4, 256, c, s, bits=2) == 3          # UNSUPPORTED
+    assert st.strata_quantize_groups_bits(w, 4, 200, c, s, bits=8) == 2          # SHAPE
+    assert st.strata_quantize_groups_bits(w, 0, 256, c, s, bits=8) == 0          # empty
