@@ -39,6 +39,16 @@ __device__ __forceinline__ uint32_t lane_id() {
 
 // ---------------------------------------------------------------------------- mma.sync bf16
 // D = A(16x16 bf16, row) * B(16x8 bf16, col) + C (fp32).
+// D = A * B + C, m16n8k16, f16 inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1, const float (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%11,%12,%13};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+        "f"(c[2]), "f"(c[3]));
+}
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                                uint32_t b1, const float (&c)[4]) {
   asm volatile(
@@ -97,6 +107,32 @@ __device__ __forceinline__ uint4 ldg_hint(const uint4* p, uint64_t pol) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p), "l"(pol));
   return v;
+}
+
+// Two fp32 values as an f16x2 word (lo in the low half), rounded to nearest and saturated to
+// +-65504 (finite inputs never become inf; NaN stays NaN).
+__device__ __forceinline__ uint32_t f32x2_to_f16x2_sat(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ __half f32_to_f16_sat(float x) {
+  unsigned short d;
+  asm("cvt.rn.satfinite.f16.f32 %0, %1;" : "=h"(d) : "f"(x));
+  return __ushort_as_half(d);
+}
+// The two bf16 values of a word as fp32 (exact), low half first.
+__device__ __forceinline__ float bf16_lo_f32(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+// One 8-wide chunk of bf16 activations (natural order, words (x0,x1) (x2,x3) (x4,x5) (x6,x7)) as
+// f16 in the pair-interleaved order (x0,x4) (x1,x5) (x2,x6) (x3,x7) the decode GEMM reads.
+__device__ __forceinline__ uint4 bf16_chunk_to_f16_pairs(uint4 v) {
+  uint4 o;
+  o.x = f32x2_to_f16x2_sat(bf16_lo_f32(v.x), bf16_lo_f32(v.z));
+  o.y = f32x2_to_f16x2_sat(bf16_hi_f32(v.x), bf16_hi_f32(v.z));
+  o.z = f32x2_to_f16x2_sat(bf16_lo_f32(v.y), bf16_lo_f32(v.w));
+  o.w = f32x2_to_f16x2_sat(bf16_hi_f32(v.y), bf16_hi_f32(v.w));
+  return o;
 }
 
 // silu(u) = u * sigmoid(u) with the fast exp and divide intrinsics (a few ulp of fp32: the result

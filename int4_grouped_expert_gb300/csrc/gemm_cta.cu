@@ -22,10 +22,15 @@
 //    slots. The activations are stored with every 8-wide chunk in (0,4,1,5,2,6,3,7) order (x by the
 //    router, h by the gate/up epilogue), which is exactly the B-fragment pairing. A dot product does
 //    not depend on the order of its terms, so no weight re-layout is needed.
-//  * int4 -> bf16 in one LOP3 per code pair: flipping each nibble's sign bit and OR-ing it into the
-//    low mantissa of bf16 128 yields q + 136 exactly. The +136 is removed after the group's MMAs
-//    with a correction MMA (A = 136 everywhere, same B) shared by both tiles, and the group's fp16
-//    scale is applied in fp32: acc += s * (partial - correction). Weights are never rounded.
+//  * The MMAs take f16 operands: the activations the decode path stages (x by the router or the
+//    row gather, h by the gate/up epilogue) are f16, converted exactly from bf16 (saturated at
+//    +-65504). int4 -> f16 takes one LOP3 per code pair and one shift per 8 codes: each word's
+//    nibbles 0/4 and 2/6 (after >> 8) become f16 1032 + q, nibbles 1/5 and 3/7 become
+//    1152 + 16 q without a shift (f16 has 10 mantissa bits). The low planes multiply the
+//    activation pairs (x0,x4), (x2,x6), the high planes (x1,x5), (x3,x7); correction MMAs with
+//    A = 1032 and A = 1152 (shared by both tiles) remove the offsets, and the group's fp16 scale
+//    is applied in fp32: acc += s * ((P_lo - C_lo) + (P_hi - C_hi) / 16). Weights are never
+//    rounded.
 //  * Small batches split the contraction; the last split to arrive (device counter per warp tile)
 //    sums the partials in split order and applies the epilogue, so results stay deterministic.
 // Gate/up writes h = silu(u) * v (bf16); down writes y (fp32) for the combine.
@@ -57,11 +62,18 @@ struct StageHdr {
 };
 static_assert(kHdrOff + static_cast<int>(sizeof(StageHdr)) <= kStageBytes, "stage layout");
 
-__device__ __forceinline__ uint32_t codes_to_bf16_biased(uint32_t v) {
+// int4 -> f16 in one LOP3 per code pair, d = (v & mask) ^ c: the masked nibbles land in the low
+// mantissa of f16 1024 with their sign bit flipped. Nibbles at bits 0-3 / 16-19 give 1032 + q;
+// nibbles at bits 4-7 / 20-23 (f16 has 10 mantissa bits, so no shift is needed) give
+// 1152 + 16 q. Both are exact.
+__device__ __forceinline__ uint32_t nib_lo_f16(uint32_t v) {
   uint32_t d;
-  // d = mask ? (v ^ c) : c, mask = 0x000F000F, c = 0x43084308: flips the nibble sign bits and
-  // puts the exponent of 128 around them
-  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(v), "n"(0x000F000F), "n"(0x43084308));
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(v), "n"(0x000F000F), "n"(0x64086408));
+  return d;
+}
+__device__ __forceinline__ uint32_t nib_hi_f16(uint32_t v) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(v), "n"(0x00F000F0), "n"(0x64806480));
   return d;
 }
 
@@ -262,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // -------------------------------------------------------------------- consumer warps
   griddep_wait();  // outputs and split-K scratch follow the previous kernel
   const int gq = lane >> 2, t4 = lane & 3;
-  const uint32_t a136[4] = {0x43084308u, 0x43084308u, 0x43084308u, 0x43084308u};
+  const uint32_t a1032[4] = {0x64086408u, 0x64086408u, 0x64086408u, 0x64086408u};  // f16 1032
+  const uint32_t a1152[4] = {0x64806480u, 0x64806480u, 0x64806480u, 0x64806480u};  // f16 1152
   const int mtile = kGateUp ? 16 : 32;
   int stage = 0;
   uint32_t phase = 0;
@@ -310,59 +323,54 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     const uint32_t w0l[4] = {a0l.x, a0l.y, a0l.z, a0l.w}, w0h[4] = {a0h.x, a0h.y, a0h.z, a0h.w};
     const uint32_t w1l[4] = {a1l.x, a1l.y, a1l.z, a1l.w}, w1h[4] = {a1h.x, a1h.y, a1h.z, a1h.w};
-    // two accumulator sets halve the MMA dependency chains: even / odd j, or (64-wide groups) the
-    // block's first and second group
-    float p0[2][4] = {}, p1[2][4] = {}, cr[2][4] = {};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int h = kG == 64 ? (j >> 1) : (j & 1);
-      // activations are stored pair-interleaved: X[4j+m] = {x[8j+m], x[8j+m+4]}
-      const uint32_t b00 = X[4 * j], b01 = X[4 * j + 1], b10 = X[4 * j + 2], b11 = X[4 * j + 3];
-      mma_bf16_16816(cr[h], a136, b00, b01, cr[h]);
-      mma_bf16_16816(cr[h], a136, b10, b11, cr[h]);
-      {
-        const uint32_t vl = w0l[j], vh = w0h[j];
-        const uint32_t fa[4] = {codes_to_bf16_biased(vl), codes_to_bf16_biased(vh),
-                                codes_to_bf16_biased(vl >> 4), codes_to_bf16_biased(vh >> 4)};
-        mma_bf16_16816(p0[h], fa, b00, b01, p0[h]);
-        const uint32_t fb[4] = {codes_to_bf16_biased(vl >> 8), codes_to_bf16_biased(vh >> 8),
-                                codes_to_bf16_biased(vl >> 12), codes_to_bf16_biased(vh >> 12)};
-        mma_bf16_16816(p0[h], fb, b10, b11, p0[h]);
-      }
-      {
-        const uint32_t vl = w1l[j], vh = w1h[j];
-        const uint32_t fa[4] = {codes_to_bf16_biased(vl), codes_to_bf16_biased(vh),
-                                codes_to_bf16_biased(vl >> 4), codes_to_bf16_biased(vh >> 4)};
-        mma_bf16_16816(p1[h], fa, b00, b01, p1[h]);
-        const uint32_t fb[4] = {codes_to_bf16_biased(vl >> 8), codes_to_bf16_biased(vh >> 8),
-                                codes_to_bf16_biased(vl >> 12), codes_to_bf16_biased(vh >> 12)};
-        mma_bf16_16816(p1[h], fb, b10, b11, p1[h]);
-      }
-    }
     auto h2f = [](uint32_t v, int sh) {
       return __half2float(__ushort_as_half(static_cast<unsigned short>(v >> sh)));
     };
-    if (kG == 64) {
-      // the pair holds the scales of the block's two groups
+    // low / high nibble planes of both tiles and their shared corrections
+    float plo0[4] = {}, phi0[4] = {}, plo1[4] = {}, phi1[4] = {}, clo[4] = {}, chi[4] = {};
+    // acc += s * partial for the rows' scales, then a fresh partial
+    auto flush = [&](float sa0, float sb0, float sa1, float sb1) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const uint32_t s0 = c < 2 ? s0a : s0b, s1 = c < 2 ? s1a : s1b;
-        acc0[c] = fmaf(h2f(s0, 0), p0[0][c] - cr[0][c], acc0[c]);
-        acc0[c] = fmaf(h2f(s0, 16), p0[1][c] - cr[1][c], acc0[c]);
-        acc1[c] = fmaf(h2f(s1, 0), p1[0][c] - cr[0][c], acc1[c]);
-        acc1[c] = fmaf(h2f(s1, 16), p1[1][c] - cr[1][c], acc1[c]);
-      }
-    } else {
-      // the block's group is the low half of its pair for an even group index, the high half else
-      const int sh = ((kG == 128 ? hd.g : hd.g >> 1) & 1) * 16;
-      const float sa0 = h2f(s0a, sh), sb0 = h2f(s0b, sh), sa1 = h2f(s1a, sh), sb1 = h2f(s1b, sh);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float q0 = (p0[0][c] - cr[0][c]) + (p0[1][c] - cr[1][c]);
-        const float q1 = (p1[0][c] - cr[0][c]) + (p1[1][c] - cr[1][c]);
+        const float corr = fmaf(0.0625f, chi[c], clo[c]);
+        const float q0 = fmaf(0.0625f, phi0[c], plo0[c]) - corr;
+        const float q1 = fmaf(0.0625f, phi1[c], plo1[c]) - corr;
         acc0[c] = fmaf(c < 2 ? sa0 : sb0, q0, acc0[c]);
         acc1[c] = fmaf(c < 2 ? sa1 : sb1, q1, acc1[c]);
+        plo0[c] = phi0[c] = plo1[c] = phi1[c] = clo[c] = chi[c] = 0.f;
       }
+    };
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // activations are stored pair-interleaved: X[4j+m] = {x[8j+m], x[8j+m+4]}
+      const uint32_t x04 = X[4 * j], x15 = X[4 * j + 1], x26 = X[4 * j + 2], x37 = X[4 * j + 3];
+      mma_f16_16816(clo, a1032, x04, x26, clo);
+      mma_f16_16816(chi, a1152, x15, x37, chi);
+      {
+        const uint32_t vl = w0l[j], vh = w0h[j], vl8 = vl >> 8, vh8 = vh >> 8;
+        const uint32_t flo[4] = {nib_lo_f16(vl), nib_lo_f16(vh), nib_lo_f16(vl8), nib_lo_f16(vh8)};
+        const uint32_t fhi[4] = {nib_hi_f16(vl), nib_hi_f16(vh), nib_hi_f16(vl8), nib_hi_f16(vh8)};
+        mma_f16_16816(plo0, flo, x04, x26, plo0);
+        mma_f16_16816(phi0, fhi, x15, x37, phi0);
+      }
+      {
+        const uint32_t vl = w1l[j], vh = w1h[j], vl8 = vl >> 8, vh8 = vh >> 8;
+        const uint32_t flo[4] = {nib_lo_f16(vl), nib_lo_f16(vh), nib_lo_f16(vl8), nib_lo_f16(vh8)};
+        const uint32_t fhi[4] = {nib_hi_f16(vl), nib_hi_f16(vh), nib_hi_f16(vl8), nib_hi_f16(vh8)};
+        mma_f16_16816(plo1, flo, x04, x26, plo1);
+        mma_f16_16816(phi1, fhi, x15, x37, phi1);
+      }
+      if (kG == 64 && (j == 1 || j == 3)) {
+        // 64-wide groups: j = 0, 1 are the block's first group (low half of the scale pair),
+        // j = 2, 3 its second (high half)
+        const int sh = j == 1 ? 0 : 16;
+        flush(h2f(s0a, sh), h2f(s0b, sh), h2f(s1a, sh), h2f(s1b, sh));
+      }
+    }
+    if (kG != 64) {
+      // the block's group is the low half of its pair for an even group index, the high half else
+      const int sh = ((kG == 128 ? hd.g : hd.g >> 1) & 1) * 16;
+      flush(h2f(s0a, sh), h2f(s0b, sh), h2f(s1a, sh), h2f(s1b, sh));
     }
     if (hd.g != hd.gend - 1) continue;
 
@@ -406,11 +414,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (col >= hd.nvalid) continue;
         const int64_t orow = hd.rbase + col;
         if (kGateUp) {
-          // h columns are stored pair-interleaved inside every 8 (the down GEMM's B order)
+          // h columns are stored pair-interleaved inside every 8 (the down GEMM's B order), as f16
           const int n0 = mt * 16 + (gq < 4 ? 2 * gq : 2 * gq - 7);
-          __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(a.out) + orow * a.N;
-          hrow[n0] = __float2bfloat16_rn(silu_f(acc0[c]) * acc1[c]);
-          hrow[n0 + 8] = __float2bfloat16_rn(silu_f(acc0[c + 2]) * acc1[c + 2]);
+          __half* hrow = static_cast<__half*>(a.out) + orow * a.N;
+          hrow[n0] = f32_to_f16_sat(silu_f(acc0[c]) * acc1[c]);
+          hrow[n0 + 8] = f32_to_f16_sat(silu_f(acc0[c + 2]) * acc1[c + 2]);
         } else {
           const int n0 = mt * 32 + gq;
           float* y = static_cast<float*>(a.out) + orow * a.N;

@@ -497,10 +497,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ----------------------------------------------------------------------------- gather
 
-// xp[r] = x[perm[r]] with every 8-wide chunk stored in (0,4,1,5,2,6,3,7) order.
+// xp[r] = x[perm[r]] with every 8-wide chunk stored in (0,4,1,5,2,6,3,7) order: bf16 for the
+// tensor-core and per-warp GEMMs, f16 (exact, saturated at +-65504) for the CTA-staged one.
+template <bool kF16>
 __global__ void __launch_bounds__(128) gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
                                                           const int* __restrict__ perm, int H,
-                                                          __nv_bfloat16* __restrict__ xp) {
+                                                          uint16_t* __restrict__ xp) {
   const int row = blockIdx.x;
   const int tok = perm[row];
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tok) * H);
@@ -508,20 +510,28 @@ __global__ void __launch_bounds__(128) gather_rows_kernel(const __nv_bfloat16* _
   for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
     const uint4 v = __ldg(src + c);
     uint4 o;
-    o.x = prmt(v.x, v.z, 0x5410);  // x0, x4
-    o.y = prmt(v.x, v.z, 0x7632);  // x1, x5
-    o.z = prmt(v.y, v.w, 0x5410);  // x2, x6
-    o.w = prmt(v.y, v.w, 0x7632);  // x3, x7
+    if (kF16) {
+      o = bf16_chunk_to_f16_pairs(v);
+    } else {
+      o.x = prmt(v.x, v.z, 0x5410);  // x0, x4
+      o.y = prmt(v.x, v.z, 0x7632);  // x1, x5
+      o.z = prmt(v.y, v.w, 0x5410);  // x2, x6
+      o.w = prmt(v.y, v.w, 0x7632);  // x3, x7
+    }
     dst[c] = o;
   }
 }
 
 cudaError_t launch_gather_rows(const void* x, const int* perm, int64_t rows, int64_t H, void* xp,
-                               cudaStream_t stream) {
+                               bool f16, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  gather_rows_kernel<<<static_cast<unsigned>(rows), 128, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(x), perm, static_cast<int>(H),
-      static_cast<__nv_bfloat16*>(xp));
+  const unsigned g = static_cast<unsigned>(rows);
+  const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(x);
+  uint16_t* xd = static_cast<uint16_t*>(xp);
+  if (f16)
+    gather_rows_kernel<true><<<g, 128, 0, stream>>>(xs, perm, static_cast<int>(H), xd);
+  else
+    gather_rows_kernel<false><<<g, 128, 0, stream>>>(xs, perm, static_cast<int>(H), xd);
   return cudaGetLastError();
 }
 

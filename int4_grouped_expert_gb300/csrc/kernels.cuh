@@ -36,7 +36,8 @@ struct GemmArgs {
   const __half* scales0;     // [experts, N, K/128]
   const uint8_t* codes1;     // up codes (gate/up mode)
   const __half* scales1;
-  const __nv_bfloat16* act;  // gate/up: x [T, K]; down: h [rows, K]
+  const __nv_bfloat16* act;  // gate/up: x [T, K]; down: h [rows, K]; pair-interleaved chunks,
+                             // f16 for the CTA-staged kernel (the type only sets the stride)
   const int* perm;           // token (activation row) of each GEMM row, or null: row = activation row
   void* out;                 // gate/up: h bf16 [rows, N]; down: y fp32 [rows, N]
   int K;                     // contraction length (H for gate/up, I for down)
@@ -81,7 +82,8 @@ struct RouteSmallArgs {
   int T, H, E, k;
   uint32_t flags;
   int epc;                 // experts per CTA (each split over 8 / epc warps along H)
-  __nv_bfloat16* x_perm;   // [T, H]: x with every 8-wide chunk in (0,4,1,5,2,6,3,7) order, or null
+  void* x_perm;            // [T, H]: x with every 8-wide chunk in (0,4,1,5,2,6,3,7) order, or null
+  bool x_f16;              // x_perm as f16 (CTA-staged GEMM) instead of bf16 (per-warp GEMM)
   float* logits;           // [T][E] scratch
   int* ids;
   float* gates;
@@ -114,7 +116,9 @@ constexpr int kTcRowsSmall = 64;  // the same for batches with few rows per expe
 // (routed + shared); tile_rows: kTcRows or kTcRowsSmall (the grouping's chunk size)
 cudaError_t launch_gemm_tc(const TcArgs& a, bool gate_up, const void* b_rows, int64_t rows,
                            int64_t experts, int tile_rows, int num_sms, cudaStream_t stream);
+// xp[r] = x[perm[r]], pair-interleaved, as f16 (f16 = true: the CTA-staged GEMM) or bf16
 cudaError_t launch_gather_rows(const void* x, const int* perm, int64_t rows, int64_t H, void* xp,
+                               bool f16,
                                cudaStream_t stream);
 cudaError_t launch_combine(const float* y, const float* gates, const int* inv, const void* x,
                            int64_t T, int64_t H, int k, int has_shared, int64_t R, int residual,

@@ -271,18 +271,23 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
     if (a.bias) v += a.bias[ee];
     a.logits[static_cast<int64_t>(t) * E + ee] = v;
   }
-  // The decode grouped GEMM reads x with every 8-wide chunk pair-interleaved. Only the GEMMs, which
-  // wait for this grid, read the copy, so the CTAs that do not take part in the top-k make it after
-  // signalling their logits (off the top-k's path); with no such CTA every CTA copies first.
+  // The decode grouped GEMM reads x with every 8-wide chunk pair-interleaved (as f16 for the
+  // CTA-staged kernel, bf16 for the per-warp one). Only the GEMMs, which wait for this grid, read
+  // the copy, so the CTAs that do not take part in the top-k make it after signalling their logits
+  // (off the top-k's path); with no such CTA every CTA copies first.
   auto copy_x = [&](int part, int nparts) {
     const int nv = T * (H / 8);
     for (int i = part * blockDim.x + threadIdx.x; i < nv; i += nparts * blockDim.x) {
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
       uint4 o;
-      o.x = prmt(v.x, v.z, 0x5410);
-      o.y = prmt(v.x, v.z, 0x7632);
-      o.z = prmt(v.y, v.w, 0x5410);
-      o.w = prmt(v.y, v.w, 0x7632);
+      if (a.x_f16) {
+        o = bf16_chunk_to_f16_pairs(v);
+      } else {
+        o.x = prmt(v.x, v.z, 0x5410);
+        o.y = prmt(v.x, v.z, 0x7632);
+        o.z = prmt(v.y, v.w, 0x5410);
+        o.w = prmt(v.y, v.w, 0x7632);
+      }
       reinterpret_cast<uint4*>(a.x_perm)[i] = o;
     }
   };

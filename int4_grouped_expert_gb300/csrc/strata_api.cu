@@ -275,7 +275,8 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     ra.logits = reinterpret_cast<float*>(base + F.r.partial);
     ra.ids = ids;
     ra.gates = gates;
-    ra.x_perm = F.tc ? nullptr : reinterpret_cast<__nv_bfloat16*>(base + F.xp);
+    ra.x_perm = F.tc ? nullptr : base + F.xp;
+    ra.x_f16 = F.cta;  // the CTA-staged GEMM multiplies f16 operands
     ra.grp = pa;
     ra.do_group = true;
     e = launch_route_small(ra, st);
@@ -292,7 +293,7 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
 
   const int64_t rows = R + (S ? T : 0);
   if (F.tc) {
-    e = launch_gather_rows(x, perm, rows, L->H, base + F.xp, st);
+    e = launch_gather_rows(x, perm, rows, L->H, base + F.xp, false, st);
     if (e != cudaSuccess) return STRATA_ERR_CUDA;
     TcArgs g{};
     g.group = layer_group(L);
@@ -335,7 +336,7 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     if (T <= kRouteSmallMaxT) {
       g.perm = perm;  // x_perm rows are tokens
     } else {
-      e = launch_gather_rows(x, perm, rows, L->H, base + F.xp, st);
+      e = launch_gather_rows(x, perm, rows, L->H, base + F.xp, F.cta, st);
       if (e != cudaSuccess) return STRATA_ERR_CUDA;
       g.perm = nullptr;  // xp rows are GEMM rows
     }
