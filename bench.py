@@ -134,11 +134,11 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- workload
 
-def build_layer(wl, threads=0, group=128):
-    """One device layer quantized from the seeded fp16 experts (strata_quantize_groups)."""
+def build_layer(wl, threads=0, group=128, bits=4):
+    """One device layer quantized from the seeded fp16 experts (strata_quantize_groups_bits)."""
     import torch
     from int4_grouped_expert_gb300 import MoELayer
-    L = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared, group=group)
+    L = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared, group=group, bits=bits)
     L.set_router(gen.router_weight(wl), gen.router_bias(wl))
     n = wl.E + wl.shared
     for s in range(0, n, 16):
@@ -155,7 +155,7 @@ def layer_copies(L0, n):
     from int4_grouped_expert_gb300 import MoELayer
     out = [L0]
     for _ in range(n - 1):
-        L = MoELayer(L0.H, L0.I, L0.E, L0.k, L0.shared, group=L0.group)
+        L = MoELayer(L0.H, L0.I, L0.E, L0.k, L0.shared, group=L0.group, bits=L0.bits)
         L.w_router = L0.w_router.clone()
         L.flags = L0.flags
         L.bias = L0.bias
@@ -359,7 +359,7 @@ def run_strata(args):
     st.lib()
     wl = CONFIGS[WORKLOAD]
     T = args.batch
-    L0 = build_layer(wl, group=args.group)
+    L0 = build_layer(wl, group=args.group, bits=args.bits)
     if args.router_fp16:
         L0.set_router(gen.router_weight(wl), gen.router_bias(wl), fp16=True)
     layers = layer_copies(L0, max(1, args.copies))
@@ -373,7 +373,7 @@ def run_strata(args):
     experts = [routed_experts(L0, x, T) for x in xs_dev]
     n_exp = float(np.mean(experts))
     eb = L0.expert_bytes()
-    gu_bytes = n_exp * (2 * wl.H * wl.I) * (0.5 + 2 / args.group)
+    gu_bytes = n_exp * (2 * wl.H * wl.I) * (args.bits / 8 + 2 / args.group)
 
     clocks = ClockSampler(local)
     time.sleep(0.3)
@@ -423,16 +423,18 @@ def run_strata(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "tokens_per_step": T, "H": wl.H, "I": wl.I, "E": wl.E,
                    "k": wl.k, "shared": wl.shared, "router": "zipf(s=1.1), top-20% take 80%",
-                   "weights": f"int4 g{args.group} codes + fp16 scales, quantized on device",
+                   "weights": f"int{args.bits} g{args.group} codes + fp16 scales, quantized on device",
                    "router_weights": "fp16" if args.router_fp16 else "fp32",
                    "l2": f"inputs larger than L2: {N_LAYER_COPIES} expert-storage copies x "
                          f"{N_TOKEN_BATCHES} token batches rotated per step",
                    "parallelism": f"replicas x{ws_n}"},
-        "roofline": {"kernel": "gate_up_gemm (grouped W4A16 GEMM + SiLU)", "bound": "hbm",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+        "roofline": {"kernel": ("gate_up_gemm (grouped W4A16 GEMM + SiLU)" if args.bits == 4 else
+                                "gate_up_gemm (tcgen05 grouped W8A16 GEMM + SiLU)"),
+                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": gu_bytes,
-                     "traffic": measured_traffic("decode_gate_up")},
+                     "traffic": (measured_traffic("decode_gate_up")
+                                 if args.bits == 4 and args.group == 128 else None)},
         "layer_hbm": {"achieved_gbs": layer_gbs, "frac": layer_gbs / peak,
                       "bytes_per_step": n_exp * eb, "experts_per_step": n_exp},
         "stages_us": {k: v * 1e3 for k, v in stages.items()},
@@ -773,6 +775,8 @@ def main(argv=None):
     p.add_argument("--router", choices=["uniform", "zipf"], default=None)
     p.add_argument("--group", type=int, choices=[64, 128, 256], default=128,
                    help="decode: scale group size of the experts")
+    p.add_argument("--bits", type=int, choices=[4, 8], default=4,
+                   help="decode: code width of the experts (8: the tensor-core W8A16 path)")
     p.add_argument("--router-fp16", action="store_true",
                    help="decode: store the router weights as fp16 (STRATA_ROUTER_FP16)")
     p.add_argument("--experts", type=int, default=0, help="prefill: override the routed expert count")
