@@ -11,7 +11,10 @@
 //    matrix (canonical row-major codes, no re-layout);
 //  * activations: the chunk's 8 rows x 128 bf16, gathered through the routing permutation by
 //    cp.async, 16-byte pieces swizzled so that the consumers' fragment loads do not conflict;
-//  * scales: the fp16 pair holding each row's scale, by 4-byte cp.async.
+//  * scales: when the scale rows allow it (row stride and base 16-byte aligned), one TMA box per
+//    matrix of 16 bytes (8 consecutive groups, the aligned run holding the stage's group) x rows;
+//    otherwise the fp16 pair holding each row's scale, by 4-byte cp.async. Either way they land
+//    on the stage's own full barrier.
 // The producer streams stages ahead (mbarrier full/empty pairs; every wait is time-bounded) while
 // the consumers compute; consumer warp w owns 16 gate + 16 up rows (gate/up) or 32 rows (down).
 //
@@ -47,12 +50,17 @@ constexpr int kThreads = (kCW + 1) * 32;   // + one producer warp
 constexpr int kStages = 5;
 constexpr int kWBytes = 16384;             // weights of one stage (256 rows x 64 bytes)
 constexpr int kActOff = kWBytes;           // 8 rows x 256 bytes
-constexpr int kScOff = kActOff + 2048;     // 256 rows x 4 bytes
-constexpr int kHdrOff = kScOff + 1024;
-constexpr int kStageBytes = 19584;         // 128-byte multiple >= kHdrOff + sizeof(StageHdr)
-constexpr int kBarOff = kStages * kStageBytes;
-constexpr int kSmemBytes = kBarOff + 2 * kStages * 8 + 16;
+constexpr int kScOff = kActOff + 2048;     // 256 rows x 4 bytes (cp.async) or 16 bytes (TMA)
 constexpr int kCtasPerSm = 2;
+// Stage layout with scales copied as 4-byte pairs (kScTma false) or as 16-byte TMA rows (true).
+template <bool kScTma>
+struct CtaLayout {
+  static constexpr int kScRowBytes = kScTma ? 16 : 4;
+  static constexpr int kHdrOff = kScOff + 256 * kScRowBytes;
+  static constexpr int kStageBytes = kScTma ? 22656 : 19584;  // 128-byte multiple >= header end
+  static constexpr int kBarOff = kStages * kStageBytes;
+  static constexpr int kSmemBytes = kBarOff + 2 * kStages * 8 + 16;
+};
 constexpr int kBlockK = 128;               // contraction per stage
 
 struct StageHdr {
@@ -60,7 +68,14 @@ struct StageHdr {
   int g, gbeg, gend;                    // this stage's group and the item's group range
   int done;                             // no more items
 };
-static_assert(kHdrOff + static_cast<int>(sizeof(StageHdr)) <= kStageBytes, "stage layout");
+static_assert(CtaLayout<false>::kHdrOff + static_cast<int>(sizeof(StageHdr)) <=
+                  CtaLayout<false>::kStageBytes,
+              "stage layout");
+static_assert(CtaLayout<true>::kHdrOff + static_cast<int>(sizeof(StageHdr)) <=
+                  CtaLayout<true>::kStageBytes,
+              "stage layout");
+static_assert(kCtasPerSm * (CtaLayout<true>::kSmemBytes + 1024) <= 228 * 1024,
+              "two CTAs per SM");
 
 // int4 -> f16 in one LOP3 per code pair, d = (v & mask) ^ c: the masked nibbles land in the low
 // mantissa of f16 1024 with their sign bit flipped. Nibbles at bits 0-3 / 16-19 give 1032 + q;
@@ -117,10 +132,17 @@ struct CtaGemmParams {
   int RB;     // rows per block (gate/up: per matrix)
 };
 
-template <bool kGateUp, int kG>
+// map0/map1: codes of gate (or down) / up; smap0/smap1: their scales (kScTma only).
+template <bool kGateUp, int kG, bool kScTma>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     grouped_gemm_cta_kernel(const __grid_constant__ CUtensorMap map0,
-                            const __grid_constant__ CUtensorMap map1, const CtaGemmParams p) {
+                            const __grid_constant__ CUtensorMap map1,
+                            const __grid_constant__ CUtensorMap smap0,
+                            const __grid_constant__ CUtensorMap smap1, const CtaGemmParams p) {
+  using Lay = CtaLayout<kScTma>;
+  constexpr int kHdrOff = Lay::kHdrOff;
+  constexpr int kStageBytes = Lay::kStageBytes;
+  constexpr int kBarOff = Lay::kBarOff;
   extern __shared__ __align__(1024) unsigned char smem[];
   const GemmArgs& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -146,6 +168,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (lane == 0) {
       tc::prefetch_tmap(&map0);
       if (kGateUp) tc::prefetch_tmap(&map1);
+      if (kScTma) {
+        tc::prefetch_tmap(&smap0);
+        if (kGateUp) tc::prefetch_tmap(&smap1);
+      }
     }
     if (kGateUp) griddep_wait();  // the work lists and x come from the router
     griddep_launch();
@@ -154,7 +180,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int nchunks = a.hdr->n_chunks;
     const int64_t srow = a.K / kG;                // scale row stride (fp16)
     const int q = lane & 15;                      // activation piece of this lane
-    const uint32_t tx_bytes = kGateUp ? 2u * p.RB * 64u : static_cast<uint32_t>(p.RB) * 64u;
+    // weights (64 bytes per row) and, with kScTma, scales (16 bytes per row) of the stage
+    constexpr uint32_t kRowTx = 64u + (kScTma ? 16u : 0u);
+    const uint32_t tx_bytes = kGateUp ? 2u * p.RB * kRowTx : static_cast<uint32_t>(p.RB) * kRowTx;
     int stage = 0;
     uint32_t phase = 0;
     bool waited = kGateUp;  // down: griddep_wait still pending (h comes from gate/up)
@@ -193,13 +221,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           if (kGateUp)
             tc::tma_load_2d_hint(st + p.RB * 64, &map1, g * 64, static_cast<int32_t>(wrow0),
                                  &full[stage], pol);
+          if (kScTma) {
+            // the aligned run of 8 scale groups holding this stage's group(s): 16 bytes per row
+            const int sx = (kG == 64 ? 2 * g : kG == 128 ? g : g >> 1) & ~7;
+            tc::tma_load_2d_hint(st + kScOff, &smap0, sx, static_cast<int32_t>(wrow0),
+                                 &full[stage], pol);
+            if (kGateUp)
+              tc::tma_load_2d_hint(st + kScOff + p.RB * 16, &smap1, sx,
+                                   static_cast<int32_t>(wrow0), &full[stage], pol);
+          }
         }
         // scales: the 4-byte fp16 pair holding group g, 8 rows per lane
         // 4-byte scale pair holding this block's scale(s): groups 2g, 2g+1 (kG = 64), g (128) or
         // g / 2 (256), the pair starting at an even group
         const int gp = kG == 64 ? 2 * g : kG == 128 ? (g & ~1) : ((g >> 1) & ~1);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < (kScTma ? 0 : 8); ++i) {
           const int r = lane + 32 * i;  // stage scale row
           const __half* sbase;
           int64_t row;
@@ -311,8 +348,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // scale pairs of rows gq, gq+8 of both tiles
     const int sr0 = kGateUp ? warp * 16 + gq : warp * 32 + gq;
     const int sr1 = kGateUp ? p.RB + warp * 16 + gq : warp * 32 + 16 + gq;
-    const uint32_t* sc = reinterpret_cast<const uint32_t*>(st + kScOff);
-    const uint32_t s0a = sc[sr0], s0b = sc[sr0 + 8], s1a = sc[sr1], s1b = sc[sr1 + 8];
+    // TMA rows: 16 bytes, the pair's word inside the stage's aligned run of 8 groups
+    constexpr int kScW = Lay::kScRowBytes / 4;
+    const int gpair = kG == 64 ? 2 * hd.g : kG == 128 ? (hd.g & ~1) : ((hd.g >> 1) & ~1);
+    const uint32_t* sc = reinterpret_cast<const uint32_t*>(st + kScOff) + (kScTma ? ((gpair & 7) >> 1) : 0);
+    const uint32_t s0a = sc[sr0 * kScW], s0b = sc[(sr0 + 8) * kScW], s1a = sc[sr1 * kScW],
+                   s1b = sc[(sr1 + 8) * kScW];
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&empty[stage]);
     if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -459,22 +500,59 @@ static bool make_codes_tmap(CUtensorMap* m, const void* base, int64_t rows, int6
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kGateUp, int kG>
+// Scales [rows, groups] fp16: boxes of 8 groups (16 bytes) x box_rows rows, zero fill. Needs a
+// 16-byte aligned base and a row stride that is a multiple of 16 bytes.
+static bool make_scales_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t groups,
+                             int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = cta_tmap_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(groups), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(groups) * 2};
+  cuuint32_t box[2] = {8, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kGateUp, int kG, bool kScTma>
 cudaError_t launch_t(const GemmArgs& a, int64_t experts, int num_sms, cudaStream_t stream) {
   CtaGemmParams p;
   p.a = a;
   p.RB = cta_gemm_block_rows(kGateUp);
   p.nblk = static_cast<int>((a.N + p.RB - 1) / p.RB);
-  CUtensorMap m0, m1;
+  CUtensorMap m0, m1, s0, s1;
   const int64_t rows = experts * a.N;
   if (!make_codes_tmap(&m0, a.codes0, rows, a.K, p.RB)) return cudaErrorInvalidValue;
   if (!make_codes_tmap(&m1, kGateUp ? a.codes1 : a.codes0, rows, a.K, p.RB))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_cta_kernel<kGateUp, kG>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (kScTma) {
+    if (!make_scales_tmap(&s0, a.scales0, rows, a.K / kG, p.RB)) return cudaErrorInvalidValue;
+    if (!make_scales_tmap(&s1, kGateUp ? a.scales1 : a.scales0, rows, a.K / kG, p.RB))
+      return cudaErrorInvalidValue;
+  } else {
+    s0 = m0;  // not read
+    s1 = m1;
+  }
+  auto kern = grouped_gemm_cta_kernel<kGateUp, kG, kScTma>;
+  constexpr int smem = CtaLayout<kScTma>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)  // two CTAs per SM need (nearly) all of its shared memory
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  return launch_kernel(grouped_gemm_cta_kernel<kGateUp, kG>, dim3(num_sms * kCtasPerSm),
-                       dim3(kThreads), kSmemBytes, stream, true, m0, m1, p);
+  return launch_kernel(kern, dim3(num_sms * kCtasPerSm), dim3(kThreads), smem, stream, true, m0,
+                       m1, s0, s1, p);
+}
+
+// The TMA scale path when every scale row starts on a 16-byte boundary.
+template <bool kGateUp, int kG>
+cudaError_t launch_g(const GemmArgs& a, int64_t experts, int num_sms, cudaStream_t stream) {
+  const int64_t row_bytes = static_cast<int64_t>(a.K / kG) * 2;
+  const bool tma = row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(a.scales0) % 16 == 0 &&
+                   (!kGateUp || reinterpret_cast<uintptr_t>(a.scales1) % 16 == 0);
+  return tma ? launch_t<kGateUp, kG, true>(a, experts, num_sms, stream)
+             : launch_t<kGateUp, kG, false>(a, experts, num_sms, stream);
 }
 
 }  // namespace
@@ -486,14 +564,14 @@ cudaError_t launch_gemm_cta(const GemmArgs& a, bool gate_up, int64_t experts, in
                             cudaStream_t stream) {
   switch (a.group) {
     case 64:
-      return gate_up ? launch_t<true, 64>(a, experts, num_sms, stream)
-                     : launch_t<false, 64>(a, experts, num_sms, stream);
+      return gate_up ? launch_g<true, 64>(a, experts, num_sms, stream)
+                     : launch_g<false, 64>(a, experts, num_sms, stream);
     case 256:
-      return gate_up ? launch_t<true, 256>(a, experts, num_sms, stream)
-                     : launch_t<false, 256>(a, experts, num_sms, stream);
+      return gate_up ? launch_g<true, 256>(a, experts, num_sms, stream)
+                     : launch_g<false, 256>(a, experts, num_sms, stream);
     default:
-      return gate_up ? launch_t<true, 128>(a, experts, num_sms, stream)
-                     : launch_t<false, 128>(a, experts, num_sms, stream);
+      return gate_up ? launch_g<true, 128>(a, experts, num_sms, stream)
+                     : launch_g<false, 128>(a, experts, num_sms, stream);
   }
 }
 
