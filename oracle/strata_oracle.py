@@ -13,7 +13,7 @@ titles, so each is named by its address):
                                               Gate/Up + Down experts, 8 routed
                                               + 1 shared per token (§01)
 
-Readings taken where the pages are silent (each is also listed in the design doc):
+Readings taken where the pages are silent:
   * quantize: round half to even (torch .round()); quotient w/s exact, from the
     scale as stored in fp16; a group whose stored scale is 0 gets codes 0;
     K % 128 != 0 is an error; non-finite weights are an error.
