@@ -11,9 +11,9 @@
 //
 // Exactness: absmax / 7.0f (or / 127.0f) is an IEEE fp32 division rounded once more to fp16 (no
 // double-rounding hazard: the exact quotient of an 11-bit significand by 7 or 127 is either exact
-// in fp16 or at least 2^-18 relative away from every fp16 midpoint), and w / s is an IEEE fp32
-// division of two fp16 values, so rintf() decides every half-way case like the exact quotient (a
-// spurious tie would need the ratio to sit within 2^-18 relative of x.5).
+// in fp16 or at least 2^-18 relative away from every fp16 midpoint). The codes round w * (1/s)
+// and settle exact ties with the exact residual w - q*s (see quantize_one), which gives
+// round-half-even of the exact quotient w / s for every pair of fp16 values.
 #include "kernels.cuh"
 
 namespace strata {
@@ -39,9 +39,19 @@ __device__ __forceinline__ void quantize_one(const uint4& v, unsigned half_mask,
   const float s = __half2float(s_h);
   uint32_t packed = 0, lo = 0, hi = 0;  // 4-bit: 8 nibbles; 8-bit: 8 bytes in (lo, hi)
   if (finite && s > 0.0f) {
+    // q = RNE(w / s) without a division per weight: w * (1/s) rounds to the right integer except
+    // at exact ties (for fp16 w and s, w/s is either a half-integer or at least 2^-13 away from
+    // every half-integer, far more than the error of the fp32 product), and the residual
+    // w - q*s, exact in fp32 (q*s has at most 8 + 11 significant bits), finds the ties: there it
+    // is +-s/2 and q moves to the even neighbour.
+    const float inv = 1.0f / s;
+    const float half_s = 0.5f * s;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      float q = rintf(__half2float(h[i]) / s);
+      const float wf = __half2float(h[i]);
+      float q = rintf(wf * inv);
+      const float r = fmaf(-q, s, wf);
+      if (static_cast<int>(q) & 1) q += r == half_s ? 1.0f : (r == -half_s ? -1.0f : 0.0f);
       q = fminf(fmaxf(q, -kQmax - 1.0f), kQmax);
       const uint32_t c = static_cast<uint32_t>(static_cast<int>(q));
       if (kBits == 4)
