@@ -160,10 +160,13 @@ strata_status strata_route_topk(const void* x_bf16, const float* w_router, const
  * GPU that loads the library holds it until the process exits. Requests whose scratch would not
  * fit (strata_route_workspace_size(T, E, k) > STRATA_NOALLOC_SCRATCH_BYTES) return
  * STRATA_ERR_UNSUPPORTED before anything runs; everything else is identical to
- * strata_route_topk (same arguments, outputs and checks). Nothing is allocated or freed, by the
- * library or any routine it calls.
- * Set-up: the first call on a device looks up the array's device address (cudaGetSymbolAddress,
- * with that device current) and keeps it; make that first call before any stream capture.
+ * strata_route_topk (same arguments, outputs and checks, applied in the same order, the size
+ * limit last). Nothing is allocated or freed, by the library or any routine it calls.
+ * Set-up: every call made while `stream` is not capturing looks up the array's device address in
+ * the current context (cudaGetSymbolAddress, with the device current) and keeps it; a call made
+ * while `stream` captures uses the address kept by the last uncaptured call on that device, and
+ * returns STRATA_ERR_UNSUPPORTED if there was none. So make one call on each device (and again
+ * after a device reset or a switch to another context) before capturing it.
  * All calls share the one array: calls that overlap on the GPU (different streams, or several
  * host threads) race and must be serialised by the caller. Each call clears the status header it
  * needs before its kernels run; the rest of the array keeps the previous call's contents.

@@ -24,6 +24,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     for (int j = 0; j < k; ++j) {
       const float g = gates[tk + j];
       const int row = inv[tk + j];
+      // a row outside the routed rows (the grouping skipped a bad expert id, or a timed-out
+      // top-k left the buffer unwritten; both set a device status bit) contributes nothing
+      if (row < 0 || row >= R) continue;
       const float4 v = __ldcg(reinterpret_cast<const float4*>(y + static_cast<int64_t>(row) * H) + c);
       acc.x = fmaf(g, v.x, acc.x); acc.y = fmaf(g, v.y, acc.y);
       acc.z = fmaf(g, v.z, acc.z); acc.w = fmaf(g, v.w, acc.w);

@@ -208,6 +208,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // down: h rows come from gate/up (wait for it before the first activation copy)
       for (int g = gbeg; g < gend; ++g) {
         if (!tc::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
+        // The consumers read the slot through the generic proxy; the TMA boxes below write it
+        // through the async proxy. The empty barrier orders those reads before this point, and
+        // this cross-proxy fence orders them before the new boxes (without it, a warp's loads of
+        // the slot's first rows could return the next stage's bytes, about one forward in 100).
+        tc::fence_proxy_async_smem();
         unsigned char* st = smem + stage * kStageBytes;
         // weights and scales are read once per call: evict them from L2 first (made here, per
         // stage, so that the policy holds no register across the loop)

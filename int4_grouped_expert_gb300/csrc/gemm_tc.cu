@@ -295,6 +295,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = false;
             break;
           }
+          // the dequant warps read the slot through the generic proxy, the TMA below rewrites it
+          // through the async proxy: a cross-proxy fence orders the two
+          tc::fence_proxy_async_smem();
           // a slot past the end of the row (nk not a multiple of SLOT_K) reads zero fill
           uint8_t* dst = ring + cs * C::CODE_BYTES;
           tc::mbar_arrive_expect_tx(cfull + cs, C::CODE_BYTES);

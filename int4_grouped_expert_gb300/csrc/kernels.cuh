@@ -120,6 +120,11 @@ cudaError_t launch_gemm_tc(const TcArgs& a, bool gate_up, const void* b_rows, in
 cudaError_t launch_gather_rows(const void* x, const int* perm, int64_t rows, int64_t H, void* xp,
                                bool f16,
                                cudaStream_t stream);
+// Argument checks shared by the router entry points (strata_api.cu).
+strata_status check_route_args(const void* x_bf16, const void* w_router, int64_t T, int64_t H,
+                               int32_t E, int32_t k, uint32_t flags, const int32_t* ids,
+                               const float* gates, const int32_t* counts, const int32_t* offsets,
+                               const int32_t* perm, const int32_t* inv);
 cudaError_t launch_combine(const float* y, const float* gates, const int* inv, const void* x,
                            int64_t T, int64_t H, int k, int has_shared, int64_t R, int residual,
                            void* out, cudaStream_t stream);

@@ -382,6 +382,25 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
   return STRATA_OK;
 }
 
+// Argument checks of the router entry points (strata_route_topk and its no-workspace variant),
+// in the order both apply them.
+strata_status check_route_args(const void* x_bf16, const void* w_router, int64_t T, int64_t H,
+                               int32_t E, int32_t k, uint32_t flags, const int32_t* ids,
+                               const float* gates, const int32_t* counts, const int32_t* offsets,
+                               const int32_t* perm, const int32_t* inv) {
+  if (T < 0 || T > kMaxTokens || H <= 0 || H > kMaxDim || H % STRATA_GROUP) return STRATA_ERR_SHAPE;
+  if (E < 1 || E > STRATA_MAX_EXPERTS) return STRATA_ERR_UNSUPPORTED;
+  if (k < 1 || k > E || k > STRATA_MAX_TOPK) return STRATA_ERR_INVALID_ARG;
+  if (flags & ~(STRATA_RENORM | STRATA_ROUTER_FP16)) return STRATA_ERR_INVALID_ARG;
+  const bool any_group = counts || offsets || perm || inv;
+  const bool all_group = counts && offsets && perm && inv;
+  if (any_group && !all_group) return STRATA_ERR_INVALID_ARG;
+  if (T > 0 && (!x_bf16 || !w_router || !ids || !gates)) return STRATA_ERR_INVALID_ARG;
+  if ((x_bf16 && !aligned(x_bf16, 16)) || (w_router && !aligned(w_router, 16)))
+    return STRATA_ERR_INVALID_ARG;
+  return STRATA_OK;
+}
+
 }  // namespace strata
 
 using namespace strata;
@@ -441,16 +460,10 @@ strata_status strata_route_topk(const void* x_bf16, const float* w_router, const
                                 int32_t* ids, float* gates, int32_t* counts, int32_t* offsets,
                                 int32_t* perm, int32_t* inv, void* workspace, size_t ws_bytes,
                                 strata_stream stream) {
-  if (T < 0 || T > kMaxTokens || H <= 0 || H > kMaxDim || H % STRATA_GROUP) return STRATA_ERR_SHAPE;
-  if (E < 1 || E > STRATA_MAX_EXPERTS) return STRATA_ERR_UNSUPPORTED;
-  if (k < 1 || k > E || k > STRATA_MAX_TOPK) return STRATA_ERR_INVALID_ARG;
-  if (flags & ~(STRATA_RENORM | STRATA_ROUTER_FP16)) return STRATA_ERR_INVALID_ARG;
-  const bool any_group = counts || offsets || perm || inv;
+  const strata_status chk = check_route_args(x_bf16, w_router, T, H, E, k, flags, ids, gates,
+                                             counts, offsets, perm, inv);
+  if (chk != STRATA_OK) return chk;
   const bool all_group = counts && offsets && perm && inv;
-  if (any_group && !all_group) return STRATA_ERR_INVALID_ARG;
-  if (T > 0 && (!x_bf16 || !w_router || !ids || !gates)) return STRATA_ERR_INVALID_ARG;
-  if ((x_bf16 && !aligned(x_bf16, 16)) || (w_router && !aligned(w_router, 16)))
-    return STRATA_ERR_INVALID_ARG;
   const RouteLayout L = route_layout(T, int64_t(16) * 128, E, k, 0);
   if (!workspace || !aligned(workspace, kAlign)) return STRATA_ERR_WORKSPACE;
   if (ws_bytes < L.total) return STRATA_ERR_WORKSPACE;
