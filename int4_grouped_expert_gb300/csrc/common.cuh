@@ -125,12 +125,14 @@ __device__ __forceinline__ __half f32_to_f16_sat(float x) {
 __device__ __forceinline__ float bf16_lo_f32(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 // One 8-wide chunk of bf16 activations (natural order, words (x0,x1) (x2,x3) (x4,x5) (x6,x7)) as
-// f16 in the pair-interleaved order (x0,x4) (x1,x5) (x2,x6) (x3,x7) the decode GEMM reads.
+// f16 in the order the CTA-staged decode GEMM reads: words (x0,x4) (x2,x6) (x1,x5) (x3,x7), i.e.
+// element i of the chunk at position bitrev3(i). A 16-byte load then gives the two B-operand
+// register pairs of one MMA step in adjacent registers.
 __device__ __forceinline__ uint4 bf16_chunk_to_f16_pairs(uint4 v) {
   uint4 o;
   o.x = f32x2_to_f16x2_sat(bf16_lo_f32(v.x), bf16_lo_f32(v.z));
-  o.y = f32x2_to_f16x2_sat(bf16_hi_f32(v.x), bf16_hi_f32(v.z));
-  o.z = f32x2_to_f16x2_sat(bf16_lo_f32(v.y), bf16_lo_f32(v.w));
+  o.y = f32x2_to_f16x2_sat(bf16_lo_f32(v.y), bf16_lo_f32(v.w));
+  o.z = f32x2_to_f16x2_sat(bf16_hi_f32(v.x), bf16_hi_f32(v.z));
   o.w = f32x2_to_f16x2_sat(bf16_hi_f32(v.y), bf16_hi_f32(v.w));
   return o;
 }

@@ -22,18 +22,20 @@
 // weight rows are the A operand, the (up to 8) tokens the B operand.
 //  * Lane (g = lane/4, t = lane%4) takes 16 bytes = 32 codes of rows g and g+8 per group, and the
 //    contraction order inside the group is permuted so that they feed exactly the lane's A-fragment
-//    slots. The activations are stored with every 8-wide chunk in (0,4,1,5,2,6,3,7) order (x by the
-//    router, h by the gate/up epilogue), which is exactly the B-fragment pairing. A dot product does
-//    not depend on the order of its terms, so no weight re-layout is needed.
-//  * The MMAs take f16 operands: the activations the decode path stages (x by the router or the
-//    row gather, h by the gate/up epilogue) are f16, converted exactly from bf16 (saturated at
-//    +-65504). int4 -> f16 takes one LOP3 per code pair and one shift per 8 codes: each word's
-//    nibbles 0/4 and 2/6 (after >> 8) become f16 1032 + q, nibbles 1/5 and 3/7 become
-//    1152 + 16 q without a shift (f16 has 10 mantissa bits). The low planes multiply the
-//    activation pairs (x0,x4), (x2,x6), the high planes (x1,x5), (x3,x7); correction MMAs with
-//    A = 1032 and A = 1152 (shared by both tiles) remove the offsets, and the group's fp16 scale
-//    is applied in fp32: acc += s * ((P_lo - C_lo) + (P_hi - C_hi) / 16). Weights are never
-//    rounded.
+//    slots. The activations are stored with element i of every 8-wide chunk at position bitrev3(i),
+//    i.e. as words (x0,x4) (x2,x6) (x1,x5) (x3,x7) (x by the router or the row gather, h by the
+//    gate/up epilogue): one 16-byte load gives the B-fragment pairs of both nibble planes of an MMA
+//    step in adjacent registers. A dot product does not depend on the order of its terms, so no
+//    weight re-layout is needed.
+//  * The MMAs take f16 operands: the activations the decode path stages are f16, converted exactly
+//    from bf16 (saturated at +-65504). int4 -> f16 takes one LOP3 per code pair and one shift per
+//    8 codes: each word's nibbles 0/4 and 2/6 (after >> 8) become f16 1032 + q (the nibble in the
+//    low mantissa bits of 1024), nibbles 1/5 and 3/7 become 72 + q without a shift (the nibble in
+//    mantissa bits 4-7 of 64, where they weigh 1). The low planes multiply the activation pairs
+//    (x0,x4), (x2,x6), the high planes (x1,x5), (x3,x7), both into one accumulator per tile; one
+//    correction accumulator (MMAs with A = 1032 and A = 72, shared by both tiles) removes the
+//    offsets, and the group's fp16 scale is applied in fp32: acc += s * (P - C). Each group's
+//    first MMAs start from zero, so nothing is cleared per group. Weights are never rounded.
 //  * Small batches split the contraction; the last split to arrive (device counter per warp tile)
 //    sums the partials in split order and applies the epilogue, so results stay deterministic.
 // Gate/up writes h = silu(u) * v (bf16); down writes y (fp32) for the combine.
@@ -77,10 +79,10 @@ static_assert(CtaLayout<true>::kHdrOff + static_cast<int>(sizeof(StageHdr)) <=
 static_assert(kCtasPerSm * (CtaLayout<true>::kSmemBytes + 1024) <= 228 * 1024,
               "two CTAs per SM");
 
-// int4 -> f16 in one LOP3 per code pair, d = (v & mask) ^ c: the masked nibbles land in the low
-// mantissa of f16 1024 with their sign bit flipped. Nibbles at bits 0-3 / 16-19 give 1032 + q;
-// nibbles at bits 4-7 / 20-23 (f16 has 10 mantissa bits, so no shift is needed) give
-// 1152 + 16 q. Both are exact.
+// int4 -> f16 in one LOP3 per code pair, d = (v & mask) ^ c: the masked nibbles land in the
+// mantissa with their sign bit flipped. Nibbles at bits 0-3 / 16-19 go into the low mantissa bits
+// of f16 1024 and give 1032 + q; nibbles at bits 4-7 / 20-23 go into mantissa bits 4-7 of f16 64,
+// where one step is worth 1, and give 72 + q. Both are exact.
 __device__ __forceinline__ uint32_t nib_lo_f16(uint32_t v) {
   uint32_t d;
   asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(v), "n"(0x000F000F), "n"(0x64086408));
@@ -88,7 +90,7 @@ __device__ __forceinline__ uint32_t nib_lo_f16(uint32_t v) {
 }
 __device__ __forceinline__ uint32_t nib_hi_f16(uint32_t v) {
   uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(v), "n"(0x00F000F0), "n"(0x64806480));
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(v), "n"(0x00F000F0), "n"(0x54805480));
   return d;
 }
 
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   griddep_wait();  // outputs and split-K scratch follow the previous kernel
   const int gq = lane >> 2, t4 = lane & 3;
   const uint32_t a1032[4] = {0x64086408u, 0x64086408u, 0x64086408u, 0x64086408u};  // f16 1032
-  const uint32_t a1152[4] = {0x64806480u, 0x64806480u, 0x64806480u, 0x64806480u};  // f16 1152
+  const uint32_t a72[4] = {0x54805480u, 0x54805480u, 0x54805480u, 0x54805480u};    // f16 72
   const int mtile = kGateUp ? 16 : 32;
   int stage = 0;
   uint32_t phase = 0;
@@ -372,39 +374,43 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     auto h2f = [](uint32_t v, int sh) {
       return __half2float(__ushort_as_half(static_cast<unsigned short>(v >> sh)));
     };
-    // low / high nibble planes of both tiles and their shared corrections
-    float plo0[4] = {}, phi0[4] = {}, plo1[4] = {}, phi1[4] = {}, clo[4] = {}, chi[4] = {};
-    // acc += s * partial for the rows' scales, then a fresh partial
+    // one group's sums: tile 0, tile 1, and the offsets both carry (weights 1032 + q / 72 + q)
+    float p0[4], p1[4], cr[4];
+    const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+    // acc += s * (P - C) for the rows' scales
     auto flush = [&](float sa0, float sb0, float sa1, float sb1) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const float corr = fmaf(0.0625f, chi[c], clo[c]);
-        const float q0 = fmaf(0.0625f, phi0[c], plo0[c]) - corr;
-        const float q1 = fmaf(0.0625f, phi1[c], plo1[c]) - corr;
-        acc0[c] = fmaf(c < 2 ? sa0 : sb0, q0, acc0[c]);
-        acc1[c] = fmaf(c < 2 ? sa1 : sb1, q1, acc1[c]);
-        plo0[c] = phi0[c] = plo1[c] = phi1[c] = clo[c] = chi[c] = 0.f;
+        acc0[c] = fmaf(c < 2 ? sa0 : sb0, p0[c] - cr[c], acc0[c]);
+        acc1[c] = fmaf(c < 2 ? sa1 : sb1, p1[c] - cr[c], acc1[c]);
       }
     };
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      // activations are stored pair-interleaved: X[4j+m] = {x[8j+m], x[8j+m+4]}
-      const uint32_t x04 = X[4 * j], x15 = X[4 * j + 1], x26 = X[4 * j + 2], x37 = X[4 * j + 3];
-      mma_f16_16816(clo, a1032, x04, x26, clo);
-      mma_f16_16816(chi, a1152, x15, x37, chi);
+      // X[4j..4j+3] = (x0,x4) (x2,x6) | (x1,x5) (x3,x7) of chunk j: low-plane pair, high-plane pair
+      const uint32_t xl0 = X[4 * j], xl1 = X[4 * j + 1], xh0 = X[4 * j + 2], xh1 = X[4 * j + 3];
+      // a group's first step starts its sums from zero (64-wide groups: steps 0 and 2)
+      const bool first = kG == 64 ? (j == 0 || j == 2) : (j == 0);
+      // (first is a constant once the loop is unrolled)
+      auto mma_acc = [&](float (&d)[4], const uint32_t (&fa)[4], uint32_t b0, uint32_t b1) {
+        if (first) mma_f16_16816(d, fa, b0, b1, zero);
+        else mma_f16_16816(d, fa, b0, b1, d);
+      };
+      mma_acc(cr, a1032, xl0, xl1);
+      mma_f16_16816(cr, a72, xh0, xh1, cr);
       {
         const uint32_t vl = w0l[j], vh = w0h[j], vl8 = vl >> 8, vh8 = vh >> 8;
         const uint32_t flo[4] = {nib_lo_f16(vl), nib_lo_f16(vh), nib_lo_f16(vl8), nib_lo_f16(vh8)};
         const uint32_t fhi[4] = {nib_hi_f16(vl), nib_hi_f16(vh), nib_hi_f16(vl8), nib_hi_f16(vh8)};
-        mma_f16_16816(plo0, flo, x04, x26, plo0);
-        mma_f16_16816(phi0, fhi, x15, x37, phi0);
+        mma_acc(p0, flo, xl0, xl1);
+        mma_f16_16816(p0, fhi, xh0, xh1, p0);
       }
       {
         const uint32_t vl = w1l[j], vh = w1h[j], vl8 = vl >> 8, vh8 = vh >> 8;
         const uint32_t flo[4] = {nib_lo_f16(vl), nib_lo_f16(vh), nib_lo_f16(vl8), nib_lo_f16(vh8)};
         const uint32_t fhi[4] = {nib_hi_f16(vl), nib_hi_f16(vh), nib_hi_f16(vl8), nib_hi_f16(vh8)};
-        mma_f16_16816(plo1, flo, x04, x26, plo1);
-        mma_f16_16816(phi1, fhi, x15, x37, phi1);
+        mma_acc(p1, flo, xl0, xl1);
+        mma_f16_16816(p1, fhi, xh0, xh1, p1);
       }
       if (kG == 64 && (j == 1 || j == 3)) {
         // 64-wide groups: j = 0, 1 are the block's first group (low half of the scale pair),
@@ -460,8 +466,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (col >= hd.nvalid) continue;
         const int64_t orow = hd.rbase + col;
         if (kGateUp) {
-          // h columns are stored pair-interleaved inside every 8 (the down GEMM's B order), as f16
-          const int n0 = mt * 16 + (gq < 4 ? 2 * gq : 2 * gq - 7);
+          // h columns: element i of every 8 at position bitrev3(i) (the down GEMM's B order), as f16
+          const int n0 = mt * 16 + (((gq & 1) << 2) | (gq & 2) | (gq >> 2));
           __half* hrow = static_cast<__half*>(a.out) + orow * a.N;
           hrow[n0] = f32_to_f16_sat(silu_f(acc0[c]) * acc1[c]);
           hrow[n0 + 8] = f32_to_f16_sat(silu_f(acc0[c + 2]) * acc1[c + 2]);
