@@ -128,18 +128,47 @@ __device__ __forceinline__ float bf16_hi_f32(uint32_t v) { return __uint_as_floa
 // f16 in the order the CTA-staged decode GEMM reads: words (x0,x4) (x2,x6) (x1,x5) (x3,x7), i.e.
 // element i of the chunk at position bitrev3(i). A 16-byte load then gives the two B-operand
 // register pairs of one MMA step in adjacent registers.
-__device__ __forceinline__ uint4 bf16_chunk_to_f16_pairs(uint4 v) {
+// s: an exact power of two that the values are multiplied by first (see range_exp).
+__device__ __forceinline__ uint4 bf16_chunk_to_f16_pairs(uint4 v, float s = 1.0f) {
   uint4 o;
-  o.x = f32x2_to_f16x2_sat(bf16_lo_f32(v.x), bf16_lo_f32(v.z));
-  o.y = f32x2_to_f16x2_sat(bf16_lo_f32(v.y), bf16_lo_f32(v.w));
-  o.z = f32x2_to_f16x2_sat(bf16_hi_f32(v.x), bf16_hi_f32(v.z));
-  o.w = f32x2_to_f16x2_sat(bf16_hi_f32(v.y), bf16_hi_f32(v.w));
+  o.x = f32x2_to_f16x2_sat(bf16_lo_f32(v.x) * s, bf16_lo_f32(v.z) * s);
+  o.y = f32x2_to_f16x2_sat(bf16_lo_f32(v.y) * s, bf16_lo_f32(v.w) * s);
+  o.z = f32x2_to_f16x2_sat(bf16_hi_f32(v.x) * s, bf16_hi_f32(v.z) * s);
+  o.w = f32x2_to_f16x2_sat(bf16_hi_f32(v.y) * s, bf16_hi_f32(v.w) * s);
   return o;
+}
+
+// Range of the f16 GEMM operands. A row of activations (x, or h) whose magnitude would leave the
+// f16 range is stored as act * 2^-e (an exact power of two: no rounding is added except to
+// values that become f16 subnormals, far below the row's largest entries), and the GEMM that reads
+// it multiplies its fp32 result by 2^e. e = 0 for every row whose entries stay below 16, so
+// ordinary inputs are untouched; rows of a residual stream that has grown without normalisation
+// are the ones that need it.
+//
+// 2^n as a float, exactly, for -126 <= n <= 127.
+__device__ __forceinline__ float exp2i(int n) { return __int_as_float((n + 127) << 23); }
+// Largest magnitude among 8 bf16 values as an integer key (bf16 bits without the sign: their
+// integer order is the order of the magnitudes).
+__device__ __forceinline__ uint32_t bf16x8_mag(uint4 v) {
+  const uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                              __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+  return max(m & 0xFFFFu, m >> 16);
+}
+// The row exponent for a largest bf16 magnitude (key as above): the smallest e >= 0 with
+// max * 2^-e < 16, capped at 60 (so that 2e stays a float exponent).
+__device__ __forceinline__ int range_exp(uint32_t mag_key) {
+  const int e = static_cast<int>(mag_key >> 7) - 127;  // max in [2^e, 2^(e+1))
+  return e < 4 ? 0 : min(e - 3, 60);
 }
 
 // silu(u) = u * sigmoid(u) with the fast exp and divide intrinsics (a few ulp of fp32: the result
 // is rounded to bf16 right after). Large negative u: exp overflows to inf and the quotient is 0.
 __device__ __forceinline__ float silu_f(float u) { return __fdividef(u, 1.0f + __expf(-u)); }
+// silu(u_s * up) / up for a power of two up: the SiLU of a value held as u_s = u / up, returned
+// at the same scale (u_s * sigmoid(u)); equal to silu_f(u_s) when up = 1.
+__device__ __forceinline__ float silu_scaled(float u_s, float up) {
+  return __fdividef(u_s, 1.0f + __expf(-u_s * up));
+}
 
 // Programmatic dependent launch: a kernel launched with the PDL attribute may start while its
 // predecessor in the stream still runs; griddep_wait() blocks until the predecessor grid has

@@ -465,19 +465,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int col = 2 * t4 + c;
         if (col >= hd.nvalid) continue;
         const int64_t orow = hd.rbase + col;
+        // the activation row was stored times 2^-e: the sums are at that scale
+        const int e = a.aexp ? a.aexp[a.perm ? a.perm[orow] : orow] : 0;
         if (kGateUp) {
-          // h columns: element i of every 8 at position bitrev3(i) (the down GEMM's B order), as f16
+          // h columns: element i of every 8 at position bitrev3(i) (the down GEMM's B order), as
+          // f16, stored times 2^-2e (u and v are at scale 2^-e each)
           const int n0 = mt * 16 + (((gq & 1) << 2) | (gq & 2) | (gq >> 2));
           __half* hrow = static_cast<__half*>(a.out) + orow * a.N;
-          hrow[n0] = f32_to_f16_sat(silu_f(acc0[c]) * acc1[c]);
-          hrow[n0 + 8] = f32_to_f16_sat(silu_f(acc0[c + 2]) * acc1[c + 2]);
+          const float up = exp2i(e);
+          hrow[n0] = f32_to_f16_sat(silu_scaled(acc0[c], up) * acc1[c]);
+          hrow[n0 + 8] = f32_to_f16_sat(silu_scaled(acc0[c + 2], up) * acc1[c + 2]);
+          if (a.hexp && mt == 0 && gq == 0) a.hexp[orow] = 2 * e;
         } else {
           const int n0 = mt * 32 + gq;
+          const float up = exp2i(e);
           float* y = static_cast<float*>(a.out) + orow * a.N;
-          y[n0] = acc0[c];
-          y[n0 + 8] = acc0[c + 2];
-          y[n0 + 16] = acc1[c];
-          y[n0 + 24] = acc1[c + 2];
+          y[n0] = acc0[c] * up;
+          y[n0 + 8] = acc0[c + 2] * up;
+          y[n0 + 16] = acc1[c] * up;
+          y[n0 + 24] = acc1[c + 2] * up;
         }
       }
     }

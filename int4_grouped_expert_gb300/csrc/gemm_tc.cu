@@ -5,11 +5,11 @@
 // 128 codes share one fp16 scale).
 //
 // Tile = (segment, 128 weight rows, up to kN token rows), contraction in 64-wide stages.
-//   warp 0       TMA producer: the stage's token rows (bf16, 128-byte swizzle) -> shared memory
+//   warp 0       TMA producer: the stage's token rows (f16, 128-byte swizzle) -> shared memory
 //   warp 1       MMA issuer: one thread issues tcgen05.mma (M=128, N=rows, K=16) into TMEM
 //   warp 2       owns the TMEM allocation
 //   warp 3       small tiles only: TMA producer of the int4 code tiles (a deep ring of stages)
-//   warps 4..11  dequant producers: int4 codes -> bf16(q*s) written in the same swizzled K-major
+//   warps 4..11  dequant producers: int4 codes -> f16(q*s) written in the same swizzled K-major
 //                layout (the A operand)
 //   warps 12..15 epilogue: TMEM -> registers -> global
 // Two tile widths: kN = 256 token rows for segments with many rows (the dequant warps load their
@@ -20,14 +20,16 @@
 // D[weight row][token] accumulates in TMEM: gate/up in one 512-column buffer (gate, then up);
 // down in two 256-column buffers, so its MMAs for the next tile run while the epilogue drains
 // this one. While the epilogue runs, the dequant warps already fill the next tile's stages.
-// Gate/up writes h = silu(gate) * up as bf16; down writes y in fp32 for the combine.
+// Gate/up writes h = silu(gate) * up as f16; down writes y in fp32 for the combine.
 //
 // Contraction order: inside every 8-wide chunk the K order is (0,4,1,5,2,6,3,7). That is the
 // order in which one LOP3 per pair unpacks the codes, so the activations are stored in it too (by
 // the gather kernel for x, by the gate/up epilogue for h); a dot product is order-independent.
 //
-// Scale: w = bf16(q * s) computed as fma(q, s_hi, q * s_lo) in bf16 with s = s_hi + s_lo, so the
-// product is rounded once (to within 2^-17 relative).
+// Operands are f16 (tcgen05.mma kind::f16 with f16 A and B): the weight is w = f16(q * s), the
+// exact code times the fp16 scale rounded once (2^-11 relative); x (gathered by the row kernel)
+// and h (written by the gate/up epilogue) are f16, exact from bf16 within the f16 range and
+// saturated at +-65504 outside it.
 //
 // Every mbarrier wait is bounded in time; on time-out the kernel sets STRATA_DEV_TIMEOUT, every
 // role leaves its loop, in-flight copies and MMAs are drained (bounded) and TMEM is freed.
@@ -39,7 +41,7 @@
 namespace strata {
 
 constexpr int kTcBM = 128;       // weight rows per tile (MMA M)
-constexpr int kTcBK = 64;        // contraction per stage: one 128-byte swizzle row of bf16
+constexpr int kTcBK = 64;        // contraction per stage: one 128-byte swizzle row of f16
 constexpr int kTcThreads = 512;  // 16 warps
 
 #ifndef STRATA_TC_SMALL_STAGES_GU
@@ -101,27 +103,20 @@ __device__ __forceinline__ bool tc_decode(const TcArgs& a, int item, int nseg, i
   return true;
 }
 
-// bf16x2 {q_i, q_{i+4}} of an 8-code word (two's complement nibbles), exact
-__device__ __forceinline__ uint32_t codes_pair_bf16(uint32_t w, int i) {
+// f16x2 {q_i, q_{i+4}} of an 8-code word (two's complement nibbles), exact: the nibble with its
+// sign bit flipped goes into the low mantissa of f16 1024 (1032 + q), then 1032 is subtracted
+__device__ __forceinline__ uint32_t codes_pair_f16(uint32_t w, int i) {
   const uint32_t v = w >> (4 * i);
   uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(v), "n"(0x000F000F), "n"(0x43084308));
-  __nv_bfloat162 r = *reinterpret_cast<__nv_bfloat162*>(&d);
-  r = __hsub2(r, __floats2bfloat162_rn(136.0f, 136.0f));
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(v), "n"(0x000F000F), "n"(0x64086408));
+  __half2 r = *reinterpret_cast<__half2*>(&d);
+  r = __hsub2(r, __floats2half2_rn(1032.0f, 1032.0f));
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-#ifndef STRATA_TC_SPLIT_SCALE
-#define STRATA_TC_SPLIT_SCALE 1  // 1: q*s rounded once (two-term scale); 0: q*bf16(s), two roundings
-#endif
-__device__ __forceinline__ uint32_t scale_pair(uint32_t q, __nv_bfloat162 hi, __nv_bfloat162 lo) {
-  const __nv_bfloat162 qq = *reinterpret_cast<__nv_bfloat162*>(&q);
-#if STRATA_TC_SPLIT_SCALE
-  const __nv_bfloat162 r = __hfma2(qq, hi, __hmul2(qq, lo));
-#else
-  const __nv_bfloat162 r = __hmul2(qq, hi);
-  (void)lo;
-#endif
+// q * s for a pair of exact codes and the fp16 scale: one f16 rounding
+__device__ __forceinline__ uint32_t scale_pair(uint32_t q, __half2 s) {
+  const __half2 r = __hmul2(*reinterpret_cast<__half2*>(&q), s);
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
@@ -135,10 +130,6 @@ __device__ __forceinline__ void codes8_scaled(uint32_t w, float s, float* v) {
     const float f = __uint_as_float(prmt(u, 0x4B000000u, 0x7540u + i)) - 8388736.0f;
     v[i] = f * s;
   }
-}
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 // Position of natural index i (0..7) inside a chunk stored in (0,4,1,5,2,6,3,7) order.
@@ -238,7 +229,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++tcount) {
         TcTile t;
         tc_decode<kN>(a, item, nseg, mtiles, t);
-        const uint32_t idesc = tc::idesc_bf16(kTcBM, t.nmma);
+        const uint32_t idesc = tc::idesc_f16(kTcBM, t.nmma);
         const int buf = tcount % C::NBUF;
         const uint32_t dtm = tmem + buf * C::ACC_COLS;
         // the epilogue has drained this buffer (the tile NBUF back)
@@ -264,8 +255,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int kk = 0; kk < kTcBK / 16; ++kk) {
             const uint32_t acc = (kb | kk) ? 1u : 0u;
             // +32 bytes per 16-wide K step inside the swizzle row (address field is in 16 B)
-            tc::mma_bf16_ss(dtm, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-            if (kGateUp) tc::mma_bf16_ss(dtm + kN, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+            tc::mma_f16_ss(dtm, da0 + 2 * kk, db + 2 * kk, idesc, acc);
+            if (kGateUp) tc::mma_f16_ss(dtm + kN, da1 + 2 * kk, db + 2 * kk, idesc, acc);
           }
           tc::mma_commit(empty + s);
         }
@@ -361,12 +352,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (kb >= nk) break;
           const int s = it % ST;
           const uint32_t ph = (it / ST) & 1;
-          // scale of this stage's group as a bf16 pair split: s = s_hi + s_lo
-          const float sf = __half2float(__ushort_as_half(sc[u]));
-          const __nv_bfloat16 hb = __float2bfloat16_rn(sf);
-          const __nv_bfloat16 lb = __float2bfloat16_rn(sf - __bfloat162float(hb));
-          const __nv_bfloat162 s_hi = __halves2bfloat162(hb, hb);
-          const __nv_bfloat162 s_lo = __halves2bfloat162(lb, lb);
+          // scale of this stage's group (fp16), and as fp32 for the exact 8-bit products
+          const __half sh = __ushort_as_half(sc[u]);
+          const __half2 s2 = __halves2half2(sh, sh);
+          const float sf = __half2float(sh);
           uint4 x0 = cA[u], x1 = cB[u];
           uint4 x8[4];  // 8-bit codes of the stage: gate/up 64 bytes of the row, down 32 of its half
           if (C::RING) {
@@ -401,8 +390,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!tc::mbar_wait(empty + s, ph ^ 1, abort_flag, a.status)) { ok = false; break; }
           uint8_t* dst = A_of(s, mat) + soff;
           if (kBits == 8) {
-            // 8 codes (bytes m0..m7, natural order) per chunk -> bf16 pairs (m0,m4) (m1,m5)
-            // (m2,m6) (m3,m7); q * s is exact in fp32 and rounded once to bf16
+            // 8 codes (bytes m0..m7, natural order) per chunk -> f16 pairs (m0,m4) (m1,m5)
+            // (m2,m6) (m3,m7); q * s is exact in fp32 and rounded once to f16
             const uint32_t wds8[16] = {x8[0].x, x8[0].y, x8[0].z, x8[0].w, x8[1].x, x8[1].y,
                                        x8[1].z, x8[1].w, x8[2].x, x8[2].y, x8[2].z, x8[2].w,
                                        x8[3].x, x8[3].y, x8[3].z, x8[3].w};
@@ -412,10 +401,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               codes8_scaled(wds8[2 * j], sf, v);
               codes8_scaled(wds8[2 * j + 1], sf, v + 4);
               uint4 o;
-              o.x = pack_bf16x2(v[0], v[4]);
-              o.y = pack_bf16x2(v[1], v[5]);
-              o.z = pack_bf16x2(v[2], v[6]);
-              o.w = pack_bf16x2(v[3], v[7]);
+              o.x = f32x2_to_f16x2_sat(v[0], v[4]);
+              o.y = f32x2_to_f16x2_sat(v[1], v[5]);
+              o.z = f32x2_to_f16x2_sat(v[2], v[6]);
+              o.w = f32x2_to_f16x2_sat(v[3], v[7]);
               const int chunk = kGateUp ? j : (half * 4 + j);
               *reinterpret_cast<uint4*>(dst + ((chunk ^ (r & 7)) << 4)) = o;
             }
@@ -425,10 +414,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int j = 0; j < (kGateUp ? 8 : 4); ++j) {
             const uint32_t w = wds[j];
             uint4 o;
-            o.x = scale_pair(codes_pair_bf16(w, 0), s_hi, s_lo);
-            o.y = scale_pair(codes_pair_bf16(w, 1), s_hi, s_lo);
-            o.z = scale_pair(codes_pair_bf16(w, 2), s_hi, s_lo);
-            o.w = scale_pair(codes_pair_bf16(w, 3), s_hi, s_lo);
+            o.x = scale_pair(codes_pair_f16(w, 0), s2);
+            o.y = scale_pair(codes_pair_f16(w, 1), s2);
+            o.z = scale_pair(codes_pair_f16(w, 2), s2);
+            o.w = scale_pair(codes_pair_f16(w, 3), s2);
             const int chunk = kGateUp ? j : (half * 4 + j);
             *reinterpret_cast<uint4*>(dst + ((chunk ^ (r & 7)) << 4)) = o;
           }
@@ -461,27 +450,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int c = 0; c < t.nmma; c += 32) {
         uint32_t g[32];
         tc::tmem_ld32(lane_addr + c, g);
+        // range exponents of this chunk's token rows (the B rows were stored times 2^-e)
+        const int n_here = min(32, t.nvalid - c);
+        const int my_e = (a.aexp && lane < n_here) ? a.aexp[t.row0 + c + lane] : 0;
         if (kGateUp) {
           uint32_t u[32];
           tc::tmem_ld32(lane_addr + kN + c, u);
           tc::tmem_ld_wait();
-          __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.out);
+          __half* h = static_cast<__half*>(a.out);
           const int col = (irow & ~7) | pair_pos(irow & 7);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int n = c + j;
+            const int e = __shfl_sync(0xffffffffu, my_e, j);
             if (n < t.nvalid) {
+              // h stored times 2^-2e (gate and up are at scale 2^-e each)
               const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
-              h[static_cast<int64_t>(t.row0 + n) * a.Nw + col] = __float2bfloat16_rn(silu_f(gv) * uv);
+              h[static_cast<int64_t>(t.row0 + n) * a.Nw + col] =
+                  f32_to_f16_sat(silu_scaled(gv, exp2i(e)) * uv);
             }
           }
+          if (a.hexp && t.mt == 0 && q4 == 0 && lane < n_here) a.hexp[t.row0 + c + lane] = 2 * my_e;
         } else {
           tc::tmem_ld_wait();
           float* y = static_cast<float*>(a.out);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int n = c + j;
-            if (n < t.nvalid) y[static_cast<int64_t>(t.row0 + n) * a.Nw + irow] = __uint_as_float(g[j]);
+            const float up = exp2i(__shfl_sync(0xffffffffu, my_e, j));
+            if (n < t.nvalid)
+              y[static_cast<int64_t>(t.row0 + n) * a.Nw + irow] = __uint_as_float(g[j]) * up;
           }
         }
       }
@@ -500,21 +498,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ----------------------------------------------------------------------------- gather
 
-// xp[r] = x[perm[r]] with every 8-wide chunk stored in (0,4,1,5,2,6,3,7) order: bf16 for the
-// tensor-core and per-warp GEMMs, f16 (exact, saturated at +-65504) for the CTA-staged one.
-template <bool kF16>
+// xp[r] = x[perm[r]], each 8-wide chunk reordered for the GEMM that reads it (kMode):
+//   0: bf16 in (0,4,1,5,2,6,3,7) order (the per-warp decode GEMM)
+//   1: f16 with element i at position bitrev3(i) (the CTA-staged decode GEMM)
+//   2: f16 in (0,4,1,5,2,6,3,7) order (the tensor-core GEMM)
+// f16 is exact from bf16 within its range and saturated at +-65504 outside it.
+template <int kMode>
 __global__ void __launch_bounds__(128) gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
                                                           const int* __restrict__ perm, int H,
-                                                          uint16_t* __restrict__ xp) {
+                                                          uint16_t* __restrict__ xp,
+                                                          int* __restrict__ rexp) {
   const int row = blockIdx.x;
   const int tok = perm[row];
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(tok) * H);
   uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<int64_t>(row) * H);
+  float s = 1.0f;
+  if (kMode != 0) {
+    // the row's range exponent (f16 copies): its largest magnitude, then 2^-e
+    __shared__ uint32_t wmag[4];
+    uint32_t m = 0;
+    for (int c = threadIdx.x; c < H / 8; c += blockDim.x) m = max(m, bf16x8_mag(__ldg(src + c)));
+    m = __reduce_max_sync(0xffffffffu, m);
+    if ((threadIdx.x & 31) == 0) wmag[threadIdx.x >> 5] = m;
+    __syncthreads();
+    const int e = range_exp(max(max(wmag[0], wmag[1]), max(wmag[2], wmag[3])));
+    if (threadIdx.x == 0 && rexp) rexp[row] = e;
+    s = exp2i(-e);
+  }
   for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
     const uint4 v = __ldg(src + c);
     uint4 o;
-    if (kF16) {
-      o = bf16_chunk_to_f16_pairs(v);
+    if (kMode == 1) {
+      o = bf16_chunk_to_f16_pairs(v, s);
+    } else if (kMode == 2) {
+      o.x = f32x2_to_f16x2_sat(bf16_lo_f32(v.x) * s, bf16_lo_f32(v.z) * s);  // x0, x4
+      o.y = f32x2_to_f16x2_sat(bf16_hi_f32(v.x) * s, bf16_hi_f32(v.z) * s);  // x1, x5
+      o.z = f32x2_to_f16x2_sat(bf16_lo_f32(v.y) * s, bf16_lo_f32(v.w) * s);  // x2, x6
+      o.w = f32x2_to_f16x2_sat(bf16_hi_f32(v.y) * s, bf16_hi_f32(v.w) * s);  // x3, x7
     } else {
       o.x = prmt(v.x, v.z, 0x5410);  // x0, x4
       o.y = prmt(v.x, v.z, 0x7632);  // x1, x5
@@ -526,15 +546,18 @@ __global__ void __launch_bounds__(128) gather_rows_kernel(const __nv_bfloat16* _
 }
 
 cudaError_t launch_gather_rows(const void* x, const int* perm, int64_t rows, int64_t H, void* xp,
-                               bool f16, cudaStream_t stream) {
+                               int mode, int* rexp, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   const unsigned g = static_cast<unsigned>(rows);
   const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(x);
   uint16_t* xd = static_cast<uint16_t*>(xp);
-  if (f16)
-    gather_rows_kernel<true><<<g, 128, 0, stream>>>(xs, perm, static_cast<int>(H), xd);
+  const int h = static_cast<int>(H);
+  if (mode == 1)
+    gather_rows_kernel<1><<<g, 128, 0, stream>>>(xs, perm, h, xd, rexp);
+  else if (mode == 2)
+    gather_rows_kernel<2><<<g, 128, 0, stream>>>(xs, perm, h, xd, rexp);
   else
-    gather_rows_kernel<false><<<g, 128, 0, stream>>>(xs, perm, static_cast<int>(H), xd);
+    gather_rows_kernel<0><<<g, 128, 0, stream>>>(xs, perm, h, xd, nullptr);
   return cudaGetLastError();
 }
 
@@ -554,7 +577,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   return fn;
 }
 
-// Row-major bf16 [rows, cols]: boxes of box_rows rows x 64 columns, 128-byte swizzle, zero fill.
+// Row-major f16 [rows, cols]: boxes of box_rows rows x 64 columns, 128-byte swizzle, zero fill.
 static bool make_row_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
                           int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
@@ -563,7 +586,7 @@ static bool make_row_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
   cuuint32_t box[2] = {kTcBK, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -39,7 +39,8 @@ struct GemmArgs {
   const __nv_bfloat16* act;  // gate/up: x [T, K]; down: h [rows, K]; pair-interleaved chunks,
                              // f16 for the CTA-staged kernel (the type only sets the stride)
   const int* perm;           // token (activation row) of each GEMM row, or null: row = activation row
-  void* out;                 // gate/up: h bf16 [rows, N]; down: y fp32 [rows, N]
+  void* out;                 // gate/up: h [rows, N] (f16 from the CTA-staged kernel, bf16 from the
+                             // per-warp one); down: y fp32 [rows, N]
   int K;                     // contraction length (H for gate/up, I for down)
   int N;                     // weight rows per expert (I for gate/up, H for down)
   WsHeader* hdr;
@@ -49,6 +50,11 @@ struct GemmArgs {
   const int* seg_item;       // exclusive prefix of work items per segment, [nseg + 1]
   const int4* chunk_list;    // {expert, first row, rows, 0} per 8-row chunk
   int ksplit;                // contraction splits per tile (gate/up only)
+  // f16 operands (CTA-staged kernel): activation row r (perm[r] when perm is set) is stored as
+  // act * 2^-aexp[.] and the result is multiplied back; gate/up stores h row r as h * 2^-2a and
+  // writes 2a to hexp[r] (each may be null: exponent 0)
+  const int* aexp;
+  int* hexp;
   int group;                 // scale group size: 64, 128 or 256 (CTA-staged kernel; others 128)
   float* split_part;         // [tiles * ksplit * 256] partial sums of split tiles
   int* split_cnt;            // [tiles] arrival counters (zero on entry)
@@ -60,10 +66,12 @@ struct TcArgs {
   const __half* scales0;
   const uint8_t* codes1;  // up codes (gate/up)
   const __half* scales1;
-  void* out;              // gate/up: h bf16 [rows, Nw] (pair-interleaved columns); down: y fp32
+  void* out;              // gate/up: h f16 [rows, Nw] (pair-interleaved columns); down: y fp32
   int K, Nw;              // contraction; weight rows per expert
   int group;              // scale group size: 64, 128 or 256
   int bits;               // code width: 4 (codes [.., K/2]) or 8 (codes [.., K])
+  const int* aexp;        // range exponent of each B row (null: 0), as GemmArgs::aexp
+  int* hexp;              // gate/up: 2a of each h row (null: not written)
   WsHeader* hdr;
   const int* seg_expert;
   const int* seg_row0;
@@ -84,6 +92,7 @@ struct RouteSmallArgs {
   int epc;                 // experts per CTA (each split over 8 / epc warps along H)
   void* x_perm;            // [T, H]: x with every 8-wide chunk in (0,4,1,5,2,6,3,7) order, or null
   bool x_f16;              // x_perm as f16 (CTA-staged GEMM) instead of bf16 (per-warp GEMM)
+  int* xexp;               // x_f16: [T] range exponent of each token's row of x_perm (range_exp)
   float* logits;           // [T][E] scratch
   int* ids;
   float* gates;
@@ -116,10 +125,12 @@ constexpr int kTcRowsSmall = 64;  // the same for batches with few rows per expe
 // (routed + shared); tile_rows: kTcRows or kTcRowsSmall (the grouping's chunk size)
 cudaError_t launch_gemm_tc(const TcArgs& a, bool gate_up, const void* b_rows, int64_t rows,
                            int64_t experts, int tile_rows, int num_sms, cudaStream_t stream);
-// xp[r] = x[perm[r]], pair-interleaved, as f16 (f16 = true: the CTA-staged GEMM) or bf16
+// xp[r] = x[perm[r]], each 8-wide chunk in the order (and type) its GEMM reads: mode 0 bf16 for
+// the per-warp decode GEMM, 1 f16 for the CTA-staged decode GEMM, 2 f16 for the tensor-core GEMM
+constexpr int kGatherWarp = 0, kGatherCta = 1, kGatherTc = 2;
+// rexp: f16 modes, the range exponent of each gathered row (see range_exp), or null
 cudaError_t launch_gather_rows(const void* x, const int* perm, int64_t rows, int64_t H, void* xp,
-                               bool f16,
-                               cudaStream_t stream);
+                               int mode, int* rexp, cudaStream_t stream);
 // Argument checks shared by the router entry points (strata_api.cu).
 strata_status check_route_args(const void* x_bf16, const void* w_router, int64_t T, int64_t H,
                                int32_t E, int32_t k, uint32_t flags, const int32_t* ids,

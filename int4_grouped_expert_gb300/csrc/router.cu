@@ -203,8 +203,13 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   const uint4* xv = reinterpret_cast<const uint4*>(a.x);
   const uint64_t pol = l2_evict_first_policy();  // the router rows are read once per call
   constexpr int TB = 8;  // tokens per pass: every load of a pass is in flight together
+  // the warps of expert slot 0 read all of x: they also find each token's largest magnitude,
+  // from which the f16 copy of x gets its range exponent
+  __shared__ uint32_t xmag[kRsWarps][kRouteSmallMaxT];
+  __shared__ int xexp_s[kRouteSmallMaxT];
   for (int t0 = 0; t0 < T; t0 += TB) {
     float acc[TB] = {};
+    uint32_t mag[TB] = {};
     if (e < E) {
       for (int v0 = vb + lane; v0 < ve; v0 += 128) {
         float4 w[4][2];
@@ -241,6 +246,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
 #pragma unroll
           for (int tt = 0; tt < TB; ++tt) {
             if (t0 + tt >= T) continue;
+            if (slot == 0) mag[tt] = max(mag[tt], bf16x8_mag(xr[tt][i]));
             const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&xr[tt][i]);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -258,9 +264,20 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
       if (lane == 0 && t0 + tt < T) red[warp][t0 + tt] = v;
+      const uint32_t m = __reduce_max_sync(0xffffffffu, mag[tt]);
+      if (slot == 0 && lane == 0 && t0 + tt < T) xmag[part][t0 + tt] = m;
     }
   }
   __syncthreads();
+  if (a.x_f16) {
+    for (int t = threadIdx.x; t < T; t += blockDim.x) {
+      uint32_t m = 0;
+      for (int p = 0; p < wpe; ++p) m = max(m, xmag[p][t]);
+      xexp_s[t] = range_exp(m);
+      if (blockIdx.x == 0 && a.xexp) a.xexp[t] = xexp_s[t];
+    }
+    __syncthreads();
+  }
   // the H slices of one expert, summed in slice order
   for (int i = threadIdx.x; i < a.epc * T; i += blockDim.x) {
     const int sl = i / T, t = i - sl * T;
@@ -281,7 +298,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
       uint4 o;
       if (a.x_f16) {
-        o = bf16_chunk_to_f16_pairs(v);
+        o = bf16_chunk_to_f16_pairs(v, exp2i(-xexp_s[i / (H / 8)]));
       } else {
         o.x = prmt(v.x, v.z, 0x5410);
         o.y = prmt(v.x, v.z, 0x7632);

@@ -42,7 +42,7 @@ static RouteLayout route_layout(int64_t T, int64_t H, int E, int k, int shared, 
 struct FwdLayout {
   RouteLayout r;
   size_t seg_expert, seg_row0, seg_rows, seg_item_gu, seg_item_dn, chunk_list, h, y, xp,
-      split_part, split_cnt, total;
+      xexp, rexp, hexp, split_part, split_cnt, total;
   int ksplit;     // gate/up contraction splits (warp paths)
   int ksplit_dn;  // down contraction splits (CTA-staged warp path)
   int nblk_gu, nblk_dn;  // CTA-staged warp path: row blocks per expert
@@ -95,6 +95,10 @@ static FwdLayout fwd_layout(const strata_moe_layer* L, int64_t T) {
   F.h = o; o = up(o + sizeof(uint16_t) * rows * L->I);
   F.y = o; o = up(o + sizeof(float) * rows * L->H);
   F.xp = o; o = up(o + sizeof(uint16_t) * rows * L->H);  // gathered / pair-interleaved x
+  // range exponents of the f16 GEMM operands: per token of x_perm, per gathered row, per h row
+  F.xexp = o; o = up(o + sizeof(int) * T);
+  F.rexp = o; o = up(o + sizeof(int) * rows);
+  F.hexp = o; o = up(o + sizeof(int) * rows);
   // the CTA-staged kernel reads scale pairs with 4-byte copies: even group counts only
   // (256-wide groups: the pair holding a block's scale starts at an even group: K / 256 even)
   const int G = layer_group(L);
@@ -277,6 +281,7 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     ra.gates = gates;
     ra.x_perm = F.tc ? nullptr : base + F.xp;
     ra.x_f16 = F.cta;  // the CTA-staged GEMM multiplies f16 operands
+    ra.xexp = reinterpret_cast<int*>(base + F.xexp);
     ra.grp = pa;
     ra.do_group = true;
     e = launch_route_small(ra, st);
@@ -293,7 +298,8 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
 
   const int64_t rows = R + (S ? T : 0);
   if (F.tc) {
-    e = launch_gather_rows(x, perm, rows, L->H, base + F.xp, false, st);
+    e = launch_gather_rows(x, perm, rows, L->H, base + F.xp, kGatherTc,
+                           reinterpret_cast<int*>(base + F.rexp), st);
     if (e != cudaSuccess) return STRATA_ERR_CUDA;
     TcArgs g{};
     g.group = layer_group(L);
@@ -306,6 +312,8 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     g.K = static_cast<int>(L->H);
     g.Nw = static_cast<int>(L->I);
     g.hdr = hdr;
+    g.aexp = reinterpret_cast<const int*>(base + F.rexp);
+    g.hexp = reinterpret_cast<int*>(base + F.hexp);
     g.seg_expert = pa.seg_expert;
     g.seg_row0 = pa.seg_row0;
     g.seg_rows = pa.seg_rows;
@@ -322,6 +330,8 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     d.out = base + F.y;
     d.K = static_cast<int>(L->I);
     d.Nw = static_cast<int>(L->H);
+    d.aexp = g.hexp;
+    d.hexp = nullptr;
     d.seg_item = pa.seg_item_dn;
     e = launch_gemm_tc(d, false, base + F.h, rows, nexp, pa.tokc, sms, st);
     if (e != cudaSuccess || !mark(4)) return STRATA_ERR_CUDA;
@@ -335,11 +345,15 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     g.act = reinterpret_cast<const __nv_bfloat16*>(base + F.xp);
     if (T <= kRouteSmallMaxT) {
       g.perm = perm;  // x_perm rows are tokens
+      g.aexp = F.cta ? reinterpret_cast<const int*>(base + F.xexp) : nullptr;
     } else {
-      e = launch_gather_rows(x, perm, rows, L->H, base + F.xp, F.cta, st);
+      e = launch_gather_rows(x, perm, rows, L->H, base + F.xp, F.cta ? kGatherCta : kGatherWarp,
+                             F.cta ? reinterpret_cast<int*>(base + F.rexp) : nullptr, st);
       if (e != cudaSuccess) return STRATA_ERR_CUDA;
       g.perm = nullptr;  // xp rows are GEMM rows
+      g.aexp = F.cta ? reinterpret_cast<const int*>(base + F.rexp) : nullptr;
     }
+    g.hexp = F.cta ? reinterpret_cast<int*>(base + F.hexp) : nullptr;
     g.out = base + F.h;
     g.K = static_cast<int>(L->H);
     g.N = static_cast<int>(L->I);
@@ -358,6 +372,8 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     d.scales1 = nullptr;
     d.act = reinterpret_cast<const __nv_bfloat16*>(base + F.h);
     d.perm = nullptr;
+    d.aexp = g.hexp;
+    d.hexp = nullptr;
     d.out = base + F.y;
     d.K = static_cast<int>(L->I);
     d.N = static_cast<int>(L->H);

@@ -109,8 +109,9 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulation, one CTA.
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+// D[tmem] (+)= A[smem] * B[smem]^T, 16-bit inputs (the type is in idesc), fp32 accumulation,
+// one CTA.
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
@@ -152,6 +153,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
   d |= static_cast<uint64_t>(2) << 61;                   // 128-byte swizzle
   return d;
+}
+// Instruction descriptor: kind::f16, f16 A and B (both K-major), fp32 D, shape M x N.
+__device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 // Instruction descriptor: kind::f16, bf16 A and B (both K-major), fp32 D, shape M x N.
 __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
