@@ -161,7 +161,9 @@ def route_topk(x_bits: np.ndarray, w_router: np.ndarray, bias, k: int, renorm: b
     lower id), gates = p[ids] (renormalised over the k only when asked).
     Returns dict(ids int32 [T,k], gates f64 [T,k], probs f64 [T,E],
     gap f64 [T] = p_(k) - p_(k+1) (inf when k == E), inner_gap f64 [T] =
-    smallest gap between adjacent selected probabilities).
+    smallest gap between adjacent selected probabilities, dot_l2 f64 [T,E] =
+    ||x_t * w_e||_2, the size of each logit's product terms, from which the
+    rounding error of a finite-precision logit is bounded).
     """
     x = bf16_to_f64(x_bits)
     wr = np.asarray(w_router, dtype=np.float32).astype(np.float64)
@@ -184,7 +186,9 @@ def route_topk(x_bits: np.ndarray, w_router: np.ndarray, bias, k: int, renorm: b
              else np.full(T, np.inf))
     if renorm:
         gates = gates / gates.sum(axis=1, keepdims=True)
-    return dict(ids=ids, gates=gates, probs=p, logits=logits, gap=gap, inner_gap=inner)
+    dot_l2 = np.sqrt((x * x) @ (wr * wr).T)
+    return dict(ids=ids, gates=gates, probs=p, logits=logits, gap=gap, inner_gap=inner,
+                dot_l2=dot_l2)
 
 
 # ----------------------------------------------------------------------------- permute
@@ -230,7 +234,7 @@ def expert_ffn(x: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray, w_down: np.n
 
 
 def moe_forward(x_bits, w_router, bias, k, experts, E, shared=0, renorm=False,
-                residual=False, tokens=None):
+                residual=False, tokens=None, expert_out=None):
     """The routed MoE FFN layer in fp64.
 
     x_bits   bf16 bits [T, H]
@@ -238,6 +242,11 @@ def moe_forward(x_bits, w_router, bias, k, experts, E, shared=0, renorm=False,
              (down_codes, down_scales)), e in [0, E] (E = shared expert)
     tokens   optional token indices; only these output rows are computed
              (each token's output depends on its own row alone).
+    expert_out  optional {e: expert_ffn rows} computed by the caller with this
+             module's quantize_groups / dequantize / expert_ffn (e.g. several
+             experts at once in worker processes): for a routed expert, the
+             rows routed to it in the order of np.argwhere(ids == e); for the
+             shared expert E, every selected token. experts is then not used.
 
     out[t] = sum_j gates[t,j] * FFN_{ids[t,j]}(x_t) + shared * FFN_E(x_t)
              (+ x_t when residual), summed j = 0..k-1, then shared, then x.
@@ -260,16 +269,20 @@ def moe_forward(x_bits, w_router, bias, k, experts, E, shared=0, renorm=False,
             deq_cache[e] = (dequantize(gc, gs), dequantize(uc, us), dequantize(dc, ds))
         return deq_cache[e]
 
+    def ffn(e, rows):
+        if expert_out is not None:
+            return expert_out[e]
+        wg, wu, wd = deq(e)
+        return expert_ffn(x[rows], wg, wu, wd)
+
     y_routed = np.zeros((T, k, H), dtype=np.float64)
     for e in np.unique(ids):
         sel = np.argwhere(ids == e)             # (token, slot) pairs routed to e
-        wg, wu, wd = deq(int(e))
-        y_routed[sel[:, 0], sel[:, 1]] = expert_ffn(x[sel[:, 0]], wg, wu, wd)
+        y_routed[sel[:, 0], sel[:, 1]] = ffn(int(e), sel[:, 0])
     for j in range(k):
         out += gates[:, j:j + 1] * y_routed[:, j]
     if shared:
-        wg, wu, wd = deq(E)
-        out += expert_ffn(x, wg, wu, wd)
+        out += ffn(E, np.arange(T))
     if residual:
         out += x
     return dict(out=out, route=r)

@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 
 import oracle
+import oracle_pool
 from helpers import (OracleExperts, bf16_tensor, bf16_to_np_bits, build_gpu_layer, compare_output,
                      compare_routing, run_forward)
 from workloads import CONFIGS, Workload, gen
@@ -30,7 +31,7 @@ def layer_for(key, layer=0, router_kind=None, flags=0):
 
 
 def check_layer(wl, L, wr, b, x, layer=0, residual=False, renorm=False, rows=None,
-                overrides=None):
+                overrides=None, ties_expected=False):
     g = run_forward(L, x)
     tokens = np.arange(x.shape[0]) if rows is None else np.asarray(rows)
     experts = OracleExperts(wl, layer, overrides, group=getattr(L, "group", 128),
@@ -38,7 +39,7 @@ def check_layer(wl, L, wr, b, x, layer=0, residual=False, renorm=False, rows=Non
     ref = oracle.moe_forward(x, wr, b, wl.k, experts, wl.E, wl.shared,
                              renorm=renorm, residual=residual, tokens=tokens)
     full_ref = oracle.route_topk(x, wr, b, wl.k, renorm=renorm)
-    diff, _ = compare_routing(g, full_ref, wl.E)
+    diff, _ = compare_routing(g, full_ref, wl.E, ties_expected=ties_expected)
     keep = ~diff[tokens]
     compare_output(g["out"][tokens][keep], ref["out"][keep])
     return int(diff.sum())
@@ -89,7 +90,7 @@ def test_dense_equivalence_on_gpu():
     wl = SMALL
     wr = np.zeros((wl.E, wl.H), np.float32)
     L, wr, b = build_gpu_layer(wl, w_router=wr)
-    check_layer(wl, L, wr, b, gen.activations(9, wl.H, 4))
+    check_layer(wl, L, wr, b, gen.activations(9, wl.H, 4), ties_expected=True)
 
 
 def test_largest_expert_count_and_top_k():
@@ -174,13 +175,16 @@ def test_tc_path_shared_expert_and_long_segments():
 
 def test_expert_statistics_accumulate_across_calls():
     """strata_moe_forward_stats adds each batch's routed rows per expert (and T for the shared
-    expert) into a caller-owned counter array; the output equals strata_moe_forward's."""
+    expert) into a caller-owned counter array (the per-expert activation counts of "Strata" 3090
+    tuning, xdnf.cn/news/329730, §5.5). The totals must equal the counts of the oracle's routing
+    (oracle.route_topk -> oracle.permute) summed over the batches; the output equals
+    strata_moe_forward's."""
     import torch
     import int4_grouped_expert_gb300 as st
     wl, L, wr, b = layer_for("c2")
     hits = torch.zeros(wl.E + wl.shared, dtype=torch.int64, device="cuda")
     expect = np.zeros(wl.E + wl.shared, np.int64)
-    for T, name in ((16, "stats16"), (5, "stats5"), (64, "stats64")):
+    for T, name in ((16, "stats16"), (5, "stats5"), (64, "stats64"), (200, "stats200")):
         xb = gen.activations(T, wl.H, wl.seed, name=name)
         x = bf16_tensor(xb)
         out = torch.empty_like(x)
@@ -188,14 +192,18 @@ def test_expert_statistics_accumulate_across_calls():
         st.check(st.strata_moe_forward_stats(L.struct(), x, T, out, hits, ws, ws.numel()), "stats")
         ref = run_forward(L, xb, taps=True)
         np.testing.assert_array_equal(bf16_to_np_bits(out), ref["out"])
-        expect[:wl.E] += ref["counts"]
+        route = oracle.route_topk(xb, wr, b, wl.k)
+        compare_routing(ref, route, wl.E)
+        assert (ref["ids"] == route["ids"]).all(), "a near-tie token routed differently"
+        expect[:wl.E] += oracle.permute(route["ids"], wl.E)["counts"]
         expect[wl.E] += T
     np.testing.assert_array_equal(hits.cpu().numpy(), expect)
 
 
 def test_forward_replays_from_a_cuda_graph():
     """The forward captured once in a CUDA graph (fixed buffers, PDL chain inside) and replayed on
-    new inputs copied into the captured input buffer gives the direct call's results."""
+    new inputs copied into the captured input buffer gives the direct call's results, and matches
+    the oracle."""
     import torch
     import int4_grouped_expert_gb300 as st
     wl, L, wr, b = layer_for("c2")
@@ -217,8 +225,12 @@ def test_forward_replays_from_a_cuda_graph():
         x_static.copy_(bf16_tensor(xb))
         g.replay()
         torch.cuda.synchronize()
+        got = bf16_to_np_bits(out)
         ref = run_forward(L, xb)
-        np.testing.assert_array_equal(bf16_to_np_bits(out), ref["out"])
+        np.testing.assert_array_equal(got, ref["out"])
+        diff, _ = compare_routing(ref, oracle.route_topk(xb, wr, b, wl.k), wl.E)
+        rows = np.array([t for t in range(T) if not diff[t]], dtype=np.int64)
+        compare_output(got[rows], oracle_pool.moe_forward(wl, xb, wr, b, rows)["out"])
 
 
 @pytest.mark.parametrize("T", [16, 200])

@@ -1,40 +1,68 @@
 """The 8-layer decode stack (hidden 4096, expert inter 2048, 128 experts top-4 + shared, Zipf
 router per layer, residual add between layers): strata_moe_stack_forward against the layer-by-layer
-calls, and each checked layer against the oracle, teacher-forced (the oracle's layer l takes the
-GPU's bf16 input to layer l, so a sub-tolerance difference cannot flip a route in a later layer).
+calls, and each layer against the oracle, teacher-forced (the oracle's layer l takes the GPU's
+bf16 input to layer l, so a sub-tolerance difference cannot flip a route in a later layer).
+
+Per batch size (1, 4, 8 and 32 tokens, the decode sweep): every layer's routing (ids, gates,
+grouping) against the oracle's routing of that layer's input, the stack call bit-for-bit against
+the layer-by-layer calls, and the output of layers 0, 3 and 7 against the oracle (for 32 tokens on
+a seeded half of them). The max-abs bound is scaled by the output's rms (the residual stream grows
+without normalisation); the unscaled max-abs is printed beside it. The residual stream of some
+tokens grows by orders of magnitude per layer (SiLU(g)*u is close to quadratic for large inputs):
+the GEMMs take their f16 operands with a per-row power-of-two range exponent, so such rows stay
+exact; tokens whose true output is beyond the largest bf16 have nothing to compare and are counted.
 """
 import numpy as np
 import pytest
 
 import oracle
-from helpers import OracleExperts, bf16_tensor, bf16_to_np_bits, build_gpu_layer, compare_output
+import oracle_pool
+from helpers import bf16_tensor, bf16_to_np_bits, build_gpu_layer, compare_output, compare_routing
 from workloads import CONFIGS, gen
 
 pytestmark = pytest.mark.gpu
 
+BF16_MAX = float(np.float32(3.3895313892515355e38))   # largest finite bf16
 
-def test_c4_stack_layerwise_teacher_forced():
-    import torch
+
+@pytest.fixture(scope="module")
+def stack():
     import int4_grouped_expert_gb300 as st
     wl = CONFIGS["c4"]
-    T = 4
     layers, routers = [], []
     for l in range(wl.layers):
         L, wr, b = build_gpu_layer(wl, layer=l, flags=st.STRATA_ADD_RESIDUAL)
         layers.append(L)
         routers.append((wr, b))
-    x0 = gen.activations(T, wl.H, wl.seed, name="stack")
+    return wl, layers, routers
+
+
+@pytest.mark.parametrize("T", [1, 4, 8, 32])
+def test_c4_stack_layerwise_teacher_forced(stack, T):
+    import torch
+    import int4_grouped_expert_gb300 as st
+    wl, layers, routers = stack
+    x0 = gen.activations(T, wl.H, wl.seed, name=f"stack{T}")
     x = bf16_tensor(x0)
-    # layer by layer
-    acts = [x0]
+    # layer by layer, with the routing taps
+    acts, taps = [x0], []
     cur = x
     for L in layers:
         out = torch.empty_like(cur)
         ws = torch.empty(L.workspace_size(T), dtype=torch.uint8, device="cuda")
-        st.check(st.strata_moe_forward(L.struct(), cur, T, out, ws, ws.numel()), "forward")
+        t = dict(ids=torch.empty(T, wl.k, dtype=torch.int32, device="cuda"),
+                 gates=torch.empty(T, wl.k, dtype=torch.float32, device="cuda"),
+                 counts=torch.empty(wl.E, dtype=torch.int32, device="cuda"),
+                 offsets=torch.empty(wl.E + 1, dtype=torch.int32, device="cuda"),
+                 perm=torch.empty(T * wl.k, dtype=torch.int32, device="cuda"),
+                 inv=torch.empty(T, wl.k, dtype=torch.int32, device="cuda"))
+        st.check(st.strata_moe_forward_ex(L.struct(), cur, T, out, workspace=ws,
+                                          ws_bytes=ws.numel(), **t), "forward_ex")
+        torch.cuda.synchronize()
         acts.append(bf16_to_np_bits(out))
+        taps.append({n: v.cpu().numpy() for n, v in t.items()})
         cur = out
-    # one stack call
+    # one stack call gives the same bits
     structs = [L.struct() for L in layers]
     need = st.strata_moe_stack_workspace_size(structs, T)
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
@@ -42,12 +70,26 @@ def test_c4_stack_layerwise_teacher_forced():
     st.check(st.strata_moe_stack_forward(structs, x, T, out, ws, need), "stack")
     torch.cuda.synchronize()
     np.testing.assert_array_equal(bf16_to_np_bits(out), acts[-1])
-    # teacher-forced oracle on sampled layers and tokens
+    s, v = st.strata_workspace_status(ws)
+    assert s == 0, f"device status 0x{v:x}"
+    # every layer's routing, teacher-forced
+    diffs = []
+    for l in range(wl.layers):
+        wr, b = routers[l]
+        diff, _ = compare_routing(taps[l], oracle.route_topk(acts[l], wr, b, wl.k), wl.E)
+        diffs.append(diff)
+    # outputs of layers 0, 3, 7
+    rows_all = np.arange(T) if T <= 8 else np.sort(
+        np.random.default_rng(T).choice(T, T // 2, replace=False))
     for l in (0, 3, 7):
         wr, b = routers[l]
-        rows = [0, 3]
-        ref = oracle.moe_forward(acts[l], wr, b, wl.k, OracleExperts(wl, l), wl.E, wl.shared,
-                                 residual=True, tokens=rows)
-        route = oracle.route_topk(acts[l][rows], wr, b, wl.k)
-        ok = route["gap"] > 1e-6
-        compare_output(acts[l + 1][rows][ok], ref["out"][ok], scale_max_abs=True)
+        rows = np.array([t for t in rows_all if not diffs[l][t]], dtype=np.int64)
+        if rows.size == 0:   # every checked token was a near tie routed differently
+            continue
+        ref = oracle_pool.moe_forward(wl, acts[l], wr, b, rows, layer=l, residual=True)
+        # without normalisation a token's residual stream can outgrow bf16 (and fp32) by the last
+        # layers: such outputs have no finite bf16 value to compare with
+        finite = np.abs(ref["out"]).max(axis=1) < BF16_MAX
+        print(f"layer {l}: {int((~finite).sum())} of {rows.size} tokens beyond the bf16 range")
+        if finite.any():
+            compare_output(acts[l + 1][rows[finite]], ref["out"][finite], scale_max_abs=True)

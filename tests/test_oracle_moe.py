@@ -133,3 +133,28 @@ def test_planted_silu_sign_mistake_is_caught(monkeypatch):
     xf = gen.bf16_bits_to_f32(x).astype(np.float64)
     ref = torch_swiglu(xf, *[oracle.dequantize(c, s) for (c, s) in ws[0]])
     assert not np.allclose(res["out"], ref, rtol=1e-6)
+
+
+def test_expert_outputs_from_worker_processes_match_the_serial_oracle():
+    """tests/oracle_pool.py evaluates the experts in spawned workers and hands them to
+    oracle.moe_forward; the result must be the serial oracle's, bit for bit."""
+    from helpers import OracleExperts
+    import oracle_pool
+    from workloads import CONFIGS
+    wl = CONFIGS["c1"]
+    x = gen.activations(9, wl.H, 3, name="pool")
+    wr, b = gen.router_weight(wl), gen.router_bias(wl)
+    tokens = [0, 2, 5, 8]
+    ref = oracle.moe_forward(x, wr, b, wl.k, OracleExperts(wl), wl.E, wl.shared, tokens=tokens)
+    got = oracle_pool.moe_forward(wl, x, wr, b, tokens, procs=2)
+    np.testing.assert_array_equal(got["out"], ref["out"])
+
+
+def test_bf16_half_ulp_of_the_output_comparison():
+    """The allowance compare_output grants for the output's final bf16 rounding: half the spacing
+    of bf16 values at the element (8 significant bits)."""
+    from helpers import bf16_half_ulp
+    v = np.array([1.0, 1.5, 8.0, 15.9, -8.22, 0.0, 2.0 ** -20])
+    np.testing.assert_array_equal(bf16_half_ulp(v),
+                                  [2.0 ** -8, 2.0 ** -8, 2.0 ** -5, 2.0 ** -5, 2.0 ** -5, 0.0,
+                                   2.0 ** -28])

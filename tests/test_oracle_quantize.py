@@ -342,3 +342,86 @@ def test_planted_divisor_mistake_is_caught_8bit(monkeypatch):
         w[0, i] = v
     codes, scales = so.quantize_groups(w, bits=8)
     assert float(scales[0, 0]) != g["scale"]
+
+
+# ---------------------------------------------------------------- the fp16-quotient reading
+
+def _fp16_rne(q):
+    """Nearest fp16 to a positive rational (ties to an even significand), normal range only:
+    written with Fractions, independent of numpy's float16 conversion."""
+    from fractions import Fraction
+    e = 0
+    while Fraction(2) ** (e + 1) <= q:
+        e += 1
+    while Fraction(2) ** e > q:
+        e -= 1
+    ulp = Fraction(2) ** (e - 10)
+    m = q / ulp
+    n = m.numerator // m.denominator
+    rem = m - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return n * ulp
+
+
+def _round_half_even(q):
+    from fractions import Fraction
+    n = q.numerator // q.denominator
+    rem = q - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return n
+
+
+def _disagreeing_pairs():
+    """(absmax, w) fp16 pairs, as Fractions, whose exact quotient w/s is not a half-integer but
+    rounds to one in fp16 (s = fp16(absmax / 7)), so that the two readings give different codes.
+    Found by an exact search over 11-bit significands near the quotients 1.5, 2.5 and 3.5."""
+    from fractions import Fraction
+    found = []
+    for target in (Fraction(3, 2), Fraction(5, 2), Fraction(7, 2)):
+        done = False
+        for S in range(1025, 2048):
+            s = Fraction(S, 2 ** 13)
+            for A in range(1024, 2048):        # absmax = A * 2^-11 must give this scale
+                a = Fraction(A, 2 ** 11)
+                if _fp16_rne(a / 7) != s or a < 7 * s * Fraction(99, 100):
+                    continue
+                for W in range(512, 2048):     # w = W * 2^-12 near target * s
+                    w = Fraction(W, 2 ** 12)
+                    if w > a:
+                        break
+                    q = w / s
+                    if abs(q - target) > Fraction(1, 256) or q == target:
+                        continue
+                    if _round_half_even(q) != _round_half_even(_fp16_rne(q)):
+                        found.append((a, w, q))
+                        done = True
+                        break
+                if done:
+                    break
+            if done:
+                break
+    return found
+
+
+def test_f16_quotient_reading_on_exact_rational_half_ties():
+    """quantize_groups_f16_quotient (the literal fp16 reading: w/s rounded to fp16, then rounded
+    half to even) against exact rational arithmetic, on groups built so that fp16(w/s) lands on a
+    half-integer while w/s itself does not: the exact reading (quantize_groups) and the fp16
+    reading must then give different codes, each the one the rational arithmetic predicts."""
+    pairs = _disagreeing_pairs()
+    assert len(pairs) == 3, pairs
+    for a, w, q in pairs:
+        g = np.zeros((1, 128), dtype=np.float16)
+        g[0, 0] = float(a)
+        g[0, 5] = float(w)
+        g[0, 9] = -float(w)
+        assert g[0, 0] == float(a) and g[0, 5] == float(w)   # exactly representable
+        exact = so.unpack_codes(so.quantize_groups(g)[0])[0]
+        lit = so.unpack_codes(so.quantize_groups_f16_quotient(g)[0])[0]
+        q_exact, q_lit = _round_half_even(q), _round_half_even(_fp16_rne(q))
+        assert q_exact != q_lit
+        assert exact[5] == q_exact and exact[9] == -q_exact
+        assert lit[5] == q_lit and lit[9] == -q_lit
+        assert exact[0] == lit[0] == 7

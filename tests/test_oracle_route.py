@@ -143,3 +143,18 @@ def test_planted_tie_break_mistake_is_caught(monkeypatch):
     x = gen.activations(2, 128, 0)
     r = so.route_topk(x, np.zeros((6, 128), np.float32), None, 2)
     assert not np.array_equal(r["ids"], np.tile([0, 1], (2, 1)))
+
+
+def test_dot_l2_is_the_norm_of_each_logits_product_terms():
+    """route_topk's dot_l2[t, e] = sqrt(sum_h (x[t,h] * w[e,h])^2), by pure-Python loops."""
+    rng = np.random.default_rng(4)
+    x = gen.f32_to_bf16_bits(rng.standard_normal((3, 16)).astype(np.float32))
+    w = (rng.standard_normal((5, 16)) * 0.3).astype(np.float32)
+    r = oracle.route_topk(x, w, None, 2)
+    xf = oracle.bf16_to_f64(x)
+    for t in range(3):
+        for e in range(5):
+            s = 0.0
+            for h in range(16):
+                s += (float(xf[t, h]) * float(w[e, h])) ** 2
+            assert abs(r["dot_l2"][t, e] - math.sqrt(s)) <= 1e-12 * math.sqrt(s)
