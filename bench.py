@@ -12,6 +12,13 @@ batches, so no step finds its weights in L2.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl strata|reference] [--batch T]
 
+The default single-GPU run also reports, each under its own key with its own roofline:
+"padded_graph" (one CUDA graph captured at 16 tokens replayed with 1/5/16 live tokens),
+"prefill_c5" (on-device quantization GB/s and the 4096-token tensor-core layer's TFLOP/s against
+the burst bf16 peak), "prefill_c3" (the 512-token layer against its HBM roof) and "stack_c4" (the
+8-layer decode stack at 1..32 tokens). Their experts are drawn N(0, 0.02) on the device (the same
+distribution as the host generator) and quantized there; --no-extras skips them.
+
 Under torchrun (N > 1) each rank runs its own replica of the layer on its own GPU (the layer is
 data-parallel over tokens: no exchange step); the time is the max over ranks and the value the
 tokens all ranks processed per second.
@@ -444,43 +451,97 @@ def run_strata(args):
         "gpu_launches": kernels_per_forward(T) * args.steps,
         "clocks": clk,
     }
+    if ws_n == 1 and not args.quick and not args.no_extras:
+        # the rest of the metric on the same GPU, each under its own key with its own roofline:
+        # the padded fixed-max-batch graph (this layer), the prefill layers and the decode stack
+        t0 = time.perf_counter()
+        rec["padded_graph"] = guarded(padded_graph_measure, layers, wl, 16, (1, 5, 16), 200,
+                                      args.warmup)
+        rec["prefill_c5"] = guarded(prefill_measure, "c5", 10, 3, local=local)
+        rec["prefill_c3"] = guarded(prefill_measure, "c3", 50, 5, local=local)
+        rec["stack_c4"] = guarded(stack_measure, 200, 5, CONFIGS["c4"].batches, local=local)
+        rec["extras_wall_s"] = time.perf_counter() - t0
     if rank == 0:
         if ws_n == 1 and not args.quick:
             rec["cpu_baseline"] = cpu_baseline(wl, xs_host, T)
         print(json.dumps(rec), flush=True)
 
 
-def run_prefill(args):
-    """Prefill workloads (c3: 512 tokens; c5: 4096 tokens + on-device quantization) on the
-    tensor-core path. Reports tokens/s, gate/up and down TFLOP/s and, for c5, quantize GB/s."""
+def guarded(fn, *a, **kw):
+    """fn's record, or the error it raised (an extra measurement never hides the headline)."""
+    try:
+        return fn(*a, **kw)
+    except Exception as exc:  # noqa: BLE001 - reported in the JSON line
+        import traceback
+        traceback.print_exc(file=sys.stderr)
+        return {"error": f"{type(exc).__name__}: {exc}"}
+
+
+def device_random_experts(L, seed, chunk=16):
+    """Fill every expert slot of L with codes quantized on the device (strata_quantize_groups_bits)
+    from fp16 weights drawn N(0, 0.02) on the device by torch's seeded CUDA generator: the
+    workloads' distribution, drawn where it is used (tens of GB of fp16 would take minutes in the
+    host generator). The timings depend on the shapes and on the routing, not on these values."""
+    import torch
+    import int4_grouped_expert_gb300 as st
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    n = L.E + L.shared
+    for codes, scales, rows, cols in ((L.gate_codes, L.gate_scales, L.I, L.H),
+                                      (L.up_codes, L.up_scales, L.I, L.H),
+                                      (L.down_codes, L.down_scales, L.H, L.I)):
+        for e0 in range(0, n, chunk):
+            e1 = min(n, e0 + chunk)
+            w = (torch.randn((e1 - e0) * rows, cols, generator=g, device="cuda") * 0.02).half()
+            st.check(st.strata_quantize_groups_bits(w, (e1 - e0) * rows, cols, codes[e0:e1],
+                                                    scales[e0:e1], L._status, group_size=L.group,
+                                                    bits=L.bits), "strata_quantize_groups_bits")
+            del w
+    torch.cuda.synchronize()
+    L.check_status()
+
+
+def tensor_peak(timed_s):
+    """Dense bf16 tensor peak (TFLOP/s) for a kernel timed over timed_s seconds: the burst figure
+    below a second, the sustained one (power cap) above. f16 operands run at the bf16 rate."""
+    try:
+        d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        if timed_s < 1.0:
+            return float(d["bf16_tflops"]), "measured burst"
+        return float(d["bf16_tflops_sustained"]), "measured sustained"
+    except Exception:
+        return (1900.0, "fallback burst") if timed_s < 1.0 else (1700.0, "fallback sustained")
+
+
+def prefill_measure(key, steps, warmup, experts=0, tokens=0, router=None, host_weights=False,
+                    local=0):
+    """A prefill layer (c3: 512 tokens over 64 experts; c5: 4096 tokens over 256 + shared, with its
+    experts quantized on the device from resident fp16 stacks, timed) on the tensor-core path:
+    tokens/s, gate/up and down TFLOP/s, the gate/up roofline and, for c5, quantize GB/s."""
     import torch
     import int4_grouped_expert_gb300 as st
     from int4_grouped_expert_gb300 import MoELayer
-    ws_n, rank = init_dist("nccl")
-    _, _, local = dist_env()
-    torch.cuda.set_device(local)
-    st.lib()
-    wl = CONFIGS[args.workload]
-    if args.experts:  # a smaller layer of the same shapes (e.g. for profiler captures)
+    wl = CONFIGS[key]
+    if experts:  # a smaller layer of the same shapes (e.g. for profiler captures)
         import dataclasses
-        wl = dataclasses.replace(wl, E=args.experts)
-    T = args.tokens or wl.batches[0]
+        wl = dataclasses.replace(wl, E=experts)
+    T = tokens or wl.batches[0]
     L = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared)
-    L.set_router(gen.router_weight(wl), gen.router_bias(wl, 0, args.router) if not args.experts
-                 else None)
+    L.set_router(gen.router_weight(wl), gen.router_bias(wl, 0, router) if not experts else None)
     n = wl.E + wl.shared
     quant = None
-    if args.workload == "c5" and not args.experts:
+    hbm_peak, hbm_kind = peak_numbers()
+    if key == "c5" and not experts:
         # fp16 experts resident on the device, then one quantize launch per projection stack
-        w16 = {"gate": torch.empty(n, wl.I, wl.H, dtype=torch.float16, device="cuda"),
-               "up": torch.empty(n, wl.I, wl.H, dtype=torch.float16, device="cuda"),
-               "down": torch.empty(n, wl.H, wl.I, dtype=torch.float16, device="cuda")}
-        for s0 in range(0, n, 16):
-            es = list(range(s0, min(n, s0 + 16)))
-            for e, (g, u, d) in zip(es, gen.expert_weights_many(wl, es)):
-                w16["gate"][e].copy_(torch.from_numpy(g))
-                w16["up"][e].copy_(torch.from_numpy(u))
-                w16["down"][e].copy_(torch.from_numpy(d))
+        g = torch.Generator(device="cuda")
+        g.manual_seed(wl.seed)
+        w16 = {}
+        for name, rows, cols in (("gate", wl.I, wl.H), ("up", wl.I, wl.H), ("down", wl.H, wl.I)):
+            t = torch.empty(n, rows, cols, dtype=torch.float16, device="cuda")
+            for e0 in range(0, n, 16):
+                e1 = min(n, e0 + 16)
+                t[e0:e1].copy_(torch.randn(e1 - e0, rows, cols, generator=g, device="cuda") * 0.02)
+            w16[name] = t
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         jobs = [(w16["gate"], L.gate_codes, L.gate_scales, wl.I * n, wl.H),
                 (w16["up"], L.up_codes, L.up_scales, wl.I * n, wl.H),
@@ -501,42 +562,41 @@ def run_prefill(args):
         torch.cuda.synchronize()
         qs = e0.elapsed_time(e1) / reps / 1e3
         nw = 3 * n * wl.H * wl.I
-        qbytes = nw * 2 + nw // 2 + 2 * (nw // 128)
-        quant = {"seconds": qs, "weights": nw, "bytes": qbytes, "gbs": qbytes / qs / 1e9,
-                 "frac_of_hbm": qbytes / qs / 1e9 / peak_numbers()[0]}
+        qbytes = nw * 2 + nw // 2 + 2 * (nw // 128)  # fp16 in, int4 codes + fp16 scales out
+        gbs = qbytes / qs / 1e9
+        quant = {"seconds_per_layer": qs, "weights": nw, "launches_per_layer": 3,
+                 "roofline": {"kernel": "quantize_groups_kernel", "bound": "hbm", "achieved": gbs,
+                              "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                              "peak_kind": hbm_kind,
+                              "algorithmic_bytes_per_launch": qbytes / 3,
+                              "traffic": measured_traffic("quantize_c5")}}
         rc, v = st.strata_read_status(status)
         assert rc == 0, hex(v)
-        del w16
+        del w16, jobs
         torch.cuda.empty_cache()
-    else:
+    elif host_weights:
         for s0 in range(0, n, 16):
             es = list(range(s0, min(n, s0 + 16)))
             for e, m in zip(es, gen.expert_weights_many(wl, es)):
                 L.load_expert_fp16(e, *m)
         torch.cuda.synchronize()
         L.check_status()
+    else:
+        device_random_experts(L, wl.seed)
     xs_host, xs_dev = token_batches(wl, T, 2)
     ws_bytes = L.workspace_size(T)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     out = torch.empty(T, wl.H, dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.Stream()
-    steps = args.steps
     clocks = ClockSampler(local)
-    torch.cuda.nvtx.range_push("timed")
-    elapsed_ms, _ = time_steps([L], xs_dev, T, steps, args.warmup, stream, ws, ws_bytes, out)
-    torch.cuda.nvtx.range_pop()
+    elapsed_ms, _ = time_steps([L], xs_dev, T, steps, warmup, stream, ws, ws_bytes, out)
     clk = clocks.stop()
-    _, stages = time_steps([L], xs_dev, T, steps, args.warmup, stream, ws, ws_bytes, out,
-                           profiled=True)
+    _, stages = time_steps([L], xs_dev, T, steps, warmup, stream, ws, ws_bytes, out, profiled=True)
     rows = T * wl.k + wl.shared * T
     gu_flops = 2 * 2 * wl.H * wl.I * rows
     dn_flops = 2 * wl.H * wl.I * rows
     ms = elapsed_ms / steps
-    peak_tf = 1695.4
-    try:
-        peak_tf = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops_sustained"])
-    except Exception:
-        pass
+    peak_tf, tf_kind = tensor_peak(elapsed_ms / 1e3)
     gu_tf = gu_flops / (stages["gate_up_gemm"] / 1e3) / 1e12
     dn_tf = dn_flops / (stages["down_gemm"] / 1e3) / 1e12
     layer_tf = (gu_flops + dn_flops) / (ms / 1e3) / 1e12
@@ -544,30 +604,54 @@ def run_prefill(args):
     # gate + up codes and scales) against the ridge of the measured peaks
     n_exp = float(np.mean([routed_experts(L, x, T) for x in xs_dev]))
     gu_bytes = n_exp * 2 * wl.H * wl.I * (0.5 + 2 / 128)
-    hbm_peak, hbm_kind = peak_numbers()
     hbm_bound = gu_flops / gu_bytes < peak_tf * 1e12 / (hbm_peak * 1e9)
-    traffic_key = {"c5": "prefill_gate_up_c5", "c3": "prefill_gate_up_c3"}.get(args.workload)
-    traffic = (measured_traffic(traffic_key)
-               if traffic_key and not args.experts and not args.tokens else None)
+    traffic_key = {"c5": "prefill_gate_up_c5", "c3": "prefill_gate_up_c3"}.get(key)
+    traffic = measured_traffic(traffic_key) if traffic_key and not experts and not tokens else None
+    kname = "gate_up_gemm (tcgen05 grouped W4A16 GEMM + SiLU, f16 operands)"
     if hbm_bound:
         gu_gbs = gu_bytes / (stages["gate_up_gemm"] / 1e3) / 1e9
-        roof = {"kernel": "gate_up_gemm (tcgen05 grouped W4A16 GEMM + SiLU)", "bound": "hbm",
-                "achieved": gu_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gu_gbs / hbm_peak,
-                "peak_kind": hbm_kind, "algorithmic_bytes_per_launch": gu_bytes,
-                "traffic": traffic, "tflops": gu_tf}
+        roof = {"kernel": kname, "bound": "hbm", "achieved": gu_gbs, "peak": hbm_peak,
+                "unit": "GB/s", "frac": gu_gbs / hbm_peak, "peak_kind": hbm_kind,
+                "algorithmic_bytes_per_launch": gu_bytes, "traffic": traffic, "tflops": gu_tf,
+                "tensor_frac": gu_tf / peak_tf}
     else:
-        roof = {"kernel": "gate_up_gemm (tcgen05 grouped W4A16 GEMM + SiLU)", "bound": "tensor",
-                "achieved": gu_tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": gu_tf / peak_tf,
-                "peak_kind": "measured sustained", "traffic": traffic}
-    rec = {"metric": f"MoE-layer tokens/s (prefill, {args.workload})", "value": T / (ms / 1e3),
-           "unit": "tokens/s", "n_gpus": ws_n, "steps": steps, "warmup": args.warmup,
-           "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-           "dtype": "bf16", "data": "synthetic",
-           "config": {"workload": wl.name, "tokens_per_step": T, "router": args.router or wl.router},
+        roof = {"kernel": kname, "bound": "tensor", "achieved": gu_tf, "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": gu_tf / peak_tf, "peak_kind": tf_kind,
+                "algorithmic_flops_per_launch": gu_flops, "traffic": traffic}
+    rec = {"workload": wl.name, "tokens_per_step": T, "router": router or wl.router,
+           "tokens_per_s": T / (ms / 1e3), "ms_per_step": ms, "steps": steps, "warmup": warmup,
            "roofline": roof, "experts_per_step": n_exp,
-           "layer_tflops": layer_tf, "layer_frac": layer_tf / peak_tf, "down_tflops": dn_tf,
+           "layer_tflops": layer_tf, "layer_frac": layer_tf / peak_tf,
+           "down_tflops": dn_tf, "down_frac": dn_tf / peak_tf, "tensor_peak": peak_tf,
+           "tensor_peak_kind": tf_kind,
            "stages_us": {k: v * 1e3 for k, v in stages.items()}, "quantize": quant,
+           "weights": ("host-generated (workloads.gen)" if host_weights else
+                       "N(0,0.02) fp16 drawn on the device, quantized on the device"),
            "gpu_launches": kernels_per_forward(T) * steps, "clocks": clk}
+    del L, ws
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_prefill(args):
+    """Prefill workloads alone (c3 / c5), one JSON line."""
+    import torch
+    import int4_grouped_expert_gb300 as st
+    ws_n, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    st.lib()
+    r = prefill_measure(args.workload, args.steps, args.warmup, experts=args.experts,
+                        tokens=args.tokens, router=args.router, host_weights=args.host_weights,
+                        local=local)
+    rec = {"metric": f"MoE-layer tokens/s (prefill, {args.workload})", "value": r["tokens_per_s"],
+           "unit": "tokens/s", "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": r["workload"], "tokens_per_step": r["tokens_per_step"],
+                      "router": r["router"], "weights": r["weights"]},
+           "roofline": r["roofline"], "gpu_launches": r["gpu_launches"], "clocks": r["clocks"],
+           "prefill": r}
     if rank == 0:
         print(json.dumps(rec), flush=True)
 
@@ -603,21 +687,22 @@ def stack_graph_us(structs, xs_dev, T, out, ws, need, steps, warmup):
         return None
 
 
-def run_stack(args):
+def stack_measure(steps, warmup, batches, host_weights=False, local=0):
     """The 8-layer decode stack (hidden 4096, expert inter 2048, 128 experts top-4 + shared, a
-    Zipf router per layer, residual add between layers) through strata_moe_stack_forward, for
-    batches of 1/4/8/16/32 tokens: stack and per-layer tokens/s."""
+    Zipf router per layer, residual add between layers) through strata_moe_stack_forward, for each
+    batch: stack and per-layer tokens/s, HBM GB/s of the activated experts, graph replay."""
     import torch
     import int4_grouped_expert_gb300 as st
     from int4_grouped_expert_gb300 import MoELayer
-    ws_n, rank = init_dist("nccl")
-    _, _, local = dist_env()
-    torch.cuda.set_device(local)
-    st.lib()
     wl = CONFIGS["c4"]
-    # layer 0's experts are generated and quantized on the device; every other layer gets its own
-    # copy of those values at its own addresses (the same bytes stream from HBM) and its own router
-    L0 = build_layer(wl)
+    # layer 0's experts are quantized on the device; every other layer gets its own copy of those
+    # values at its own addresses (the same bytes stream from HBM) and its own router
+    if host_weights:
+        L0 = build_layer(wl)
+    else:
+        L0 = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared)
+        L0.set_router(gen.router_weight(wl), gen.router_bias(wl))
+        device_random_experts(L0, wl.seed)
     layers = [L0]
     for l in range(1, wl.layers):
         L = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared, flags=st.STRATA_ADD_RESIDUAL)
@@ -628,10 +713,10 @@ def run_stack(args):
     structs = [L.struct() for L in layers]
     stream = torch.cuda.Stream()
     eb = wl.expert_bytes()
+    peak, peak_kind = peak_numbers()
     sweep = {}
     clocks = ClockSampler(local)
-    head = args.tokens or max(wl.batches)
-    for T in ((args.tokens,) if args.tokens else wl.batches):
+    for T in batches:
         xs_host, xs_dev = token_batches(wl, T, N_TOKEN_BATCHES)
         need = st.strata_moe_stack_workspace_size(structs, T)
         ws = torch.empty(need, dtype=torch.uint8, device="cuda")
@@ -647,9 +732,8 @@ def run_stack(args):
                                               workspace=wsl, ws_bytes=wsl.numel()), "forward_ex")
             n_exp.append(int((counts.cpu().numpy() > 0).sum()) + wl.shared)
             cur = nxt
-        steps = args.steps
         with torch.cuda.stream(stream):
-            for i in range(args.warmup):
+            for i in range(warmup):
                 st.check(st.strata_moe_stack_forward(structs, xs_dev[i % N_TOKEN_BATCHES], T, out,
                                                      ws, need, stream), "stack")
             torch.cuda.synchronize()
@@ -657,7 +741,6 @@ def run_stack(args):
             torch.cuda.synchronize()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
-            torch.cuda.nvtx.range_push("timed")
             e0.record(stream)
             for i in range(steps):
                 rc = st.strata_moe_stack_forward(structs, xs_dev[i % N_TOKEN_BATCHES], T, out, ws,
@@ -665,41 +748,113 @@ def run_stack(args):
                 if rc:
                     st.check(rc, "stack")
             e1.record(stream)
-            torch.cuda.nvtx.range_pop()
             torch.cuda.synchronize()
             barrier()
         ms = max_over_ranks(e0.elapsed_time(e1)) / steps
-        graph_us = stack_graph_us(structs, xs_dev, T, out, ws, need, steps, args.warmup)
+        graph_us = stack_graph_us(structs, xs_dev, T, out, ws, need, steps, warmup)
         # per-stage times of single layers (events between the kernels), same inputs and layers
         wsl = torch.empty(max(L.workspace_size(T) for L in layers), dtype=torch.uint8, device="cuda")
-        _, stages = time_steps(layers, xs_dev, T, min(steps, 400), args.warmup, stream, wsl,
+        _, stages = time_steps(layers, xs_dev, T, min(steps, 400), warmup, stream, wsl,
                                wsl.numel(), out, profiled=True)
         st_bytes = float(sum(n_exp)) * eb
-        sweep[str(T)] = {"stack_tokens_per_s": aggregate_throughput(T * steps, ms * steps / 1e3, ws_n),
+        gbs = st_bytes / (ms / 1e3) / 1e9
+        sweep[str(T)] = {"stack_tokens_per_s": T / (ms / 1e3),
                          "layer_tokens_per_s": T / (ms / wl.layers / 1e3),
                          "us_per_stack": ms * 1e3, "us_per_layer": ms * 1e3 / wl.layers,
                          "experts_per_layer": float(np.mean(n_exp)),
-                         "hbm_gbs": st_bytes / (ms / 1e3) / 1e9, "steps": steps,
+                         "hbm_gbs": gbs, "hbm_frac": gbs / peak, "steps": steps,
                          "us_per_stack_graph": graph_us,
                          "stages_us": {k: v * 1e3 for k, v in stages.items()}}
+        del ws, wsl
     clk = clocks.stop()
-    peak, peak_kind = peak_numbers()
-    h = sweep[str(head)]
-    rec = {"metric": "MoE stack tokens/s (decode, 8 layers)", "value": h["stack_tokens_per_s"],
+    head = str(max(batches))
+    h = sweep[head]
+    rec = {"workload": wl.name, "layers": wl.layers, "tokens_per_step": int(head),
+           "roofline": {"kernel": "whole stack (all kernels)", "bound": "hbm",
+                        "achieved": h["hbm_gbs"], "peak": peak, "unit": "GB/s",
+                        "frac": h["hbm_gbs"] / peak, "peak_kind": peak_kind,
+                        "algorithmic_bytes_per_step": h["experts_per_layer"] * wl.layers * eb,
+                        "traffic": None},
+           "sweep": sweep,
+           "weights": ("layer 0's int4 g128 experts ("
+                       + ("host-generated" if host_weights else "N(0,0.02) drawn on the device")
+                       + ", quantized on the device) copied into each layer's own storage; "
+                         "per-layer Zipf routers"),
+           "l2": f"each step streams {wl.layers} layers' activated experts (GBs) > L2",
+           "gpu_launches": kernels_per_forward(int(head)) * wl.layers * h["steps"], "clocks": clk}
+    del layers, L0
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_stack(args):
+    """The 8-layer decode stack alone, one JSON line."""
+    import torch
+    import int4_grouped_expert_gb300 as st
+    ws_n, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    st.lib()
+    wl = CONFIGS["c4"]
+    batches = (args.tokens,) if args.tokens else wl.batches
+    r = stack_measure(args.steps, args.warmup, batches, host_weights=args.host_weights, local=local)
+    h = r["sweep"][str(r["tokens_per_step"])]
+    rec = {"metric": "MoE stack tokens/s (decode, 8 layers)",
+           "value": aggregate_throughput(r["tokens_per_step"] * h["steps"],
+                                         h["us_per_stack"] * h["steps"] / 1e6, ws_n),
            "unit": "tokens/s", "n_gpus": ws_n, "steps": h["steps"], "warmup": args.warmup,
            "ms_per_step": h["us_per_stack"] / 1e3, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-           "config": {"workload": wl.name, "tokens_per_step": head, "layers": wl.layers,
-                      "weights": "layer 0's int4 g128 experts (quantized on device) copied into "
-                                 "each layer's own storage; per-layer Zipf routers",
-                      "l2": f"each step streams {wl.layers} layers' experts (GBs) > L2"},
-           "roofline": {"kernel": "whole stack (all kernels)", "bound": "hbm",
-                        "achieved": h["hbm_gbs"], "peak": peak, "unit": "GB/s",
-                        "frac": h["hbm_gbs"] / peak, "peak_kind": peak_kind, "traffic": None},
-           "sweep": sweep, "gpu_launches": kernels_per_forward(head) * wl.layers * h["steps"],
-           "clocks": clk}
+           "config": {"workload": r["workload"], "tokens_per_step": r["tokens_per_step"],
+                      "layers": r["layers"], "weights": r["weights"], "l2": r["l2"]},
+           "roofline": r["roofline"], "sweep": r["sweep"], "gpu_launches": r["gpu_launches"],
+           "clocks": r["clocks"]}
     if rank == 0:
         print(json.dumps(rec), flush=True)
+
+
+def padded_graph_measure(layers, wl, T_max, batches, steps, warmup):
+    """One CUDA graph holding a strata_moe_forward_padded call per layer copy (each copy's own
+    expert storage, so every layer streams its weights from HBM), captured once at T_max and
+    replayed with each batch's live count written to the device: microseconds per layer."""
+    import torch
+    import int4_grouped_expert_gb300 as st
+    n_tok = torch.full((1,), T_max, dtype=torch.int32, device="cuda")
+    xs_host, _ = token_batches(wl, T_max, 1)
+    x_static = torch.from_numpy(xs_host[0].view(np.int16)).view(torch.bfloat16).cuda()
+    out = torch.empty_like(x_static)
+    ws = torch.empty(max(L.workspace_size(T_max) for L in layers), dtype=torch.uint8, device="cuda")
+    structs = [L.struct() for L in layers]
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):  # first calls outside the capture (one-time host set-up)
+        for s in structs:
+            st.check(st.strata_moe_forward_padded(s, x_static, n_tok, T_max, out, ws, ws.numel(),
+                                                  side), "padded")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream()
+        for s in structs:
+            st.check(st.strata_moe_forward_padded(s, x_static, n_tok, T_max, out, ws, ws.numel(),
+                                                  cs), "capture")
+    res = {}
+    for T in batches:
+        n_tok.fill_(T)
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / steps / len(structs) * 1e3
+        res[str(T)] = {"us_per_layer": us, "tokens_per_s": T / (us / 1e6)}
+    rc, v = st.strata_workspace_status(ws)
+    assert rc == 0, hex(v)
+    return {"T_max": T_max, "layers_per_replay": len(structs), "replays": steps, "batches": res}
 
 
 def run_reference(args):
@@ -782,6 +937,11 @@ def main(argv=None):
     p.add_argument("--experts", type=int, default=0, help="prefill: override the routed expert count")
     p.add_argument("--tokens", type=int, default=0,
                    help="prefill: override the batch; c4: run this batch only")
+    p.add_argument("--no-extras", action="store_true",
+                   help="c2: skip the padded-graph, prefill and stack measurements of the default run")
+    p.add_argument("--host-weights", action="store_true",
+                   help="c3/c4/c5: draw the experts with the host generator (workloads.gen) instead "
+                        "of on the device")
     p.add_argument("--oracle-sample", type=int, default=0, help=argparse.SUPPRESS)
     args = p.parse_args(argv)
     if args.oracle_sample:  # child of cpu_baseline: the oracle sample alone, tokens/s on stdout

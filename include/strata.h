@@ -74,6 +74,8 @@ typedef enum {
                                      its codes as 0) */
 #define STRATA_DEV_BAD_ID 0x2u    /* an expert id outside [0, E) reached the permutation */
 #define STRATA_DEV_TIMEOUT 0x4u   /* a bounded device wait gave up */
+#define STRATA_DEV_BAD_TOKENS 0x8u /* strata_moe_forward_padded: the device token count was outside
+                                      [0, T_max]; the call ran with no live token */
 
 #define STRATA_GROUP 128     /* [tuning-moe] §2.1: 128 weights share one scale */
 #define STRATA_MAX_EXPERTS 1024
@@ -181,6 +183,23 @@ strata_status strata_route_topk_noalloc(const void* x_bf16, const float* w_route
                                         int32_t* inv, strata_stream stream);
 
 /*
+ * strata_group_rows — the grouping step alone, for routes the caller computed ([tuning-3090]
+ * §3.2: the rows routed to one expert are gathered into one group of the grouped GEMM): the
+ * counts, offsets, perm and inv of strata_route_topk for a given ids [T,k] int32 (device), rows
+ * ordered by (expert, token, slot) (a token may name one expert in several slots).
+ * counts [E], offsets [E+1] (required); perm [T*k], inv [T,k] (required when T > 0); all int32,
+ * device, 4-byte aligned. An id outside [0, E) sets STRATA_DEV_BAD_ID in the workspace status
+ * word; its row is left out of every group (inv = -1, no perm entry) and offsets[E] counts the
+ * valid rows only, which keep the positions they would have without the invalid ones.
+ * Limits: 0 <= T <= 2^22, 1 <= k <= 32, 1 <= E <= 1024. workspace >=
+ * STRATA_GROUP_WORKSPACE_BYTES, 256-byte aligned (it holds the status word only).
+ */
+#define STRATA_GROUP_WORKSPACE_BYTES 256u
+strata_status strata_group_rows(const int32_t* ids, int64_t T, int32_t k, int32_t E,
+                                int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                                void* workspace, size_t ws_bytes, strata_stream stream);
+
+/*
  * One routed MoE FFN layer. Expert weights are the outputs of strata_quantize_groups, stacked
  * over experts; the shared expert, when has_shared != 0, is index E of each stack.
  * Expert e computes y = (silu(x Wg_e^T) * (x Wu_e^T)) Wd_e^T   ([glm-4090] §01: Gate/Up, Down).
@@ -221,6 +240,30 @@ size_t strata_moe_workspace_size(const strata_moe_layer* layer, int64_t T_max);
 strata_status strata_moe_forward(const strata_moe_layer* layer, const void* x_bf16, int64_t T,
                                  void* out_bf16, void* workspace, size_t ws_bytes,
                                  strata_stream stream);
+
+/*
+ * strata_moe_forward_padded — strata_moe_forward at a fixed maximum batch whose live token count
+ * is read on the device when the call runs, so that one CUDA graph captured at T_max serves every
+ * batch of 0..T_max tokens ([tuning-3090] §3.2: the grouped GEMM captured as a fixed graph node
+ * at a fixed maximum batch, smaller batches padded with empty tokens; §5.2: every buffer
+ * allocated before the graph is built).
+ * n_tokens  device int32, 4-byte aligned: T, the live tokens, rows 0..T-1 of x. It is read by the
+ *           call's first kernel, so a graph replays with whatever it holds at that point (write it
+ *           with a copy in stream order before the replay).
+ * x_bf16    [T_max, H] bf16 (device); rows T..T_max-1 are never read and may hold anything.
+ * out_bf16  [T_max, H] bf16 (device); rows 0..T-1 get exactly what strata_moe_forward gives for
+ *           those T tokens up to the order of its split-K sums (the contraction split is chosen
+ *           for T_max); rows T..T_max-1 are not written. The padding tokens route to no expert and
+ *           cost no weight traffic: every grid is sized for T_max, every loop stops at T.
+ * A count outside [0, T_max] sets STRATA_DEV_BAD_TOKENS in the device status word and the call
+ * then runs with no live token (out untouched).
+ * T_max: 1..64 (the fused decode router); 4-bit codes; not STRATA_FORCE_TC_PATH. Otherwise
+ * STRATA_ERR_UNSUPPORTED (T_max < 1: STRATA_ERR_SHAPE). workspace >=
+ * strata_moe_workspace_size(layer, T_max). Other errors as strata_moe_forward.
+ */
+strata_status strata_moe_forward_padded(const strata_moe_layer* layer, const void* x_bf16,
+                                        const int32_t* n_tokens, int64_t T_max, void* out_bf16,
+                                        void* workspace, size_t ws_bytes, strata_stream stream);
 
 /*
  * strata_moe_stack_forward — n_layers MoE layers in sequence with a residual add between them:
@@ -288,12 +331,29 @@ strata_status strata_moe_forward_host(const strata_moe_layer* layer, const void*
 
 /*
  * Device status of a route/forward workspace: synchronizes `stream`, returns the status word in
- * *status_out (host) and clears it. Returns STRATA_ERR_DEVICE_STATUS when any bit was set.
+ * *status_out (host) and clears it. Returns STRATA_ERR_TIMEOUT when STRATA_DEV_TIMEOUT was set (a
+ * bounded device wait gave up: the call's outputs are incomplete), else STRATA_ERR_DEVICE_STATUS
+ * when any other bit was set, else STRATA_OK.
  */
 strata_status strata_workspace_status(void* workspace, strata_stream stream, uint32_t* status_out);
 
 /* Same for a caller-owned device status word (e.g. the one given to strata_quantize_groups). */
 strata_status strata_read_status(uint32_t* dev_status, strata_stream stream, uint32_t* status_out);
+
+/*
+ * strata_selftest_bounded_waits — a diagnostic of the failure path of the library's two bounded
+ * device waits (no data path): the mbarrier wait of the TMA-fed grouped GEMMs and the counter
+ * spin of the fused router run, one after the other, on a barrier and a counter that nothing
+ * completes, each with a limit of limit_cycles SM clocks instead of its ~1-2 s. Each must give
+ * up, OR STRATA_DEV_TIMEOUT into dev_words[0] and return, so the kernel ends after about
+ * 2 * limit_cycles clocks and the context stays usable.
+ * dev_words  [4] uint32, device, 16-byte aligned, caller-zeroed: [0] status word (read it with
+ *            strata_read_status, which then returns STRATA_ERR_TIMEOUT), [1] the counter (must
+ *            stay 0), [2] / [3] set to 1 when the mbarrier wait / the counter spin gave up.
+ * limit_cycles 1 .. 4e9; outside -> STRATA_ERR_INVALID_ARG. Asynchronous on `stream`.
+ */
+strata_status strata_selftest_bounded_waits(uint32_t* dev_words, int64_t limit_cycles,
+                                            strata_stream stream);
 
 #ifdef __cplusplus
 }

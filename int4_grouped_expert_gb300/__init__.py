@@ -26,6 +26,10 @@ STRATA_FORCE_TC_PATH = 0x200
 STRATA_DEV_NONFINITE = 0x1
 STRATA_DEV_BAD_ID = 0x2
 STRATA_DEV_TIMEOUT = 0x4
+STRATA_DEV_BAD_TOKENS = 0x8
+STRATA_ERR_DEVICE_STATUS = 6
+STRATA_ERR_TIMEOUT = 7
+GROUP_WORKSPACE_BYTES = 256
 GROUP = 128
 
 
@@ -68,6 +72,10 @@ _SIGNATURES = {
                                                  _P, _P, _P, _P, _P, _P, _P]),
     "strata_moe_workspace_size": (_SZ, [ctypes.POINTER(strata_moe_layer), _I64]),
     "strata_moe_forward": (ctypes.c_int, [ctypes.POINTER(strata_moe_layer), _P, _I64, _P, _P, _SZ, _P]),
+    "strata_moe_forward_padded": (ctypes.c_int, [ctypes.POINTER(strata_moe_layer), _P, _P, _I64,
+                                                 _P, _P, _SZ, _P]),
+    "strata_group_rows": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
+    "strata_selftest_bounded_waits": (ctypes.c_int, [_P, _I64, _P]),
     "strata_moe_forward_ex": (ctypes.c_int, [ctypes.POINTER(strata_moe_layer), _P, _I64, _P,
                                              _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "strata_moe_forward_stats": (ctypes.c_int, [ctypes.POINTER(strata_moe_layer), _P, _I64, _P, _P,
@@ -179,6 +187,21 @@ def strata_moe_workspace_size(layer: strata_moe_layer, T_max: int) -> int:
 def strata_moe_forward(layer, x, T, out, workspace, ws_bytes, stream=None):
     return lib().strata_moe_forward(ctypes.byref(layer), ptr(x), T, ptr(out), ptr(workspace),
                                     ws_bytes, stream_handle(stream))
+
+
+def strata_moe_forward_padded(layer, x, n_tokens, T_max, out, workspace, ws_bytes, stream=None):
+    """n_tokens: a device int32 (tensor or pointer) holding the live token count."""
+    return lib().strata_moe_forward_padded(ctypes.byref(layer), ptr(x), ptr(n_tokens), T_max, ptr(out),
+                                           ptr(workspace), ws_bytes, stream_handle(stream))
+
+
+def strata_group_rows(ids, T, k, E, counts, offsets, perm, inv, workspace, ws_bytes, stream=None):
+    return lib().strata_group_rows(ptr(ids), T, k, E, ptr(counts), ptr(offsets), ptr(perm), ptr(inv),
+                                   ptr(workspace), ws_bytes, stream_handle(stream))
+
+
+def strata_selftest_bounded_waits(dev_words, limit_cycles, stream=None):
+    return lib().strata_selftest_bounded_waits(ptr(dev_words), limit_cycles, stream_handle(stream))
 
 
 def strata_moe_forward_stats(layer, x, T, out, expert_rows, workspace, ws_bytes, stream=None):

@@ -12,9 +12,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const int* __restrict__ inv,
                                                       const __nv_bfloat16* __restrict__ x, int T,
                                                       int H, int k, int has_shared, int R,
-                                                      int residual, __nv_bfloat16* __restrict__ out) {
+                                                      int residual, __nv_bfloat16* __restrict__ out,
+                                                      const int* __restrict__ T_dev) {
   griddep_wait();  // y comes from the down GEMM
   const int t = blockIdx.x;
+  if (T_dev) {  // a padded batch: only its live tokens have rows (routed rows first, then shared)
+    const int live = live_tokens(T_dev, T);
+    if (t >= live) return;
+    R = live * k;
+  }
   const int64_t H4 = H / 4;
   for (int64_t c = blockIdx.y * blockDim.x + threadIdx.x; c < H4; c += gridDim.y * blockDim.x) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -51,14 +57,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 
 cudaError_t launch_combine(const float* y, const float* gates, const int* inv, const void* x,
                            int64_t T, int64_t H, int k, int has_shared, int64_t R, int residual,
-                           void* out, cudaStream_t stream) {
+                           void* out, const int* T_dev, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   // one float4 of one token per thread: T x ceil(H / 1024) CTAs
   dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((H / 4 + 255) / 256));
   return launch_kernel(combine_kernel, grid, dim3(256), 0, stream, true, y, gates, inv,
                        static_cast<const __nv_bfloat16*>(x), static_cast<int>(T),
                        static_cast<int>(H), k, has_shared, static_cast<int>(R), residual,
-                       static_cast<__nv_bfloat16*>(out));
+                       static_cast<__nv_bfloat16*>(out), T_dev);
 }
 
 }  // namespace strata

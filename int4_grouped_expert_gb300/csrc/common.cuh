@@ -31,6 +31,28 @@ __device__ __forceinline__ void set_status(uint32_t* st, uint32_t bits) {
   if (st) atomicOr(st, bits);
 }
 
+// Spin until the device-scope counter reaches `target`, giving up after `limit` SM clocks: then
+// the status gets STRATA_DEV_TIMEOUT and the result is false.
+__device__ __forceinline__ bool spin_until_geq(const unsigned* ctr, unsigned target,
+                                               long long limit, uint32_t* status) {
+  const long long t0 = clock64();
+  while (*reinterpret_cast<const volatile unsigned*>(ctr) < target) {
+    __nanosleep(64);
+    if (clock64() - t0 > limit) {
+      set_status(status, STRATA_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Live tokens of a fixed-size batch whose count sits in device memory: the count itself when it
+// lies in [0, max], else 0 (the caller flags STRATA_DEV_BAD_TOKENS).
+__device__ __forceinline__ int live_tokens(const int* count, int max) {
+  const int t = *reinterpret_cast<const volatile int*>(count);
+  return (t >= 0 && t <= max) ? t : 0;
+}
+
 __device__ __forceinline__ uint32_t lane_id() {
   uint32_t l;
   asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));

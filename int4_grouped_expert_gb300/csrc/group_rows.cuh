@@ -139,6 +139,8 @@ __device__ void group_rows(const PermuteArgs& a, const int* ids, GroupSmem sm) {
         const int pos = hist[warp * E + e] + __popc(m & lt_mask);
         a.perm[pos] = r / a.k;
         a.inv[r] = pos;
+      } else {
+        a.inv[r] = -1;  // left out of every group
       }
       __syncwarp(active);
       if (e >= 0 && (m & lt_mask) == 0) hist[warp * E + e] += __popc(m);
@@ -361,7 +363,10 @@ __device__ void group_rows_small(const PermuteArgs& a, const int* ids, int* smem
 #pragma unroll 1
   for (int r = tid; r < R; r += NT) {
     const int e = ids[r];
-    if (e < 0 || e >= E) continue;
+    if (e < 0 || e >= E) {
+      a.inv[r] = -1;  // left out of every group
+      continue;
+    }
     const uint32_t* m = mask + e * MW;
     int pos = off[e] + __popc(m[r >> 5] & ((1u << (r & 31)) - 1u));
 #pragma unroll 1

@@ -87,7 +87,8 @@ struct RouteSmallArgs {
   const void* wr;          // [E, H] fp32, or fp16 with wr_fp16
   bool wr_fp16;
   const float* bias;       // [E] or null
-  int T, H, E, k;
+  int T, H, E, k;          // T: tokens, or the maximum when T_dev is set
+  const int* T_dev;        // optional device token count (live rows 0..*T_dev-1 of x), or null
   uint32_t flags;
   int epc;                 // experts per CTA (each split over 8 / epc warps along H)
   void* x_perm;            // [T, H]: x with every 8-wide chunk in (0,4,1,5,2,6,3,7) order, or null
@@ -136,8 +137,12 @@ strata_status check_route_args(const void* x_bf16, const void* w_router, int64_t
                                int32_t E, int32_t k, uint32_t flags, const int32_t* ids,
                                const float* gates, const int32_t* counts, const int32_t* offsets,
                                const int32_t* perm, const int32_t* inv);
+// T_dev (optional): the live token count on the device; T is then the maximum, R is taken as
+// live * k and rows of out beyond the live tokens are left untouched
+// selftest.cu: both bounded waits on things nothing completes (see strata_selftest_bounded_waits)
+cudaError_t launch_wait_selftest(uint32_t* words, long long limit, cudaStream_t stream);
 cudaError_t launch_combine(const float* y, const float* gates, const int* inv, const void* x,
                            int64_t T, int64_t H, int k, int has_shared, int64_t R, int residual,
-                           void* out, cudaStream_t stream);
+                           void* out, const int* T_dev, cudaStream_t stream);
 
 }  // namespace strata

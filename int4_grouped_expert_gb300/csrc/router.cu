@@ -162,6 +162,7 @@ __device__ void warp_softmax_topk(const float* lg, int64_t ld, int t0, int tstri
 // ----------------------------------------------------------------------------- decode: fused
 
 constexpr int kRsWarps = 8;
+constexpr long long kRouterWaitCycles = 2000000000ll;  // bound of the top-k CTAs' wait
 
 int route_small_epc(int E, int num_sms) {
   int epc = 1;  // experts per CTA: about one CTA per SM
@@ -187,7 +188,12 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   extern __shared__ __align__(16) unsigned char rs_smem[];
   __shared__ float red[kRsWarps][kRouteSmallMaxT];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = a.T, H = a.H, E = a.E;
+  // a.T sizes the launch and the shared memory; with a device token count (a fixed-size batch
+  // with padding) the live tokens are its first T, and a count outside [0, a.T] means none
+  const int T = a.T_dev ? live_tokens(a.T_dev, a.T) : a.T;
+  const int H = a.H, E = a.E;
+  if (a.T_dev && blockIdx.x == 0 && threadIdx.x == 0 && T != *a.T_dev)
+    set_status(a.grp.status, STRATA_DEV_BAD_TOKENS);
   griddep_launch();  // the gate/up GEMM may launch now; it waits for this grid before reading
   const int wpe = kRsWarps / a.epc;  // warps per expert
   const int slot = warp / wpe, part = warp - slot * wpe;
@@ -313,7 +319,8 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   // the others, take the top-k of their tokens, and the last of them groups the rows. With one
   // such CTA (T <= 8) the ids stay in its shared memory.
   __shared__ int role_s, arrival_s;
-  const int G = min(static_cast<int>(gridDim.x), (T + kRsWarps - 1) / kRsWarps);
+  // (at least one: with no live token it still writes the empty grouping the GEMMs read)
+  const int G = min(static_cast<int>(gridDim.x), max(1, (T + kRsWarps - 1) / kRsWarps));
   const int ncopy = static_cast<int>(gridDim.x) - G;  // CTAs outside the top-k
   if (a.x_perm && ncopy == 0) copy_x(blockIdx.x, gridDim.x);
   __threadfence();
@@ -322,19 +329,12 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
     const unsigned prev = atomicAdd(&a.grp.hdr->route_done, 1u);
     arrival_s = static_cast<int>(prev);
     int r = static_cast<int>(prev) - ncopy;
-    if (r >= 0 && prev != gridDim.x - 1) {
-      // wait (bounded, ~1 s) for the CTAs still writing logits: all of them run already (this
-      // grid's dependents launch only once every CTA of it has started)
-      const long long t0 = clock64();
-      while (*reinterpret_cast<volatile unsigned*>(&a.grp.hdr->route_done) < gridDim.x) {
-        __nanosleep(64);
-        if (clock64() - t0 > 2000000000ll) {
-          set_status(a.grp.status, STRATA_DEV_TIMEOUT);
-          r = -1;  // give up: no top-k from this CTA, the status tells the host
-          break;
-        }
-      }
-    }
+    // wait (bounded, ~1 s) for the CTAs still writing logits: all of them run already (this
+    // grid's dependents launch only once every CTA of it has started); on time-out this CTA
+    // gives up its top-k and the status tells the host
+    if (r >= 0 && prev != gridDim.x - 1 &&
+        !spin_until_geq(&a.grp.hdr->route_done, gridDim.x, kRouterWaitCycles, a.grp.status))
+      r = -1;
     role_s = r;
   }
   __syncthreads();
@@ -386,10 +386,12 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
     a.grp.hdr->topk_done = 0;
   }
   if (a.do_group) {
+    PermuteArgs g = a.grp;
+    g.T = T;
     if (route_small_compact_group(a))
-      group_rows_small<kRsWarps>(a.grp, s_ids, reinterpret_cast<int*>(rs_smem));
+      group_rows_small<kRsWarps>(g, s_ids, reinterpret_cast<int*>(rs_smem));
     else
-      group_rows<kRsWarps>(a.grp, s_ids, carve_group_smem(reinterpret_cast<int*>(rs_smem), kRsWarps, E));
+      group_rows<kRsWarps>(g, s_ids, carve_group_smem(reinterpret_cast<int*>(rs_smem), kRsWarps, E));
   }
 }
 

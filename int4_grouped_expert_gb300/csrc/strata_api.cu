@@ -7,6 +7,7 @@
 #include <algorithm>
 
 #include "kernels.cuh"
+#include "tc_ptx.cuh"
 
 namespace strata {
 
@@ -178,7 +179,8 @@ struct Taps {
 static strata_status run_forward(const strata_moe_layer* L, const void* x, int64_t T, void* out,
                                  const Taps* taps, void* ws, size_t ws_bytes, cudaStream_t st,
                                  void* const* events = nullptr, bool keep_status = false,
-                                 unsigned long long* hits = nullptr) {
+                                 unsigned long long* hits = nullptr,
+                                 const int32_t* T_dev = nullptr) {
   auto mark = [&](int i) -> bool {
     if (!events || !events[i]) return true;
     return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
@@ -195,6 +197,9 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
   if (!F.tc && !F.cta && layer_group(L) != STRATA_GROUP) return STRATA_ERR_UNSUPPORTED;
   // 8-bit codes run on the tensor-core kernel, which a forced warp path would bypass
   if (layer_bits(L) == 8 && (L->flags & STRATA_FORCE_WARP_PATH)) return STRATA_ERR_UNSUPPORTED;
+  // a device token count needs the fused decode router and the decode GEMMs (whose work lists
+  // are built on the device): T is then the maximum batch
+  if (T_dev && (T > kRouteSmallMaxT || F.tc || taps)) return STRATA_ERR_UNSUPPORTED;
   if (!ws || !aligned(ws, kAlign)) return STRATA_ERR_WORKSPACE;
   if (ws_bytes < F.total) return STRATA_ERR_WORKSPACE;
 
@@ -271,6 +276,7 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     ra.wr_fp16 = (L->flags & STRATA_ROUTER_FP16) != 0;
     ra.bias = L->bias;
     ra.T = static_cast<int>(T);
+    ra.T_dev = T_dev;
     ra.H = static_cast<int>(L->H);
     ra.E = E;
     ra.k = k;
@@ -383,7 +389,7 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
   }
 
   e = launch_combine(reinterpret_cast<const float*>(base + F.y), gates, inv, x, T, L->H, k, S, R,
-                     (L->flags & STRATA_ADD_RESIDUAL) ? 1 : 0, out, st);
+                     (L->flags & STRATA_ADD_RESIDUAL) ? 1 : 0, out, T_dev, st);
   if (e != cudaSuccess || !mark(5)) return STRATA_ERR_CUDA;
 
   if (taps) {
@@ -531,6 +537,15 @@ strata_status strata_moe_forward(const strata_moe_layer* layer, const void* x_bf
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
+strata_status strata_moe_forward_padded(const strata_moe_layer* layer, const void* x_bf16,
+                                        const int32_t* n_tokens, int64_t T_max, void* out_bf16,
+                                        void* workspace, size_t ws_bytes, strata_stream stream) {
+  if (!n_tokens || !aligned(n_tokens, 4)) return STRATA_ERR_INVALID_ARG;
+  if (T_max < 1) return STRATA_ERR_SHAPE;
+  return run_forward(layer, x_bf16, T_max, out_bf16, nullptr, workspace, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream), nullptr, false, nullptr, n_tokens);
+}
+
 strata_status strata_moe_forward_ex(const strata_moe_layer* layer, const void* x_bf16, int64_t T,
                                     void* out_bf16, int32_t* ids, float* gates, int32_t* counts,
                                     int32_t* offsets, int32_t* perm, int32_t* inv,
@@ -646,7 +661,44 @@ strata_status strata_read_status(uint32_t* dev_status, strata_stream stream, uin
   if (cudaMemsetAsync(dev_status, 0, sizeof(uint32_t), st) != cudaSuccess) return STRATA_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return STRATA_ERR_CUDA;
   *status_out = v;
-  return v ? STRATA_ERR_DEVICE_STATUS : STRATA_OK;
+  if (v == 0) return STRATA_OK;
+  return (v & STRATA_DEV_TIMEOUT) ? STRATA_ERR_TIMEOUT : STRATA_ERR_DEVICE_STATUS;
+}
+
+strata_status strata_group_rows(const int32_t* ids, int64_t T, int32_t k, int32_t E,
+                                int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                                void* workspace, size_t ws_bytes, strata_stream stream) {
+  if (T < 0 || T > kMaxTokens) return STRATA_ERR_SHAPE;
+  if (k < 1 || k > STRATA_MAX_TOPK || E < 1 || E > STRATA_MAX_EXPERTS) return STRATA_ERR_INVALID_ARG;
+  if (!counts || !offsets || (T > 0 && (!ids || !perm || !inv))) return STRATA_ERR_INVALID_ARG;
+  if ((ids && !aligned(ids, 4)) || !aligned(counts, 4) || !aligned(offsets, 4) ||
+      (perm && !aligned(perm, 4)) || (inv && !aligned(inv, 4)))
+    return STRATA_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, kAlign) || ws_bytes < STRATA_GROUP_WORKSPACE_BYTES)
+    return STRATA_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return STRATA_ERR_CUDA;
+  PermuteArgs pa{};
+  pa.ids = ids;
+  pa.T = static_cast<int>(T);
+  pa.k = k;
+  pa.E = E;
+  pa.counts = counts;
+  pa.offsets = offsets;
+  pa.perm = perm;
+  pa.inv = inv;
+  pa.hdr = hdr;
+  pa.status = &hdr->status;
+  return cuda_fail(launch_permute(pa, st));
+}
+
+strata_status strata_selftest_bounded_waits(uint32_t* dev_words, int64_t limit_cycles,
+                                            strata_stream stream) {
+  if (!dev_words || !aligned(dev_words, 16)) return STRATA_ERR_INVALID_ARG;
+  if (limit_cycles < 1 || limit_cycles > tc::kWaitCycles) return STRATA_ERR_INVALID_ARG;
+  return cuda_fail(launch_wait_selftest(dev_words, limit_cycles,
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 strata_status strata_workspace_status(void* workspace, strata_stream stream, uint32_t* status_out) {

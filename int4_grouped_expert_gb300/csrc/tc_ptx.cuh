@@ -38,18 +38,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait until the phase with `parity` completes, giving up after ~2 s (clock64 cycles at ~2 GHz).
-// On time-out the device status gets STRATA_DEV_TIMEOUT and the shared abort flag is raised, so
-// every role of the CTA leaves its loops.
+// Wait until the phase with `parity` completes, giving up after `limit` SM clocks (by default
+// ~2 s at ~2 GHz). On time-out the device status gets STRATA_DEV_TIMEOUT and the shared abort flag
+// is raised, so every role of the CTA leaves its loops.
 constexpr long long kWaitCycles = 4000000000ll;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* status) {
+                                          uint32_t* status, long long limit = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       set_status(status, STRATA_DEV_TIMEOUT);
       *abort_flag = 1;
       return false;

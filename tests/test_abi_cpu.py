@@ -136,3 +136,40 @@ def test_stack_host_checks(st):
     assert st.strata_moe_stack_forward(Ls, A, 4, 2 * A, A, need - 1) == 4
     assert st.strata_moe_stack_forward(Ls, A, 4, A, A, need) == 1
     assert st.strata_moe_stack_forward(Ls, A, 0, 2 * A, A, need) == 0
+
+
+def test_padded_forward_host_checks(st):
+    A = 1 << 12
+    L = layer(st)
+    need = st.strata_moe_workspace_size(L, 16)
+    assert st.strata_moe_forward_padded(L, A, None, 16, 2 * A, A, need) == 1       # no count
+    assert st.strata_moe_forward_padded(L, A, A + 2, 16, 2 * A, A, need) == 1      # misaligned
+    assert st.strata_moe_forward_padded(L, A, 3 * A, 0, 2 * A, A, need) == 2       # T_max < 1
+    big = st.strata_moe_workspace_size(L, 65)
+    assert st.strata_moe_forward_padded(L, A, 3 * A, 65, 2 * A, A, big) == 3       # > fused router
+    assert st.strata_moe_forward_padded(layer(st, flags=0x200), A, 3 * A, 16, 2 * A, A, need) == 3
+    assert st.strata_moe_forward_padded(layer(st, bits=8), A, 3 * A, 16, 2 * A, A, 1 << 30) == 3
+    assert st.strata_moe_forward_padded(L, A, 3 * A, 16, 2 * A, A, need - 1) == 4
+    assert st.strata_moe_forward_padded(L, A, 3 * A, 16, A, A, need) == 1          # out aliases x
+
+
+def test_group_rows_host_checks(st):
+    A = 1 << 12
+    W = st.GROUP_WORKSPACE_BYTES
+    assert st.strata_group_rows(A, -1, 8, 288, A, A, A, A, A, W) == 2
+    assert st.strata_group_rows(A, 4, 0, 288, A, A, A, A, A, W) == 1
+    assert st.strata_group_rows(A, 4, 33, 288, A, A, A, A, A, W) == 1
+    assert st.strata_group_rows(A, 4, 8, 1025, A, A, A, A, A, W) == 1
+    assert st.strata_group_rows(A, 4, 8, 288, None, A, A, A, A, W) == 1
+    assert st.strata_group_rows(A, 4, 8, 288, A, A, None, A, A, W) == 1
+    assert st.strata_group_rows(A + 2, 4, 8, 288, A, A, A, A, A, W) == 1
+    assert st.strata_group_rows(A, 4, 8, 288, A, A, A, A, A, W - 1) == 4
+    assert st.strata_group_rows(A, 4, 8, 288, A, A, A, A, A + 16, W) == 4
+
+
+def test_wait_selftest_host_checks(st):
+    A = 1 << 12
+    assert st.strata_selftest_bounded_waits(None, 1000) == 1
+    assert st.strata_selftest_bounded_waits(A + 4, 1000) == 1
+    assert st.strata_selftest_bounded_waits(A, 0) == 1
+    assert st.strata_selftest_bounded_waits(A, 5_000_000_000) == 1
