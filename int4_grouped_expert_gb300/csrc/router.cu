@@ -270,20 +270,13 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
       if (lane == 0 && t0 + tt < T) red[warp][t0 + tt] = v;
-      const uint32_t m = __reduce_max_sync(0xffffffffu, mag[tt]);
-      if (slot == 0 && lane == 0 && t0 + tt < T) xmag[part][t0 + tt] = m;
+      if (a.x_f16 && slot == 0) {
+        const uint32_t m = __reduce_max_sync(0xffffffffu, mag[tt]);
+        if (lane == 0 && t0 + tt < T) xmag[part][t0 + tt] = m;
+      }
     }
   }
   __syncthreads();
-  if (a.x_f16) {
-    for (int t = threadIdx.x; t < T; t += blockDim.x) {
-      uint32_t m = 0;
-      for (int p = 0; p < wpe; ++p) m = max(m, xmag[p][t]);
-      xexp_s[t] = range_exp(m);
-      if (blockIdx.x == 0 && a.xexp) a.xexp[t] = xexp_s[t];
-    }
-    __syncthreads();
-  }
   // the H slices of one expert, summed in slice order
   for (int i = threadIdx.x; i < a.epc * T; i += blockDim.x) {
     const int sl = i / T, t = i - sl * T;
@@ -299,6 +292,17 @@ __global__ void __launch_bounds__(256) route_small_kernel(RouteSmallArgs a) {
   // the copy, so the CTAs that do not take part in the top-k make it after signalling their logits
   // (off the top-k's path); with no such CTA every CTA copies first.
   auto copy_x = [&](int part, int nparts) {
+    if (a.x_f16) {
+      // each token's range exponent, from the magnitudes found by the expert-slot-0 warps; the
+      // copying CTA of part 0 publishes them for the GEMMs
+      for (int t = threadIdx.x; t < T; t += blockDim.x) {
+        uint32_t m = 0;
+        for (int p = 0; p < wpe; ++p) m = max(m, xmag[p][t]);
+        xexp_s[t] = range_exp(m);
+        if (part == 0 && a.xexp) a.xexp[t] = xexp_s[t];
+      }
+      __syncthreads();
+    }
     const int nv = T * (H / 8);
     for (int i = part * blockDim.x + threadIdx.x; i < nv; i += nparts * blockDim.x) {
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
