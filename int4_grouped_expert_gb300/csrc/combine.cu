@@ -14,22 +14,34 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       int H, int k, int has_shared, int R,
                                                       int residual, __nv_bfloat16* __restrict__ out,
                                                       const int* __restrict__ T_dev) {
-  griddep_wait();  // y comes from the down GEMM
+  // The token's routing (gates, rows) comes from the router, which completed before the GEMMs
+  // that precede this grid started, and x is the layer input: both are read before waiting for
+  // the down GEMM, so only the y rows are on the path after it.
+  __shared__ float s_gate[STRATA_MAX_TOPK];
+  __shared__ int s_row[STRATA_MAX_TOPK];
   const int t = blockIdx.x;
   if (T_dev) {  // a padded batch: only its live tokens have rows (routed rows first, then shared)
     const int live = live_tokens(T_dev, T);
     if (t >= live) return;
     R = live * k;
   }
+  if (threadIdx.x < k) {
+    const int64_t tk = static_cast<int64_t>(t) * k + threadIdx.x;
+    s_gate[threadIdx.x] = gates[tk];
+    s_row[threadIdx.x] = inv[tk];
+  }
   const int64_t H4 = H / 4;
-  for (int64_t c = blockIdx.y * blockDim.x + threadIdx.x; c < H4; c += gridDim.y * blockDim.x) {
+  const int64_t c0 = blockIdx.y * blockDim.x + threadIdx.x;
+  uint2 xres = make_uint2(0u, 0u);
+  if (residual && c0 < H4) xres = reinterpret_cast<const uint2*>(x + static_cast<int64_t>(t) * H)[c0];
+  __syncthreads();
+  griddep_wait();  // y comes from the down GEMM
+  for (int64_t c = c0; c < H4; c += gridDim.y * blockDim.x) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int64_t tk = static_cast<int64_t>(t) * k;
-    // rows and gates first, then all row loads: the k loads are independent
 #pragma unroll 8
     for (int j = 0; j < k; ++j) {
-      const float g = gates[tk + j];
-      const int row = inv[tk + j];
+      const float g = s_gate[j];
+      const int row = s_row[j];
       // a row outside the routed rows (the grouping skipped a bad expert id, or a timed-out
       // top-k left the buffer unwritten; both set a device status bit) contributes nothing
       if (row < 0 || row >= R) continue;
@@ -42,7 +54,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
     if (residual) {
-      const uint2 raw = reinterpret_cast<const uint2*>(x + static_cast<int64_t>(t) * H)[c];
+      const uint2 raw = c == c0 ? xres : reinterpret_cast<const uint2*>(x + static_cast<int64_t>(t) * H)[c];
       const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&raw);
       const float2 a = __bfloat1622float2(p[0]), b = __bfloat1622float2(p[1]);
       acc.x += a.x; acc.y += a.y; acc.z += b.x; acc.w += b.y;
