@@ -594,12 +594,33 @@ cudaError_t launch_gemm_cta(const GemmArgs& a, bool gate_up, int64_t experts, in
 
 // Contraction splits for a batch whose grouped GEMM has `items` (chunk x row block) work items:
 // enough for about two items per CTA, each split keeping at least two 128-wide groups.
+// Contraction splits per work item. An item streams K/128 stages of 16 KB; a split piece also
+// pays the cross-CTA reduction of its partial sums (a fence, an atomic and the loads of the other
+// splits' partials: about 3.5 stages' time, measured at the decode shapes). The persistent CTAs
+// take the pieces in rounds, so ks splits cost about rounds(ks) x (stages per piece + reduction),
+// rounds = ceil(items * ks / CTAs). Only counts that give every CTA a piece in the first round are
+// weighed (a CTA's stream rate is capped by its consumers, so idle CTAs lose bandwidth), unless no
+// count reaches that; the cheapest wins (the fewest splits on a tie), and a piece keeps at least
+// 2 stages.
 int cta_gemm_ksplit(int64_t items, int64_t K, int num_sms) {
-  const int64_t want = 2 * static_cast<int64_t>(num_sms) * kCtasPerSm;
+  const int64_t ctas = static_cast<int64_t>(num_sms) * kCtasPerSm;
   const int64_t groups = K / kBlockK;
-  int ks = 1;
-  while (items * ks < want && 2 * ks * 2 <= groups && ks < 16) ks *= 2;
-  return ks;
+  constexpr double kReduceStages = 3.5;
+  int ks_max = 1;
+  while (2 * ks_max <= 16 && groups >= 2 * (2 * ks_max)) ks_max *= 2;
+  int best = 0;
+  double best_cost = 0.0;
+  for (int ks = 1; ks <= ks_max; ks *= 2) {
+    if (items * ks < ctas && ks < ks_max) continue;  // leaves CTAs idle in the first round
+    const int64_t rounds = (items * ks + ctas - 1) / ctas;
+    const double cost = static_cast<double>(rounds) *
+                        (static_cast<double>(groups) / ks + (ks > 1 ? kReduceStages : 0.0));
+    if (best == 0 || cost < best_cost) {
+      best_cost = cost;
+      best = ks;
+    }
+  }
+  return best;
 }
 
 }  // namespace strata

@@ -17,12 +17,13 @@ FP32_MIN_NORMAL = 2.0 ** -126
 
 def gate_rtol(route):
     """Relative tolerance of each token's gates: no bound is stated for them, so it follows from
-    the arithmetic. A gate is exp(l_j - m) / sum exp(l_e - m) with fp32 logits; its relative error
-    is about the error of a logit difference, and a logit summed in fp32 from rounded products
-    errs by about u * ||x_t * w_e||_2 (random rounding errors). Ten times the largest of these
-    over the experts, never below GATE_RTOL: 1e-5 for N(0,1) activations, wider only where the
-    activations are large (deep layers of a residual stack without normalisation)."""
-    return np.maximum(GATE_RTOL, 10 * U32 * route["dot_l2"].max(axis=1))
+    the arithmetic. A logit summed in fp32 from rounded products errs by about u * ||x_t * w_e||_2
+    (random rounding errors; ten times that is the bound taken per logit). A gate is
+    exp(l_j - m) / sum_e exp(l_e - m): its relative error is the error of l_j minus the
+    probability-weighted mean of the errors of all l_e, so up to twice the logit bound. Never
+    below GATE_RTOL: 1e-5 for N(0,1) activations, wider only where the activations are large
+    (deep layers of a residual stack without normalisation)."""
+    return np.maximum(GATE_RTOL, 2 * 10 * U32 * route["dot_l2"].max(axis=1))
 
 
 def torch_mod():

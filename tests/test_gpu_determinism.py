@@ -5,8 +5,9 @@ persistent CTAs claim their work items in: the split-K reductions sum in a fixed
 routing and grouping are deterministic, and the ring of shared-memory stages must never hand a
 consumer a stage that the producer has begun to overwrite. That last property depends on the
 cross-proxy fence between the consumers' generic-proxy reads and the producer's next TMA box; a
-build without it gave a different output in about one forward in a hundred at the c4 shape below
-(split-K on both GEMMs), so each case runs hundreds of forwards.
+build without it gave a different output in about one forward in a hundred at the c4 shape
+(T=4), so each case runs hundreds of forwards. At one token both GEMMs split the contraction
+(the split-K reduction runs) on both the c2 and the c4 shapes.
 """
 import numpy as np
 import pytest
@@ -17,7 +18,8 @@ from workloads import CONFIGS, gen
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("key,T,n", [("c4", 4, 400), ("c2", 1, 200), ("c2", 16, 200)])
+@pytest.mark.parametrize("key,T,n", [("c4", 4, 400), ("c4", 1, 200), ("c2", 1, 200),
+                                     ("c2", 16, 200)])
 def test_repeated_forwards_are_bit_identical(key, T, n):
     import torch
     import int4_grouped_expert_gb300 as st
