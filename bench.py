@@ -142,10 +142,14 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- workload
 
 def build_layer(wl, threads=0, group=128, bits=4):
-    """One device layer quantized from the seeded fp16 experts (strata_quantize_groups_bits)."""
+    """One device layer quantized from the seeded fp16 experts (strata_quantize_groups_bits).
+    Its calls skip the per-call clearing of the workspace header (STRATA_WS_REUSE): every
+    workspace here is zero-filled once and then reused by completed calls only."""
     import torch
+    import int4_grouped_expert_gb300 as st
     from int4_grouped_expert_gb300 import MoELayer
-    L = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared, group=group, bits=bits)
+    L = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared, group=group, bits=bits,
+                 flags=st.STRATA_WS_REUSE)
     L.set_router(gen.router_weight(wl), gen.router_bias(wl))
     n = wl.E + wl.shared
     for s in range(0, n, 16):
@@ -181,7 +185,7 @@ def routed_experts(L, x_dev, T):
     """Distinct experts (incl. shared) the batch activates, read back from the GPU routing."""
     import torch
     import int4_grouped_expert_gb300 as st
-    ws = torch.empty(L.workspace_size(T), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(L.workspace_size(T), dtype=torch.uint8, device="cuda")
     out = torch.empty_like(x_dev)
     counts = torch.zeros(L.E, dtype=torch.int32, device="cuda")
     st.check(st.strata_moe_forward_ex(L.struct(), x_dev, T, out, counts=counts, workspace=ws,
@@ -265,7 +269,7 @@ def time_e2e(L, xs_host, T, steps, warmup, stream):
     import int4_grouped_expert_gb300 as st
     s = L.struct()
     need = st.strata_moe_workspace_size(s, T) + st.strata_moe_host_staging_size(s, T)
-    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     xh = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs_host]
     oh = torch.empty_like(xh[0]).pin_memory()
     for i in range(warmup):
@@ -373,7 +377,7 @@ def run_strata(args):
     stream = torch.cuda.Stream()
     xs_host, xs_dev = token_batches(wl, T, N_TOKEN_BATCHES)
     ws_bytes = L0.workspace_size(T)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
     out = torch.empty(T, wl.H, dtype=torch.bfloat16, device="cuda")
 
     # distinct activated experts per step (all batches): bytes the layer must stream
@@ -401,7 +405,7 @@ def run_strata(args):
         if Tb == T:
             continue
         xh_b, xd_b = token_batches(wl, Tb, N_TOKEN_BATCHES)
-        wsb = torch.empty(L0.workspace_size(Tb), dtype=torch.uint8, device="cuda")
+        wsb = torch.zeros(L0.workspace_size(Tb), dtype=torch.uint8, device="cuda")
         ob = torch.empty(Tb, wl.H, dtype=torch.bfloat16, device="cuda")
         eb_n = float(np.mean([routed_experts(L0, x, Tb) for x in xd_b]))
         ms, _ = time_steps(layers, xd_b, Tb, min(args.steps, 2000), args.warmup, stream, wsb,
@@ -434,6 +438,7 @@ def run_strata(args):
                    "router_weights": "fp16" if args.router_fp16 else "fp32",
                    "l2": f"inputs larger than L2: {N_LAYER_COPIES} expert-storage copies x "
                          f"{N_TOKEN_BATCHES} token batches rotated per step",
+                   "workspace": "zero-filled once, reused by every step (STRATA_WS_REUSE)",
                    "parallelism": f"replicas x{ws_n}"},
         "roofline": {"kernel": ("gate_up_gemm (grouped W4A16 GEMM + SiLU)" if args.bits == 4 else
                                 "gate_up_gemm (tcgen05 grouped W8A16 GEMM + SiLU)"),
@@ -526,7 +531,7 @@ def prefill_measure(key, steps, warmup, experts=0, tokens=0, router=None, host_w
         import dataclasses
         wl = dataclasses.replace(wl, E=experts)
     T = tokens or wl.batches[0]
-    L = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared)
+    L = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared, flags=st.STRATA_WS_REUSE)
     L.set_router(gen.router_weight(wl), gen.router_bias(wl, 0, router) if not experts else None)
     n = wl.E + wl.shared
     quant = None
@@ -585,7 +590,7 @@ def prefill_measure(key, steps, warmup, experts=0, tokens=0, router=None, host_w
         device_random_experts(L, wl.seed)
     xs_host, xs_dev = token_batches(wl, T, 2)
     ws_bytes = L.workspace_size(T)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
     out = torch.empty(T, wl.H, dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.Stream()
     clocks = ClockSampler(local)
@@ -700,12 +705,13 @@ def stack_measure(steps, warmup, batches, host_weights=False, local=0):
     if host_weights:
         L0 = build_layer(wl)
     else:
-        L0 = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared)
+        L0 = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared, flags=st.STRATA_WS_REUSE)
         L0.set_router(gen.router_weight(wl), gen.router_bias(wl))
         device_random_experts(L0, wl.seed)
     layers = [L0]
     for l in range(1, wl.layers):
-        L = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared, flags=st.STRATA_ADD_RESIDUAL)
+        L = MoELayer(wl.H, wl.I, wl.E, wl.k, wl.shared,
+                     flags=st.STRATA_ADD_RESIDUAL | st.STRATA_WS_REUSE)
         L.set_router(gen.router_weight(wl, l), gen.router_bias(wl, l))
         L.copy_expert_from(L0)
         layers.append(L)
@@ -719,7 +725,7 @@ def stack_measure(steps, warmup, batches, host_weights=False, local=0):
     for T in batches:
         xs_host, xs_dev = token_batches(wl, T, N_TOKEN_BATCHES)
         need = st.strata_moe_stack_workspace_size(structs, T)
-        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
         out = torch.empty(T, wl.H, dtype=torch.bfloat16, device="cuda")
         # distinct experts each layer streams: route the layer-by-layer activations
         n_exp = []
@@ -727,7 +733,7 @@ def stack_measure(steps, warmup, batches, host_weights=False, local=0):
         for L in layers:
             nxt = torch.empty_like(cur)
             counts = torch.zeros(wl.E, dtype=torch.int32, device="cuda")
-            wsl = torch.empty(L.workspace_size(T), dtype=torch.uint8, device="cuda")
+            wsl = torch.zeros(L.workspace_size(T), dtype=torch.uint8, device="cuda")
             st.check(st.strata_moe_forward_ex(L.struct(), cur, T, nxt, counts=counts,
                                               workspace=wsl, ws_bytes=wsl.numel()), "forward_ex")
             n_exp.append(int((counts.cpu().numpy() > 0).sum()) + wl.shared)
@@ -753,7 +759,7 @@ def stack_measure(steps, warmup, batches, host_weights=False, local=0):
         ms = max_over_ranks(e0.elapsed_time(e1)) / steps
         graph_us = stack_graph_us(structs, xs_dev, T, out, ws, need, steps, warmup)
         # per-stage times of single layers (events between the kernels), same inputs and layers
-        wsl = torch.empty(max(L.workspace_size(T) for L in layers), dtype=torch.uint8, device="cuda")
+        wsl = torch.zeros(max(L.workspace_size(T) for L in layers), dtype=torch.uint8, device="cuda")
         _, stages = time_steps(layers, xs_dev, T, min(steps, 400), warmup, stream, wsl,
                                wsl.numel(), out, profiled=True)
         st_bytes = float(sum(n_exp)) * eb
@@ -823,7 +829,7 @@ def padded_graph_measure(layers, wl, T_max, batches, steps, warmup):
     xs_host, _ = token_batches(wl, T_max, 1)
     x_static = torch.from_numpy(xs_host[0].view(np.int16)).view(torch.bfloat16).cuda()
     out = torch.empty_like(x_static)
-    ws = torch.empty(max(L.workspace_size(T_max) for L in layers), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(max(L.workspace_size(T_max) for L in layers), dtype=torch.uint8, device="cuda")
     structs = [L.struct() for L in layers]
     side = torch.cuda.Stream()
     with torch.cuda.stream(side):  # first calls outside the capture (one-time host set-up)

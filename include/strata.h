@@ -68,6 +68,13 @@ typedef enum {
    tensor-core path from 128 tokens up, the warp path below). For tests and tuning. */
 #define STRATA_FORCE_WARP_PATH 0x100u /* mma.sync warp GEMMs, B from registers */
 #define STRATA_FORCE_TC_PATH 0x200u   /* tcgen05 / TMEM GEMMs fed by TMA */
+/* Forward entry points: the caller promises that the workspace is zero-filled or was last used by
+   a completed forward call (of any layer) that reported no device timeout. The per-call clearing
+   of the workspace header (one memset between the previous kernel and the router) is then
+   skipped; the device status word is not cleared per call either, but accumulates until
+   strata_workspace_status reads (and clears) it. After a call that timed out, zero the workspace
+   again before reusing it with this flag. */
+#define STRATA_WS_REUSE 0x8u
 
 /* Bits of the device status word. */
 #define STRATA_DEV_NONFINITE 0x1u /* a quantized group held inf/nan (its scale is written as NaN,
@@ -211,7 +218,7 @@ typedef struct {
   int32_t k;             /* experts per token, 1..min(E, 32) */
   int32_t has_shared;    /* 0 or 1: expert E is always on, gate 1 */
   uint32_t flags;        /* STRATA_RENORM | STRATA_ADD_RESIDUAL | STRATA_ROUTER_FP16 |
-                            STRATA_FORCE_*_PATH */
+                            STRATA_FORCE_*_PATH | STRATA_WS_REUSE */
   const float* w_router; /* [E, H] fp32, or fp16 with STRATA_ROUTER_FP16 (cast the pointer) */
   const float* bias;     /* [E] fp32 or NULL */
   const uint8_t* gate_codes; const void* gate_scales; /* [E+S, I, H/2] u8, [E+S, I, H/128] fp16 */

@@ -23,6 +23,7 @@ STRATA_ADD_RESIDUAL = 0x2
 STRATA_ROUTER_FP16 = 0x4
 STRATA_FORCE_WARP_PATH = 0x100
 STRATA_FORCE_TC_PATH = 0x200
+STRATA_WS_REUSE = 0x8
 STRATA_DEV_NONFINITE = 0x1
 STRATA_DEV_BAD_ID = 0x2
 STRATA_DEV_TIMEOUT = 0x4

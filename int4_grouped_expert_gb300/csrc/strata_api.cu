@@ -153,7 +153,7 @@ static strata_status check_layer(const strata_moe_layer* L) {
   if (L->E < 1 || L->E + L->has_shared > STRATA_MAX_EXPERTS) return STRATA_ERR_UNSUPPORTED;
   if (L->k < 1 || L->k > L->E || L->k > STRATA_MAX_TOPK) return STRATA_ERR_INVALID_ARG;
   if (L->flags & ~(STRATA_RENORM | STRATA_ADD_RESIDUAL | STRATA_ROUTER_FP16 | STRATA_FORCE_WARP_PATH |
-                   STRATA_FORCE_TC_PATH))
+                   STRATA_FORCE_TC_PATH | STRATA_WS_REUSE))
     return STRATA_ERR_INVALID_ARG;
   if ((L->flags & STRATA_FORCE_WARP_PATH) && (L->flags & STRATA_FORCE_TC_PATH))
     return STRATA_ERR_INVALID_ARG;
@@ -218,11 +218,16 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
 
   if (!mark(0)) return STRATA_ERR_CUDA;
   // keep_status: a later layer of a stack clears the counters but keeps the status word, so a
-  // fault flagged by any layer stays visible after the whole stack
-  const size_t clear_from = keep_status ? sizeof(hdr->status) : 0;
-  cudaError_t e = cudaMemsetAsync(reinterpret_cast<char*>(hdr) + clear_from, 0,
-                                  sizeof(WsHeader) - clear_from, st);
-  if (e != cudaSuccess) return STRATA_ERR_CUDA;
+  // fault flagged by any layer stays visible after the whole stack. STRATA_WS_REUSE: the header
+  // is zero or as the last completed call left it (the fused router resets its counters as it
+  // ends), so no clearing op runs between the previous kernel and this call's first one.
+  cudaError_t e = cudaSuccess;
+  if (!(L->flags & STRATA_WS_REUSE)) {
+    const size_t clear_from = keep_status ? sizeof(hdr->status) : 0;
+    e = cudaMemsetAsync(reinterpret_cast<char*>(hdr) + clear_from, 0,
+                        sizeof(WsHeader) - clear_from, st);
+    if (e != cudaSuccess) return STRATA_ERR_CUDA;
+  }
 
   PermuteArgs pa{};
   pa.ids = ids;

@@ -86,7 +86,7 @@ def test_workspace_sizes(st):
 
 
 @pytest.mark.parametrize("kw,expect", [(dict(H=1000), 2), (dict(I=100), 2), (dict(k=9, E=8), 1),
-                                       (dict(k=33, E=64), 1), (dict(E=0), 3), (dict(flags=8), 1),
+                                       (dict(k=33, E=64), 1), (dict(E=0), 3), (dict(flags=0x10), 1),
                                        (dict(has_shared=2), 1), (dict(gate_codes=None), 1),
                                        (dict(up_codes=(1 << 12) + 8), 1), (dict(bits=3), 3),
                                        (dict(bits=8, flags=0x100), 3)])

@@ -173,6 +173,30 @@ def test_tc_path_shared_expert_and_long_segments():
     check_layer(wl, L, wr, b, gen.activations(600, wl.H, 8))
 
 
+@pytest.mark.parametrize("key,T", [("c2", 1), ("c2", 16), ("c1", 64), ("c1", 200)])
+def test_workspace_reuse_flag(key, T):
+    """STRATA_WS_REUSE: on a zero-filled workspace the calls skip the clearing of its header and
+    give the default call's bits, call after call (the fused router resets its counters as it
+    ends); the status word is not cleared per call but stays 0 here. 200 tokens take the
+    multi-launch router and the tensor-core GEMMs."""
+    import torch
+    import int4_grouped_expert_gb300 as st
+    wl, L, wr, b = layer_for(key)
+    xb = gen.activations(T, wl.H, wl.seed, name=f"reuse/{T}")
+    ref = run_forward(L, xb, taps=False)["out"]
+    s = L.struct()
+    s.flags |= st.STRATA_WS_REUSE
+    x = bf16_tensor(xb)
+    ws = torch.zeros(L.workspace_size(T), dtype=torch.uint8, device="cuda")
+    outs = torch.empty((6, T, wl.H), dtype=torch.bfloat16, device="cuda")
+    for i in range(6):
+        st.check(st.strata_moe_forward(s, x, T, outs[i], ws, ws.numel()), "forward")
+    torch.cuda.synchronize()
+    for i in range(6):
+        np.testing.assert_array_equal(bf16_to_np_bits(outs[i]), ref)
+    assert st.strata_workspace_status(ws) == (0, 0)
+
+
 def test_expert_statistics_accumulate_across_calls():
     """strata_moe_forward_stats adds each batch's routed rows per expert (and T for the shared
     expert) into a caller-owned counter array (the per-expert activation counts of "Strata" 3090
