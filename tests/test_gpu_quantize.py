@@ -171,3 +171,17 @@ def test_8bit_zero_groups_and_argument_errors():
     assert st.strata_quantize_groups_bits(w, 4, 256, c, s, bits=2) == 3          # UNSUPPORTED
     assert st.strata_quantize_groups_bits(w, 4, 200, c, s, bits=8) == 2          # SHAPE
     assert st.strata_quantize_groups_bits(w, 0, 256, c, s, bits=8) == 0          # empty
+
+
+@pytest.mark.parametrize("group", [64, 128, 256])
+def test_subnormal_scales_take_the_clamp(group):
+    """Groups whose absmax is a few subnormal steps (2^-24): the scale rounds coarsely to a
+    subnormal fp16 and the clamp to [-8, 7] decides the ends (the kernel's exact-quotient branch
+    for scales below the smallest normal fp16), beside ordinary groups in the same rows."""
+    rng = np.random.default_rng(group)
+    n, k = 6, 4 * group
+    steps = rng.integers(-12, 13, (n, k)).astype(np.float64)
+    w = (steps * 2.0 ** -24).astype(np.float16)
+    w[:, group:2 * group] = (rng.standard_normal((n, group)) * 0.02).astype(np.float16)
+    for bits in (4, 8):
+        assert_same(w, group=group, bits=bits)

@@ -425,3 +425,22 @@ def test_f16_quotient_reading_on_exact_rational_half_ties():
         assert exact[5] == q_exact and exact[9] == -q_exact
         assert lit[5] == q_lit and lit[9] == -q_lit
         assert exact[0] == lit[0] == 7
+
+
+def test_subnormal_scale_takes_the_clamp():
+    """A group with absmax 10 * 2^-24 (a subnormal fp16) has absmax / 7 = 1.43 * 2^-24, which rounds
+    to the scale 2^-24: the quotients are then the integers w / 2^-24 themselves, and the sketch's
+    clamp to [-8, 7] decides the ends (+10 -> 7, -10 -> -8). With 8-bit codes (divisor 127) the
+    scale 10/127 * 2^-24 rounds to 0 and every code is 0."""
+    tiny = 2.0 ** -24
+    vals = np.array([10, -10, 3, -3, 7, -8, 9, 0] * 16, dtype=np.float64) * tiny
+    w = vals.astype(np.float16).reshape(1, 128)
+    assert np.array_equal(w.astype(np.float64).ravel(), vals)        # exact in fp16
+    codes, scales = oracle.quantize_groups(w)
+    assert float(scales[0, 0]) == tiny
+    q = oracle.unpack_codes(codes).astype(np.int64).ravel()
+    expect = np.clip(np.array([10, -10, 3, -3, 7, -8, 9, 0] * 16), -8, 7)
+    np.testing.assert_array_equal(q, expect)
+    codes8, scales8 = oracle.quantize_groups(w, bits=8)
+    assert float(scales8[0, 0]) == 0.0
+    assert not np.asarray(codes8).any()
