@@ -9,9 +9,9 @@
 //   warp 1       MMA issuer: one thread issues tcgen05.mma (M=128, N=rows, K=16) into TMEM
 //   warp 2       owns the TMEM allocation
 //   warp 3       small tiles only: TMA producer of the int4 code tiles (a deep ring of stages)
-//   warps 4..11  dequant producers: int4 codes -> f16(q*s) written in the same swizzled K-major
-//                layout (the A operand)
-//   warps 12..15 epilogue: TMEM -> registers -> global
+//   warps 4..    dequant producers (16 warps for 256-row gate/up tiles, 8 otherwise): int4
+//                codes -> f16(q*s) written in the same swizzled K-major layout (the A operand)
+//   last 4 warps epilogue: TMEM -> registers -> global
 // Two tile widths: kN = 256 token rows for segments with many rows (the dequant warps load their
 // codes from global memory themselves, four stages ahead in registers), and kN = 64 for batches
 // with few rows per expert. There the shared memory the wide B tiles would take holds a ring of
@@ -42,7 +42,7 @@ namespace strata {
 
 constexpr int kTcBM = 128;       // weight rows per tile (MMA M)
 constexpr int kTcBK = 64;        // contraction per stage: one 128-byte swizzle row of f16
-constexpr int kTcThreads = 512;  // 16 warps
+
 
 #ifndef STRATA_TC_SMALL_STAGES_GU
 #define STRATA_TC_SMALL_STAGES_GU 3
@@ -67,6 +67,10 @@ struct TcCfg {
   static constexpr int BOX_BYTES = BOX_ROWS * kTcBK * 2;
   static constexpr int NMAT = kGateUp ? 2 : 1;
   static constexpr int STAGE_BYTES = NMAT * A_BYTES + B_BYTES;
+  // dequant producer warps: 16 for the 256-row gate/up tiles, whose stage conversion (two
+  // matrices) is the kernel's critical chain; 8 elsewhere (more were slower there)
+  static constexpr int DQW = (kGateUp && !RING) ? 16 : 8;
+  static constexpr int THREADS = (4 + DQW + 4) * 32;  // + 4 role warps + 4 epilogue warps
   // ring slot: the codes of SLOT_K consecutive stages (128 bytes of every weight row, one TMA box
   // of 128 rows per matrix, 128-byte swizzle): four stages of 4-bit codes or two of 8-bit ones
   static constexpr int STAGE_CODE_BYTES = kTcBK * kBits / 8;  // bytes of one row per stage
@@ -136,7 +140,7 @@ __device__ __forceinline__ void codes8_scaled(uint32_t w, float s, float* v) {
 __device__ __forceinline__ int pair_pos(int i) { return i < 4 ? 2 * i : 2 * (i - 4) + 1; }
 
 template <bool kGateUp, int kN, int kBits>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__((TcCfg<kGateUp, kN, kBits>::THREADS), 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_b,
                            const __grid_constant__ CUtensorMap tmap_c0,
                            const __grid_constant__ CUtensorMap tmap_c1, TcArgs a) {
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* acc_empty = bars + 3 * ST + 2;  // [2]
   uint64_t* drain = bars + 3 * ST + 4;      // abort path: completion of the issued MMAs
   uint64_t* cfull = bars + 3 * ST + 5;      // [RS] code slot landed
-  uint64_t* cempty = cfull + RS;            // [RS] code slot read by the 8 dequant warps
+  uint64_t* cempty = cfull + RS;            // [RS] code slot read by the dequant warps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cempty + RS);
   __shared__ int abort_flag_s;
   volatile int* abort_flag = &abort_flag_s;
@@ -164,7 +168,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < ST; ++s) {
-      tc::mbar_init(full_a + s, 8);
+      tc::mbar_init(full_a + s, C::DQW);
       tc::mbar_init(full_b + s, 1);
       tc::mbar_init(empty + s, 1);
     }
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::mbar_init(drain, 1);
     for (int s = 0; s < C::RING_STAGES; ++s) {
       tc::mbar_init(cfull + s, 1);
-      tc::mbar_init(cempty + s, 8);
+      tc::mbar_init(cempty + s, C::DQW);
     }
     tc::fence_barrier_init();
     abort_flag_s = 0;
@@ -303,20 +307,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::mbar_wait_drain(cfull + (j % RS), (j / RS) & 1);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp >= 4 && warp < 4 + C::DQW) {
     // ------------------------------------------------------------------ dequant producers
-    const int pt = threadIdx.x - 128;  // 0..255
-    const int mat = kGateUp ? (pt >> 7) : 0;
-    const int half = kGateUp ? 0 : (pt >> 7);
-    const int r = pt & 127;
+    // SUBS threads per weight row and matrix, each converting CPT of the stage's eight 8-code
+    // chunks: 16 warps on 256-row gate/up tiles (2 x 4 chunks), 8 warps elsewhere (gate/up
+    // 1 x 8, down 2 x 4)
+    constexpr int SUBS = (C::DQW * 32) / (C::NMAT * kTcBM);  // threads per row
+    constexpr int CPT = 8 / SUBS;                              // chunks per thread and stage
+    constexpr int TB = kBits * CPT;       // bytes of codes per thread and stage: 8 .. 64
+    constexpr int NV = TB >= 16 ? TB / 16 : 1;  // 16-byte vectors of them (8 bytes: one half)
+    const int pt = threadIdx.x - 128;
+    const int sub = pt % SUBS;
+    const int rr = pt / SUBS;             // gate/up: matrix x 128 + row; down: row
+    const int mat = kGateUp ? (rr >> 7) : 0;
+    const int r = rr & 127;
     const uint8_t* codes = mat ? a.codes1 : a.codes0;
     const __half* scales = mat ? a.scales1 : a.scales0;
-    const int64_t row_bytes = a.K / 2;
+    const int64_t row_bytes = static_cast<int64_t>(a.K) * kBits / 8;
     const int64_t srow = a.K / a.group;
     // scale of stage kb (64 codes): group (64 kb) / G
     const int gs = a.group == 64 ? 0 : a.group == 128 ? 1 : 2;
-    // ring: this thread's weight row inside a slot; a stage is 32 bytes (two 16-byte chunks) of
-    // it, chunk c stored at c ^ (r % 8) (128-byte swizzle)
+    // ring: this thread's weight row inside a slot (128 bytes: SLOT_K stages, 16-byte chunks
+    // swizzled as c ^ (r % 8))
     const int roff = (kGateUp ? mat * (C::CODE_BYTES / 2) : 0) + r * 128;
     int it = 0, cit = 0;
     bool ok = true;
@@ -324,25 +336,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       TcTile t;
       tc_decode<kN>(a, item, nseg, mtiles, t);
       const int64_t wrow = static_cast<int64_t>(t.e) * a.Nw + t.mt * kTcBM + r;
-      const uint8_t* cp = codes + wrow * row_bytes + half * 16;
+      const uint8_t* cp = codes + wrow * row_bytes + sub * TB;
       const __half* sp = scales + wrow * srow;
       const uint32_t soff = (r >> 3) * 1024 + (r & 7) * 128;
       // codes (and scales) of the next 4 stages stay in flight in fixed register slots: the loop
       // is unrolled by 4 so slot u is refilled for stage kb + 4 right after stage kb used it
+      // (the 256-row kernel; the 64-row kernel reads its codes from the TMA ring)
       constexpr int PD = 4;
-      uint4 cA[PD], cB[PD];
+      constexpr int NVG = C::RING ? 1 : NV;  // register vectors of the global-load path
+      uint4 cA[PD][NVG];
       // scale of stage kb's group, kept as raw fp16 bits: converting on load would make the load
       // complete right away
       unsigned short sc[PD];
-      auto ld = [&](int kb, uint4& x0, uint4& x1) {
+      auto ld = [&](int kb, uint4 (&x)[NVG]) {
         if (!C::RING && kb < nk) {
-          x0 = __ldg(reinterpret_cast<const uint4*>(cp + static_cast<int64_t>(kb) * 32));
-          if (kGateUp) x1 = __ldg(reinterpret_cast<const uint4*>(cp + static_cast<int64_t>(kb) * 32 + 16));
+          const uint8_t* src = cp + static_cast<int64_t>(kb) * (kTcBK * kBits / 8);
+          if (TB >= 16) {
+#pragma unroll
+            for (int v = 0; v < NVG; ++v) x[v] = __ldg(reinterpret_cast<const uint4*>(src) + v);
+          } else {
+            const uint2 h = __ldg(reinterpret_cast<const uint2*>(src));
+            x[0] = make_uint4(h.x, h.y, 0u, 0u);
+          }
         }
       };
 #pragma unroll
       for (int u = 0; u < PD; ++u) {
-        ld(u, cA[u], cB[u]);
+        ld(u, cA[u]);
         if (u < nk) sc[u] = __ldg(reinterpret_cast<const unsigned short*>(sp) + (u >> gs));
       }
       for (int kb0 = 0; ok && kb0 < nk; kb0 += PD) {
@@ -356,8 +376,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const __half sh = __ushort_as_half(sc[u]);
           const __half2 s2 = __halves2half2(sh, sh);
           const float sf = __half2float(sh);
-          uint4 x0 = cA[u], x1 = cB[u];
-          uint4 x8[4];  // 8-bit codes of the stage: gate/up 64 bytes of the row, down 32 of its half
+          uint4 xv[NV];
           if (C::RING) {
             const int cs = cit % RS;
             const int ks = kb % C::SLOT_K;
@@ -366,16 +385,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               break;
             }
             const uint8_t* src = ring + cs * C::CODE_BYTES + roff;
-            if (kBits == 8) {
+            // byte offset of this thread's piece inside the slot row (unswizzled), then the
+            // 16-byte chunk it starts in and the offset inside that chunk
+            const int boff = ks * (kTcBK * kBits / 8) + sub * TB;
+            const int ch = boff >> 4, inb = boff & 15;
+            if (TB >= 16) {
 #pragma unroll
-              for (int c = 0; c < (kGateUp ? 4 : 2); ++c) {
-                const int lc = 4 * ks + (kGateUp ? c : 2 * half + c);
-                x8[c] = *reinterpret_cast<const uint4*>(src + ((lc ^ (r & 7)) << 4));
-              }
+              for (int v = 0; v < NV; ++v)
+                xv[v] = *reinterpret_cast<const uint4*>(src + (((ch + v) ^ (r & 7)) << 4));
             } else {
-              const int c0 = 2 * ks + (kGateUp ? 0 : half);
-              x0 = *reinterpret_cast<const uint4*>(src + ((c0 ^ (r & 7)) << 4));
-              if (kGateUp) x1 = *reinterpret_cast<const uint4*>(src + (((c0 + 1) ^ (r & 7)) << 4));
+              const uint2 h = *reinterpret_cast<const uint2*>(src + ((ch ^ (r & 7)) << 4) + inb);
+              xv[0] = make_uint4(h.x, h.y, 0u, 0u);
             }
             if (ks == C::SLOT_K - 1 || kb == nk - 1) {
               __syncwarp();
@@ -383,45 +403,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               ++cit;
             }
           } else {
-            ld(kb + PD, cA[u], cB[u]);
+#pragma unroll
+            for (int v = 0; v < NV; ++v) xv[v] = cA[u][v < NVG ? v : 0];
+            ld(kb + PD, cA[u]);
           }
           if (kb + PD < nk)
             sc[u] = __ldg(reinterpret_cast<const unsigned short*>(sp) + ((kb + PD) >> gs));
           if (!tc::mbar_wait(empty + s, ph ^ 1, abort_flag, a.status)) { ok = false; break; }
           uint8_t* dst = A_of(s, mat) + soff;
+          // the codes as words: 4-bit one word per 8-code chunk, 8-bit two
+          uint32_t wd[4 * NV];
+#pragma unroll
+          for (int v = 0; v < NV; ++v) {
+            wd[4 * v] = xv[v].x; wd[4 * v + 1] = xv[v].y; wd[4 * v + 2] = xv[v].z; wd[4 * v + 3] = xv[v].w;
+          }
           if (kBits == 8) {
             // 8 codes (bytes m0..m7, natural order) per chunk -> f16 pairs (m0,m4) (m1,m5)
             // (m2,m6) (m3,m7); q * s is exact in fp32 and rounded once to f16
-            const uint32_t wds8[16] = {x8[0].x, x8[0].y, x8[0].z, x8[0].w, x8[1].x, x8[1].y,
-                                       x8[1].z, x8[1].w, x8[2].x, x8[2].y, x8[2].z, x8[2].w,
-                                       x8[3].x, x8[3].y, x8[3].z, x8[3].w};
 #pragma unroll
-            for (int j = 0; j < (kGateUp ? 8 : 4); ++j) {
+            for (int j = 0; j < CPT; ++j) {
               float v[8];
-              codes8_scaled(wds8[2 * j], sf, v);
-              codes8_scaled(wds8[2 * j + 1], sf, v + 4);
+              codes8_scaled(wd[2 * j], sf, v);
+              codes8_scaled(wd[2 * j + 1], sf, v + 4);
               uint4 o;
               o.x = f32x2_to_f16x2_sat(v[0], v[4]);
               o.y = f32x2_to_f16x2_sat(v[1], v[5]);
               o.z = f32x2_to_f16x2_sat(v[2], v[6]);
               o.w = f32x2_to_f16x2_sat(v[3], v[7]);
-              const int chunk = kGateUp ? j : (half * 4 + j);
+              const int chunk = sub * CPT + j;
               *reinterpret_cast<uint4*>(dst + ((chunk ^ (r & 7)) << 4)) = o;
             }
           } else {
-          const uint32_t wds[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-          for (int j = 0; j < (kGateUp ? 8 : 4); ++j) {
-            const uint32_t w = wds[j];
-            uint4 o;
-            o.x = scale_pair(codes_pair_f16(w, 0), s2);
-            o.y = scale_pair(codes_pair_f16(w, 1), s2);
-            o.z = scale_pair(codes_pair_f16(w, 2), s2);
-            o.w = scale_pair(codes_pair_f16(w, 3), s2);
-            const int chunk = kGateUp ? j : (half * 4 + j);
-            *reinterpret_cast<uint4*>(dst + ((chunk ^ (r & 7)) << 4)) = o;
+            for (int j = 0; j < CPT; ++j) {
+              const uint32_t w = wd[j];
+              uint4 o;
+              o.x = scale_pair(codes_pair_f16(w, 0), s2);
+              o.y = scale_pair(codes_pair_f16(w, 1), s2);
+              o.z = scale_pair(codes_pair_f16(w, 2), s2);
+              o.w = scale_pair(codes_pair_f16(w, 3), s2);
+              const int chunk = sub * CPT + j;
+              *reinterpret_cast<uint4*>(dst + ((chunk ^ (r & 7)) << 4)) = o;
+            }
           }
-          }  // 4-bit
           tc::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(full_a + s);
@@ -431,7 +455,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!ok) break;
     }
     __syncwarp();
-  } else if (warp >= 12) {
+  } else if (warp >= 4 + C::DQW) {
     // ------------------------------------------------------------------ epilogue
     const int q4 = warp & 3;  // TMEM lane quarter of this warp
     int tcount = 0;
@@ -447,20 +471,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::tc_fence_after();
       const int irow = t.mt * kTcBM + q4 * 32 + lane;  // weight row = output column
       const uint32_t lane_addr = tmem + buf * C::ACC_COLS + (static_cast<uint32_t>(q4 * 32) << 16);
-      for (int c = 0; c < t.nmma; c += 32) {
-        uint32_t g[32];
-        tc::tmem_ld32(lane_addr + c, g);
+      // 16 token columns at a time (the registers of 768-thread CTAs are few)
+      for (int c = 0; c < t.nmma; c += 16) {
+        uint32_t g[16];
+        tc::tmem_ld16(lane_addr + c, g);
         // range exponents of this chunk's token rows (the B rows were stored times 2^-e)
-        const int n_here = min(32, t.nvalid - c);
+        const int n_here = min(16, t.nvalid - c);
         const int my_e = (a.aexp && lane < n_here) ? a.aexp[t.row0 + c + lane] : 0;
         if (kGateUp) {
-          uint32_t u[32];
-          tc::tmem_ld32(lane_addr + kN + c, u);
+          uint32_t u[16];
+          tc::tmem_ld16(lane_addr + kN + c, u);
           tc::tmem_ld_wait();
           __half* h = static_cast<__half*>(a.out);
           const int col = (irow & ~7) | pair_pos(irow & 7);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < 16; ++j) {
             const int n = c + j;
             const int e = __shfl_sync(0xffffffffu, my_e, j);
             if (n < t.nvalid) {
@@ -475,7 +500,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::tmem_ld_wait();
           float* y = static_cast<float*>(a.out);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < 16; ++j) {
             const int n = c + j;
             const float up = exp2i(__shfl_sync(0xffffffffu, my_e, j));
             if (n < t.nvalid)
@@ -623,7 +648,7 @@ cudaError_t launch_gemm_tc_t(const TcArgs& a, const void* b_rows, int64_t rows, 
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
-  grouped_gemm_tc_kernel<kGateUp, kN, kBits><<<num_sms, kTcThreads, C::SMEM, stream>>>(map, c0, c1,
+  grouped_gemm_tc_kernel<kGateUp, kN, kBits><<<num_sms, C::THREADS, C::SMEM, stream>>>(map, c0, c1,
                                                                                          a);
   return cudaGetLastError();
 }
