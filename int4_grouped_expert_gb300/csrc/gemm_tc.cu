@@ -63,7 +63,10 @@ struct TcCfg {
                                      : (kGateUp ? 3 : 4);
   static constexpr int A_BYTES = kTcBM * kTcBK * 2;    // 16 KB per weight matrix
   static constexpr int B_BYTES = kN * kTcBK * 2;       // 32 KB (kN = 256) or 8 KB (64)
-  static constexpr int BOX_ROWS = kN < 128 ? kN : 128;  // TMA box of token rows x 64 columns
+  // TMA box of token rows x 64 columns: the whole tile for 64-row tiles, else 32 rows, so that a
+  // stage loads only the boxes its MMAs read (the B tile's shared-memory writes are part of the
+  // per-stage traffic that bounds these kernels)
+  static constexpr int BOX_ROWS = kN < 128 ? kN : 32;
   static constexpr int BOX_BYTES = BOX_ROWS * kTcBK * 2;
   static constexpr int NMAT = kGateUp ? 2 : 1;
   static constexpr int STAGE_BYTES = NMAT * A_BYTES + B_BYTES;
@@ -209,7 +212,7 @@ __global__ void __launch_bounds__((TcCfg<kGateUp, kN, kBits>::THREADS), 1)
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         TcTile t;
         tc_decode<kN>(a, item, nseg, mtiles, t);
-        const int nbox = t.nmma > C::BOX_ROWS ? 2 : 1;  // only the rows the MMA reads
+        const int nbox = (t.nmma + C::BOX_ROWS - 1) / C::BOX_ROWS;  // only the rows the MMA reads
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % ST;
           const uint32_t ph = (it / ST) & 1;
