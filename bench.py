@@ -352,6 +352,19 @@ def measured_traffic(key):
         return None
 
 
+def stale_traffic_note(key):
+    """When measured_traffic(key) is None because the source changed: the last capture's figure and
+    profile, for context (it no longer describes the current kernel)."""
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))[key]
+    except Exception:
+        return None
+    if measured_traffic(key) is not None:
+        return None
+    return (f"no capture of the current {rec['source']}; the last one measured "
+            f"{rec['bytes_per_launch'] / 1e6:.1f} MB per launch ({rec['profile']})")
+
+
 def peak_numbers():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -446,7 +459,9 @@ def run_strata(args):
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": gu_bytes,
                      "traffic": (measured_traffic("decode_gate_up")
-                                 if args.bits == 4 and args.group == 128 else None)},
+                                 if args.bits == 4 and args.group == 128 else None),
+                     "traffic_note": (stale_traffic_note("decode_gate_up")
+                                      if args.bits == 4 and args.group == 128 else None)},
         "layer_hbm": {"achieved_gbs": layer_gbs, "frac": layer_gbs / peak,
                       "bytes_per_step": n_exp * eb, "experts_per_step": n_exp},
         "stages_us": {k: v * 1e3 for k, v in stages.items()},

@@ -38,6 +38,13 @@
 //    first MMAs start from zero, so nothing is cleared per group. Weights are never rounded.
 //  * Small batches split the contraction; the last split to arrive (device counter per warp tile)
 //    sums the partials in split order and applies the epilogue, so results stay deterministic.
+//  * The smallest batches (fewer than two tiles per CTA, tile = chunk x row block) take the kEven
+//    schedule instead: the launch's stages (tiles x K/128, tiles in chunk-fastest order) are cut
+//    into one equal contiguous range per CTA, so that every CTA streams the same weight bytes. A
+//    tile whose stages fall into two or more CTAs' ranges is split; its pieces publish partial
+//    sums in per-CTA slots (a CTA has at most two split pieces: its range's first and last) and
+//    the last piece to arrive sums them in piece order. With two or more tiles per CTA, claiming
+//    whole tiles is faster: a CTA that streams faster takes more.
 // Gate/up writes h = silu(u) * v (bf16); down writes y (fp32) for the combine.
 #include <cudaTypedefs.h>
 
@@ -69,6 +76,7 @@ struct StageHdr {
   int e, rbase, nvalid, blk, ks, cidx;  // item: expert, first GEMM row, rows, row block, split, chunk
   int g, gbeg, gend;                    // this stage's group and the item's group range
   int done;                             // no more items
+  int split;                            // kEven: the piece's split word (split_np, split_slot)
 };
 static_assert(CtaLayout<false>::kHdrOff + static_cast<int>(sizeof(StageHdr)) <=
                   CtaLayout<false>::kStageBytes,
@@ -128,6 +136,22 @@ __device__ __forceinline__ int act_swz(int n, int q) {
   return kG == 64 ? q ^ (n & 1) : q ^ ((q >> 3) & 1) ^ ((n & 1) << 1);
 }
 
+// kEven schedule. The CTA whose stage range holds stage u, the ranges being [c W / C, (c + 1) W / C)
+// for c = 0 .. C - 1 with C <= W (no range is empty): the largest c with c W / C <= u.
+__device__ __forceinline__ int cta_of_stage(int u, int W, int C) {
+  return static_cast<int>(((static_cast<int64_t>(u) + 1) * C + W - 1) / W) - 1;
+}
+// A piece's split word: bits 0-11 the tile's first CTA c0, bits 12-23 the tile's pieces np (CTAs
+// c0 .. c0 + np - 1; 1 = not split), bit 24 set when the piece is not its CTA's first (its slot is
+// then 2 cta + 1, else 2 cta), bit 25 set when the tile's first piece is not c0's first piece (its
+// slot is then 2 c0 + 1, else 2 c0); the later pieces are their CTAs' first (slots 2 c). A launch
+// has at most 4096 CTAs (checked on the host), so c0 and np fit.
+__device__ __forceinline__ int split_np(int w) { return (w >> 12) & 0xFFF; }
+__device__ __forceinline__ int split_slot(int w, int pc) {
+  const int c = (w & 0xFFF) + pc;
+  return 2 * c + (pc == 0 ? (w >> 25) & 1 : 0);
+}
+
 struct CtaGemmParams {
   GemmArgs a;
   int nblk;   // row blocks per expert
@@ -135,7 +159,8 @@ struct CtaGemmParams {
 };
 
 // map0/map1: codes of gate (or down) / up; smap0/smap1: their scales (kScTma only).
-template <bool kGateUp, int kG, bool kScTma>
+// kEven: the equal-stage-range schedule of the smallest batches (see above).
+template <bool kGateUp, int kG, bool kScTma, bool kEven>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     grouped_gemm_cta_kernel(const __grid_constant__ CUtensorMap map0,
                             const __grid_constant__ CUtensorMap map1,
@@ -189,10 +214,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint32_t phase = 0;
     bool waited = kGateUp;  // down: griddep_wait still pending (h comes from gate/up)
     int npend = 0;          // down, first item: stages whose activation copies wait for it
+    bool ok = true;
+    if constexpr (!kEven) {
     int item = 0;
     if (lane == 0) item = atomicAdd(next_ctr, 1);
     item = __shfl_sync(0xffffffffu, item, 0);
-    bool ok = true;
     while (item < n_items && ok) {
       int nxt = 0;
       if (lane == 0) nxt = atomicAdd(next_ctr, 1);
@@ -298,6 +324,131 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
       item = __shfl_sync(0xffffffffu, nxt, 0);
+    }
+    } else {
+    // this CTA's stage range; C = the CTAs that get a range (each at least one stage); the host
+    // takes this schedule only for launches with fewer than two tiles per CTA, so W is small
+    const int W = nchunks * p.nblk * ngroups;
+    const int C = W < static_cast<int>(gridDim.x) ? W : static_cast<int>(gridDim.x);
+    const int cta = blockIdx.x;
+    constexpr int kRB = kGateUp ? kCW * 16 : kCW * 32;  // p.RB as a constant
+    int u = cta < C ? static_cast<int>(static_cast<int64_t>(cta) * W / C) : 0;
+    const int u_end = cta < C ? static_cast<int>(static_cast<int64_t>(cta + 1) * W / C) : 0;
+    bool first_piece = true;
+    while (u < u_end && ok) {
+      // the piece: stages [gbeg, gend) of tile `tile`
+      const int tile = u / ngroups;
+      const int t0u = tile * ngroups;  // the tile's first stage
+      const int gbeg = u - t0u;
+      const int gend = u_end - t0u < ngroups ? u_end - t0u : ngroups;
+      // CTAs c0 .. c0 + np - 1 hold the tile's pieces; each CTA's range is contiguous, so a CTA
+      // has a split tile only as its first piece (slot 2 cta) and its last (slot 2 cta + 1)
+      const int c0 = cta_of_stage(t0u, W, C);
+      const int np = cta_of_stage(t0u + ngroups - 1, W, C) - c0 + 1;
+      const int split = c0 | (np << 12) | (first_piece ? 0 : 1 << 24) |
+                        (static_cast<int64_t>(c0) * W / C == t0u ? 0 : 1 << 25);
+      first_piece = false;
+      u = t0u + gend;
+      const int cidx = tile % nchunks;
+      const int blk = tile / nchunks;
+      const int4 ch = __ldg(a.chunk_list + cidx);
+      const int e = ch.x, rbase = ch.y, nvalid = ch.z;
+      const int64_t wrow0 = static_cast<int64_t>(e) * a.N + static_cast<int64_t>(blk) * kRB;
+      // activation rows of this lane's pieces (n = 2 i + lane / 16) and which of them are live
+      int arow[4];
+      unsigned amask = 0;
+      // down: h rows come from gate/up (wait for it before the first activation copy)
+      for (int g = gbeg; g < gend; ++g) {
+        if (!tc::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
+        // The consumers read the slot through the generic proxy; the TMA boxes below write it
+        // through the async proxy. The empty barrier orders those reads before this point, and
+        // this cross-proxy fence orders them before the new boxes (without it, a warp's loads of
+        // the slot's first rows could return the next stage's bytes, about one forward in 100).
+        tc::fence_proxy_async_smem();
+        unsigned char* st = smem + stage * kStageBytes;
+        // weights and scales are read once per call: evict them from L2 first (made here, per
+        // stage, so that the policy holds no register across the loop)
+        const uint64_t pol = l2_evict_first_policy();
+        if (lane == 0) {
+          StageHdr* h = reinterpret_cast<StageHdr*>(st + kHdrOff);
+          h->e = e; h->rbase = rbase; h->nvalid = nvalid; h->blk = blk; h->ks = 0; h->cidx = cidx;
+          h->g = g; h->gbeg = gbeg; h->gend = gend; h->done = 0; h->split = split;
+          tc::mbar_arrive_expect_tx(&full[stage], tx_bytes);
+          tc::tma_load_2d_hint(st, &map0, g * 64, static_cast<int32_t>(wrow0), &full[stage], pol);
+          if (kGateUp)
+            tc::tma_load_2d_hint(st + kRB * 64, &map1, g * 64, static_cast<int32_t>(wrow0),
+                                 &full[stage], pol);
+          if (kScTma) {
+            // the aligned run of 8 scale groups holding this stage's group(s): 16 bytes per row
+            const int sx = (kG == 64 ? 2 * g : kG == 128 ? g : g >> 1) & ~7;
+            tc::tma_load_2d_hint(st + kScOff, &smap0, sx, static_cast<int32_t>(wrow0),
+                                 &full[stage], pol);
+            if (kGateUp)
+              tc::tma_load_2d_hint(st + kScOff + kRB * 16, &smap1, sx,
+                                   static_cast<int32_t>(wrow0), &full[stage], pol);
+          }
+        }
+        // scales: the 4-byte fp16 pair holding group g, 8 rows per lane
+        // 4-byte scale pair holding this block's scale(s): groups 2g, 2g+1 (kG = 64), g (128) or
+        // g / 2 (256), the pair starting at an even group
+        const int gp = kG == 64 ? 2 * g : kG == 128 ? (g & ~1) : ((g >> 1) & ~1);
+#pragma unroll
+        for (int i = 0; i < (kScTma ? 0 : 8); ++i) {
+          const int r = lane + 32 * i;  // stage scale row
+          const __half* sbase;
+          int64_t row;
+          if (kGateUp) {
+            sbase = r < kRB ? a.scales0 : a.scales1;
+            row = wrow0 + (r < kRB ? r : r - kRB);
+          } else {
+            sbase = a.scales0;
+            row = wrow0 + r;
+          }
+          const bool in = kGateUp ? true : (blk * kRB + r < a.N);
+          cp_async4(tc::smem_u32(st + kScOff + r * 4), sbase + (in ? row : wrow0) * srow + gp, in,
+                    pol);
+        }
+        if (g == gbeg) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int n = 2 * i + (lane >> 4);
+            const bool live = n < nvalid;
+            amask |= live ? 1u << i : 0u;
+            int src = rbase + (live ? n : 0);
+            if (a.perm) src = __ldg(a.perm + src);
+            arow[i] = src;
+          }
+        }
+        auto issue_act = [&](int gg, unsigned char* sst, uint64_t* bar) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int n = 2 * i + (lane >> 4);
+            const uint32_t dst = tc::smem_u32(sst + kActOff + n * 256 + (act_swz<kG>(n, q) << 4));
+            const __nv_bfloat16* src = a.act + static_cast<int64_t>(arow[i]) * a.K + gg * kBlockK;
+            cp_async16s(dst, reinterpret_cast<const char*>(src) + q * 16, (amask >> i) & 1u);
+          }
+          cp_async_arrive_noinc(bar);
+        };
+        if (waited) {
+          issue_act(g, st, &full[stage]);
+        } else {
+          // down, first piece: weights and scales of up to kStages groups go out before waiting
+          // for gate/up (which writes h); their activation copies follow the wait
+          ++npend;
+          if (npend == kStages || g == gend - 1) {
+            griddep_wait();
+            waited = true;
+            int s0 = stage - (npend - 1);
+            if (s0 < 0) s0 += kStages;
+            for (int j = 0; j < npend; ++j) {
+              const int ss = (s0 + j) % kStages;
+              issue_act(g - (npend - 1) + j, smem + ss * kStageBytes, &full[ss]);
+            }
+          }
+        }
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
     }
     if (!waited) griddep_wait();
     if (ok && tc::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status)) {
@@ -430,7 +581,40 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int mt = hd.blk * kCW + warp;  // global tile index of this warp inside the expert
     if (mt * mtile >= a.N) continue;     // rows past the expert (last, partial block)
     bool write = true;
-    if (KS > 1) {
+    if constexpr (kEven) {
+      const int np = split_np(hd.split);
+      if (np > 1) {
+        // split tile: publish this piece's partial sums; the last piece to arrive reduces them
+        const int tile = (hd.cidx * p.nblk + hd.blk) * kCW + warp;
+        const int slot = 2 * static_cast<int>(blockIdx.x) + ((hd.split >> 24) & 1);
+        float* part = a.split_part + (static_cast<int64_t>(slot) * kCW + warp) * 256 + lane * 8;
+        reinterpret_cast<float4*>(part)[0] = make_float4(acc0[0], acc0[1], acc0[2], acc0[3]);
+        reinterpret_cast<float4*>(part)[1] = make_float4(acc1[0], acc1[1], acc1[2], acc1[3]);
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          last = (atomicAdd(a.split_cnt + tile, 1) == np - 1);
+          if (last) a.split_cnt[tile] = 0;  // ready for the next launch that uses the scratch
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        write = last != 0;
+        if (last) {
+          __threadfence();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) { acc0[c] = 0.f; acc1[c] = 0.f; }
+          for (int pc = 0; pc < np; ++pc) {  // piece order: deterministic
+            const float* src = a.split_part +
+                               (static_cast<int64_t>(split_slot(hd.split, pc)) * kCW + warp) * 256 +
+                               lane * 8;
+            const float4 u = __ldcg(reinterpret_cast<const float4*>(src));
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(src) + 1);
+            acc0[0] += u.x; acc0[1] += u.y; acc0[2] += u.z; acc0[3] += u.w;
+            acc1[0] += v.x; acc1[1] += v.y; acc1[2] += v.z; acc1[3] += v.w;
+          }
+        }
+      }
+    } else if (KS > 1) {
       // split-K: publish this split's partial sums; the last split to arrive reduces them
       const int tile = (hd.cidx * p.nblk + hd.blk) * kCW + warp;
       float* part = a.split_part + (static_cast<int64_t>(tile) * KS + hd.ks) * 256 + lane * 8;
@@ -532,8 +716,10 @@ static bool make_scales_tmap(CUtensorMap* m, const void* base, int64_t rows, int
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kGateUp, int kG, bool kScTma>
+template <bool kGateUp, int kG, bool kScTma, bool kEven>
 cudaError_t launch_t(const GemmArgs& a, int64_t experts, int num_sms, cudaStream_t stream) {
+  // the kEven split words hold CTA indices and piece counts in 12 bits
+  if (kEven && (num_sms < 1 || num_sms * kCtasPerSm > 4096)) return cudaErrorInvalidValue;
   CtaGemmParams p;
   p.a = a;
   p.RB = cta_gemm_block_rows(kGateUp);
@@ -551,7 +737,7 @@ cudaError_t launch_t(const GemmArgs& a, int64_t experts, int num_sms, cudaStream
     s0 = m0;  // not read
     s1 = m1;
   }
-  auto kern = grouped_gemm_cta_kernel<kGateUp, kG, kScTma>;
+  auto kern = grouped_gemm_cta_kernel<kGateUp, kG, kScTma, kEven>;
   constexpr int smem = CtaLayout<kScTma>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)  // two CTAs per SM need (nearly) all of its shared memory
@@ -564,12 +750,16 @@ cudaError_t launch_t(const GemmArgs& a, int64_t experts, int num_sms, cudaStream
 
 // The TMA scale path when every scale row starts on a 16-byte boundary.
 template <bool kGateUp, int kG>
-cudaError_t launch_g(const GemmArgs& a, int64_t experts, int num_sms, cudaStream_t stream) {
+cudaError_t launch_g(const GemmArgs& a, int64_t experts, int num_sms, bool even,
+                     cudaStream_t stream) {
   const int64_t row_bytes = static_cast<int64_t>(a.K / kG) * 2;
   const bool tma = row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(a.scales0) % 16 == 0 &&
                    (!kGateUp || reinterpret_cast<uintptr_t>(a.scales1) % 16 == 0);
-  return tma ? launch_t<kGateUp, kG, true>(a, experts, num_sms, stream)
-             : launch_t<kGateUp, kG, false>(a, experts, num_sms, stream);
+  if (even)
+    return tma ? launch_t<kGateUp, kG, true, true>(a, experts, num_sms, stream)
+               : launch_t<kGateUp, kG, false, true>(a, experts, num_sms, stream);
+  return tma ? launch_t<kGateUp, kG, true, false>(a, experts, num_sms, stream)
+             : launch_t<kGateUp, kG, false, false>(a, experts, num_sms, stream);
 }
 
 }  // namespace
@@ -578,18 +768,30 @@ int cta_gemm_block_rows(bool gate_up) { return gate_up ? kCW * 16 : kCW * 32; }
 int cta_gemm_warps() { return kCW; }
 
 cudaError_t launch_gemm_cta(const GemmArgs& a, bool gate_up, int64_t experts, int num_sms,
-                            cudaStream_t stream) {
+                            bool even, cudaStream_t stream) {
   switch (a.group) {
     case 64:
-      return gate_up ? launch_g<true, 64>(a, experts, num_sms, stream)
-                     : launch_g<false, 64>(a, experts, num_sms, stream);
+      return gate_up ? launch_g<true, 64>(a, experts, num_sms, even, stream)
+                     : launch_g<false, 64>(a, experts, num_sms, even, stream);
     case 256:
-      return gate_up ? launch_g<true, 256>(a, experts, num_sms, stream)
-                     : launch_g<false, 256>(a, experts, num_sms, stream);
+      return gate_up ? launch_g<true, 256>(a, experts, num_sms, even, stream)
+                     : launch_g<false, 256>(a, experts, num_sms, even, stream);
     default:
-      return gate_up ? launch_g<true, 128>(a, experts, num_sms, stream)
-                     : launch_g<false, 128>(a, experts, num_sms, stream);
+      return gate_up ? launch_g<true, 128>(a, experts, num_sms, even, stream)
+                     : launch_g<false, 128>(a, experts, num_sms, even, stream);
   }
+}
+
+// The kEven schedule for a launch with at most max_tiles (chunk x row block) tiles: when even
+// that many leave fewer than two tiles per CTA.
+bool cta_gemm_even(int64_t max_tiles, int num_sms) {
+  return max_tiles < 2 * static_cast<int64_t>(num_sms) * kCtasPerSm;
+}
+
+// kEven partial-sum scratch of a launch on num_sms SMs: two slots per CTA (its range's first and
+// last piece), 256 floats per consumer warp each.
+int64_t cta_gemm_partial_floats(int num_sms) {
+  return static_cast<int64_t>(2) * num_sms * kCtasPerSm * kCW * 256;
 }
 
 // Contraction splits for a batch whose grouped GEMM has `items` (chunk x row block) work items:

@@ -70,6 +70,20 @@ __device__ __forceinline__ GroupSmem carve_group_smem(int* base, int NW, int E) 
 }
 
 // ids: the [T, k] ids (global or shared memory).
+// The split-K arrival counters of nchunks chunks, zeroed by threads tid = 0 .. nt - 1 (16-byte
+// stores when the count and the base allow them).
+__device__ __forceinline__ void zero_split_counters(const PermuteArgs& a, int nchunks, int tid,
+                                                    int nt) {
+  const int n = nchunks * a.cnt_per_chunk;
+  if ((n & 3) == 0 && (reinterpret_cast<uintptr_t>(a.split_cnt) & 15) == 0) {
+#pragma unroll 1
+    for (int i = tid; i < n / 4; i += nt) reinterpret_cast<int4*>(a.split_cnt)[i] = make_int4(0, 0, 0, 0);
+  } else {
+#pragma unroll 1
+    for (int i = tid; i < n; i += nt) a.split_cnt[i] = 0;
+  }
+}
+
 template <int NW>
 __device__ void group_rows(const PermuteArgs& a, const int* ids, GroupSmem sm) {
   constexpr int NT = NW * 32;
@@ -200,8 +214,7 @@ __device__ void group_rows(const PermuteArgs& a, const int* ids, GroupSmem sm) {
       a.hdr->next_gu = 0;
       a.hdr->next_dn = 0;
     }
-    if (a.split_cnt)
-      for (int i = tid; i < nchunks * a.cnt_per_chunk; i += NT) a.split_cnt[i] = 0;
+    if (a.split_cnt) zero_split_counters(a, nchunks, tid, NT);
     return;
   }
   // Tensor-core path: tiles per segment = (token chunks) x (row tiles); prefix over segments.
@@ -354,10 +367,7 @@ __device__ void group_rows_small(const PermuteArgs& a, const int* ids, int* smem
 #pragma unroll 1
   for (int q = tid; q < sh_chunks; q += NT)
     a.chunk_list[q] = make_int4(E, R + q * a.tokc, min(a.tokc, a.T - q * a.tokc), 0);
-  if (a.split_cnt) {
-#pragma unroll 1
-    for (int i = tid; i < nchunks * a.cnt_per_chunk; i += NT) a.split_cnt[i] = 0;
-  }
+  if (a.split_cnt) zero_split_counters(a, nchunks, tid, NT);
   __syncthreads();
   // positions: expert offset + marked rows of that expert below r (stable by token)
 #pragma unroll 1

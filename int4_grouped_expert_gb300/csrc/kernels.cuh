@@ -117,8 +117,12 @@ cudaError_t launch_gemm_warp(const GemmArgs& a, bool gate_up, int num_sms, cudaS
 int cta_gemm_block_rows(bool gate_up);
 int cta_gemm_warps();
 int cta_gemm_ksplit(int64_t items, int64_t K, int num_sms);
+// even: the equal-stage-range schedule (cta_gemm_even), which needs cta_gemm_partial_floats(num_sms)
+// floats of split_part and one split_cnt counter per (chunk, row block, consumer warp)
+bool cta_gemm_even(int64_t max_tiles, int num_sms);
+int64_t cta_gemm_partial_floats(int num_sms);
 cudaError_t launch_gemm_cta(const GemmArgs& a, bool gate_up, int64_t experts, int num_sms,
-                            cudaStream_t stream);
+                            bool even, cudaStream_t stream);
 int warp_ksplit(int64_t T, int E, int k, int shared, int64_t I, int64_t H);
 constexpr int kTcRows = 256;      // token rows per tensor-core tile
 constexpr int kTcRowsSmall = 64;  // the same for batches with few rows per expert

@@ -47,6 +47,7 @@ struct FwdLayout {
   int ksplit;     // gate/up contraction splits (warp paths)
   int ksplit_dn;  // down contraction splits (CTA-staged warp path)
   int nblk_gu, nblk_dn;  // CTA-staged warp path: row blocks per expert
+  bool even_gu, even_dn; // CTA-staged warp path: equal stage ranges per CTA (smallest batches)
   bool tc;   // tensor-core path for the grouped GEMMs
   bool cta;  // CTA-staged warp GEMM (else the per-warp one)
 };
@@ -55,7 +56,8 @@ struct FwdLayout {
 #define STRATA_WARP_GEMM_LEGACY 0
 #endif
 // SM count the work split is sized for (the same on every device, so the workspace size and the
-// launch agree); it only steers how many contraction splits small batches get.
+// launch agree): it steers how many contraction splits small batches get and which take equal
+// stage ranges, whose partial-sum scratch is sized for at most this many SMs.
 constexpr int kSizingSms = 152;
 
 // Tensor-core path for batches with enough rows per expert to fill 128 x N tiles, and for layers
@@ -108,16 +110,24 @@ static FwdLayout fwd_layout(const strata_moe_layer* L, int64_t T) {
           aligned(L->gate_scales, 4) && aligned(L->up_scales, 4) && aligned(L->down_scales, 4);
   F.ksplit = 1;
   F.ksplit_dn = 1;
+  F.even_gu = F.even_dn = false;
   int64_t part_floats = 0, ncnt = 0;
   if (F.cta) {
     F.nblk_gu = static_cast<int>((L->I + cta_gemm_block_rows(true) - 1) / cta_gemm_block_rows(true));
     F.nblk_dn = static_cast<int>((L->H + cta_gemm_block_rows(false) - 1) / cta_gemm_block_rows(false));
-    F.ksplit = cta_gemm_ksplit(segs * F.nblk_gu, L->H, kSizingSms);
-    F.ksplit_dn = cta_gemm_ksplit(segs * F.nblk_dn, L->I, kSizingSms);
-    // per split tile: one 256-float partial per consumer warp
-    const int64_t tgu = F.ksplit > 1 ? max_chunks * F.nblk_gu * cta_gemm_warps() : 0;
-    const int64_t tdn = F.ksplit_dn > 1 ? max_chunks * F.nblk_dn * cta_gemm_warps() : 0;
-    part_floats = std::max(tgu * F.ksplit, tdn * F.ksplit_dn) * 256;
+    // batches that leave fewer than two tiles per CTA take equal stage ranges, the others whole
+    // tiles with contraction splits
+    F.even_gu = cta_gemm_even(max_chunks * F.nblk_gu, kSizingSms);
+    F.even_dn = cta_gemm_even(max_chunks * F.nblk_dn, kSizingSms);
+    if (!F.even_gu) F.ksplit = cta_gemm_ksplit(segs * F.nblk_gu, L->H, kSizingSms);
+    if (!F.even_dn) F.ksplit_dn = cta_gemm_ksplit(segs * F.nblk_dn, L->I, kSizingSms);
+    // per split tile: one arrival counter per consumer warp; split-K: one 256-float partial per
+    // split too; equal ranges: two slots per CTA
+    const bool cnt_gu = F.ksplit > 1 || F.even_gu, cnt_dn = F.ksplit_dn > 1 || F.even_dn;
+    const int64_t tgu = cnt_gu ? max_chunks * F.nblk_gu * cta_gemm_warps() : 0;
+    const int64_t tdn = cnt_dn ? max_chunks * F.nblk_dn * cta_gemm_warps() : 0;
+    part_floats = std::max((F.ksplit > 1 ? tgu * F.ksplit : 0), (F.ksplit_dn > 1 ? tdn * F.ksplit_dn : 0)) * 256;
+    if (F.even_gu || F.even_dn) part_floats = std::max(part_floats, cta_gemm_partial_floats(kSizingSms));
     ncnt = std::max(tgu, tdn);
   } else if (!F.tc) {
     F.ksplit = warp_ksplit(T, L->E, L->k, L->has_shared, L->I, L->H);
@@ -258,7 +268,7 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     pa.mtiles_dn = F.nblk_dn;
     pa.ksplit_gu = F.ksplit;
     pa.ksplit_dn = F.ksplit_dn;
-    pa.cnt_per_chunk = (F.ksplit > 1 || F.ksplit_dn > 1)
+    pa.cnt_per_chunk = (F.ksplit > 1 || F.ksplit_dn > 1 || F.even_gu || F.even_dn)
                            ? std::max(F.nblk_gu, F.nblk_dn) * cta_gemm_warps() : 0;
     pa.chunk_list = reinterpret_cast<int4*>(base + F.chunk_list);
   } else {
@@ -374,7 +384,10 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     g.split_part = reinterpret_cast<float*>(base + F.split_part);
     g.split_cnt = pa.split_cnt;
     const int64_t experts = E + S;
-    e = F.cta ? launch_gemm_cta(g, true, experts, sms, st) : launch_gemm_warp(g, true, sms, st);
+    // the equal-range schedule's scratch is sized for at most kSizingSms SMs
+    e = F.cta ? launch_gemm_cta(g, true, experts, F.even_gu ? std::min(sms, kSizingSms) : sms,
+                                F.even_gu, st)
+              : launch_gemm_warp(g, true, sms, st);
     if (e != cudaSuccess || !mark(3)) return STRATA_ERR_CUDA;
     GemmArgs d = g;
     d.codes0 = L->down_codes;
@@ -389,7 +402,9 @@ static strata_status run_forward(const strata_moe_layer* L, const void* x, int64
     d.K = static_cast<int>(L->I);
     d.N = static_cast<int>(L->H);
     d.ksplit = F.cta ? F.ksplit_dn : 1;
-    e = F.cta ? launch_gemm_cta(d, false, experts, sms, st) : launch_gemm_warp(d, false, sms, st);
+    e = F.cta ? launch_gemm_cta(d, false, experts, F.even_dn ? std::min(sms, kSizingSms) : sms,
+                                F.even_dn, st)
+              : launch_gemm_warp(d, false, sms, st);
     if (e != cudaSuccess || !mark(4)) return STRATA_ERR_CUDA;
   }
 
