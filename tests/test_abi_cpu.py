@@ -75,7 +75,7 @@ def layer(st, **kw):
 def test_workspace_sizes(st):
     s1 = st.strata_moe_workspace_size(layer(st), 1)
     s16 = st.strata_moe_workspace_size(layer(st), 16)
-    assert s1 > 0 and s16 > 0          # (tiny batches add split-K scratch, so no monotonicity)
+    assert s1 > 0 and s16 > 0          # (tiny batches add partial-sum scratch: no monotonicity)
     assert s16 % 256 == 0 and s1 % 256 == 0
     # h (bf16 [T*k+T, I]) and y (fp32 [T*k+T, H]) dominate
     assert s16 >= 2 * 144 * 1536 + 4 * 144 * 4096
@@ -83,6 +83,17 @@ def test_workspace_sizes(st):
     assert st.strata_moe_workspace_size(layer(st, k=0), 4) == 0
     assert st.strata_moe_workspace_size(layer(st, E=1024, has_shared=1), 4) == 0
     assert st.strata_route_workspace_size(16, 288, 8) > 0
+
+
+def test_workspace_follows_the_decode_schedule(st):
+    """The decode GEMMs cut their stages into equal ranges per CTA when a batch leaves fewer than two
+    tiles per CTA, and those ranges need two 8 KB partial-sum slots per CTA (2 x 152 SMs). Here
+    tiles = (T*k/8 + segments) chunks x 12 (gate/up) or 16 (down) row blocks: T <= 4 stays below
+    2 x 304, T = 8 claims whole tiles with no contraction split and needs no slots."""
+    slots = 2 * 152 * 2 * 8 * 256 * 4
+    for T in (1, 2, 4):
+        assert st.strata_moe_workspace_size(layer(st), T) >= slots
+    assert st.strata_moe_workspace_size(layer(st), 8) < slots
 
 
 @pytest.mark.parametrize("kw,expect", [(dict(H=1000), 2), (dict(I=100), 2), (dict(k=9, E=8), 1),
