@@ -4,10 +4,11 @@ GEMMs captured as fixed graph nodes at a maximum batch, smaller batches padded w
 GEMM" as the last step of the ladder).
 
 One graph is captured at T_max = 16 on the decode layer (hidden 4096, 288 experts top-8 + shared)
-and replayed with 1, 5, 16 and 0 live tokens written to the device count. Rows of x beyond the live
-tokens hold NaN (they must never be read), rows of out beyond them hold a sentinel (they must not
-be written). Live rows are compared with the oracle; at T = T_max the padded call must equal the
-unpadded one bit for bit (same launch configuration).
+and replayed with 1, 5, 16 and 0 live tokens written to the device count; a second one at T_max = 4
+(where the decode GEMMs cut their stages into equal ranges per CTA) with 1, 3, 4 and 0. Rows of x
+beyond the live tokens hold NaN (they must never be read), rows of out beyond them hold a sentinel
+(they must not be written). Live rows are compared with the oracle; at T = T_max the padded call
+must equal the unpadded one bit for bit (same launch configuration).
 """
 import numpy as np
 import pytest
@@ -21,15 +22,19 @@ pytestmark = pytest.mark.gpu
 
 NAN_BF16 = 0x7FC0
 SENTINEL = 0x1234
-T_MAX = 16
 
 
 @pytest.fixture(scope="module")
-def captured():
+def layer_c2():
+    wl = CONFIGS["c2"]
+    return (wl,) + tuple(build_gpu_layer(wl))
+
+
+def capture(layer, T_MAX):
+    """The padded forward at T_MAX, captured once in a CUDA graph."""
     import torch
     import int4_grouped_expert_gb300 as st
-    wl = CONFIGS["c2"]
-    L, wr, b = build_gpu_layer(wl)
+    wl, L, wr, b = layer
     x_static = torch.zeros(T_MAX, wl.H, dtype=torch.int16, device="cuda").view(torch.bfloat16)
     out = torch.empty_like(x_static)
     n_tok = torch.full((1,), T_MAX, dtype=torch.int32, device="cuda")
@@ -46,12 +51,22 @@ def captured():
     return wl, L, wr, b, g, x_static, out, n_tok, ws
 
 
+@pytest.fixture(scope="module")
+def captured16(layer_c2):
+    return capture(layer_c2, 16)
+
+
+@pytest.fixture(scope="module")
+def captured4(layer_c2):
+    return capture(layer_c2, 4)
+
+
 def replay(cap, live_bits, count):
     """Write the live rows (NaN padding) and the count, replay the graph, return out's bits."""
     import torch
     import int4_grouped_expert_gb300 as st
     wl, L, wr, b, g, x_static, out, n_tok, ws = cap
-    xs = np.full((T_MAX, wl.H), NAN_BF16, dtype=np.uint16)
+    xs = np.full((x_static.shape[0], wl.H), NAN_BF16, dtype=np.uint16)
     xs[:live_bits.shape[0]] = live_bits
     x_static.copy_(bf16_tensor(xs))
     n_tok.fill_(count)
@@ -61,8 +76,10 @@ def replay(cap, live_bits, count):
     return bf16_to_np_bits(out), st.strata_workspace_status(ws)
 
 
-@pytest.mark.parametrize("T", [1, 5, 16, 0])
-def test_one_graph_serves_every_batch_up_to_the_maximum(captured, T):
+@pytest.mark.parametrize("T_MAX,T", [(16, 1), (16, 5), (16, 16), (16, 0),
+                                     (4, 1), (4, 3), (4, 4), (4, 0)])
+def test_one_graph_serves_every_batch_up_to_the_maximum(request, T_MAX, T):
+    captured = request.getfixturevalue(f"captured{T_MAX}")
     wl, L, wr, b = captured[:4]
     xb = gen.activations(max(T, 1), wl.H, wl.seed, name=f"padded/{T}")[:T]
     got, (s, v) = replay(captured, xb, T)
@@ -78,11 +95,12 @@ def test_one_graph_serves_every_batch_up_to_the_maximum(captured, T):
     compare_output(got[rows], oracle_pool.moe_forward(wl, xb, wr, b, rows)["out"])
 
 
-@pytest.mark.parametrize("count", [T_MAX + 1, -1])
-def test_a_count_beyond_the_maximum_runs_no_token(captured, count):
+@pytest.mark.parametrize("count", [17, -1])
+def test_a_count_beyond_the_maximum_runs_no_token(captured16, count):
     import int4_grouped_expert_gb300 as st
+    captured = captured16
     wl = captured[0]
-    xb = gen.activations(T_MAX, wl.H, wl.seed, name="padded/bad")
+    xb = gen.activations(16, wl.H, wl.seed, name="padded/bad")
     got, (s, v) = replay(captured, xb, count)
     assert s == st.STRATA_ERR_DEVICE_STATUS
     assert v == st.STRATA_DEV_BAD_TOKENS, f"device status 0x{v:x}"
