@@ -38,12 +38,12 @@
 //    first MMAs start from zero, so nothing is cleared per group. Weights are never rounded.
 //  * Small batches split the contraction; the last split to arrive (device counter per warp tile)
 //    sums the partials in split order and applies the epilogue, so results stay deterministic.
-//  * The smallest batches (fewer than two tiles per CTA, tile = chunk x row block) take the kEven
+//  * The smallest batches (at most two tiles per CTA, tile = chunk x row block) take the kEven
 //    schedule instead: the launch's stages (tiles x K/128, tiles in chunk-fastest order) are cut
 //    into one equal contiguous range per CTA, so that every CTA streams the same weight bytes. A
 //    tile whose stages fall into two or more CTAs' ranges is split; its pieces publish partial
 //    sums in per-CTA slots (a CTA has at most two split pieces: its range's first and last) and
-//    the last piece to arrive sums them in piece order. With two or more tiles per CTA, claiming
+//    the last piece to arrive sums them in piece order. With more tiles per CTA, claiming
 //    whole tiles is faster: a CTA that streams faster takes more.
 // Gate/up writes h = silu(u) * v (bf16); down writes y (fp32) for the combine.
 #include <cudaTypedefs.h>
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     } else {
     // this CTA's stage range; C = the CTAs that get a range (each at least one stage); the host
-    // takes this schedule only for launches with fewer than two tiles per CTA, so W is small
+    // takes this schedule only for launches with at most two tiles per CTA, so W is small
     const int W = nchunks * p.nblk * ngroups;
     const int C = W < static_cast<int>(gridDim.x) ? W : static_cast<int>(gridDim.x);
     const int cta = blockIdx.x;
@@ -783,9 +783,10 @@ cudaError_t launch_gemm_cta(const GemmArgs& a, bool gate_up, int64_t experts, in
 }
 
 // The kEven schedule for a launch with at most max_tiles (chunk x row block) tiles: when even
-// that many leave fewer than two tiles per CTA.
+// that many leave at most two tiles per CTA (the count is an upper bound: experts that several
+// tokens share make fewer chunks).
 bool cta_gemm_even(int64_t max_tiles, int num_sms) {
-  return max_tiles < 2 * static_cast<int64_t>(num_sms) * kCtasPerSm;
+  return max_tiles <= 2 * static_cast<int64_t>(num_sms) * kCtasPerSm;
 }
 
 // kEven partial-sum scratch of a launch on num_sms SMs: two slots per CTA (its range's first and

@@ -115,7 +115,7 @@ static FwdLayout fwd_layout(const strata_moe_layer* L, int64_t T) {
   if (F.cta) {
     F.nblk_gu = static_cast<int>((L->I + cta_gemm_block_rows(true) - 1) / cta_gemm_block_rows(true));
     F.nblk_dn = static_cast<int>((L->H + cta_gemm_block_rows(false) - 1) / cta_gemm_block_rows(false));
-    // batches that leave fewer than two tiles per CTA take equal stage ranges, the others whole
+    // batches that leave at most two tiles per CTA take equal stage ranges, the others whole
     // tiles with contraction splits
     F.even_gu = cta_gemm_even(max_chunks * F.nblk_gu, kSizingSms);
     F.even_dn = cta_gemm_even(max_chunks * F.nblk_dn, kSizingSms);

@@ -86,14 +86,18 @@ def test_workspace_sizes(st):
 
 
 def test_workspace_follows_the_decode_schedule(st):
-    """The decode GEMMs cut their stages into equal ranges per CTA when a batch leaves fewer than two
-    tiles per CTA, and those ranges need two 8 KB partial-sum slots per CTA (2 x 152 SMs). Here
-    tiles = (T*k/8 + segments) chunks x 12 (gate/up) or 16 (down) row blocks: T <= 4 stays below
-    2 x 304, T = 8 claims whole tiles with no contraction split and needs no slots."""
+    """The decode GEMMs cut their stages into equal ranges per CTA when a batch leaves at most two
+    tiles per CTA, and those ranges need two 8 KB partial-sum slots per CTA (2 x 152 SMs). At most
+    ((T*k + T)/8 + segments) chunks x 12 (gate/up) or 16 (down) row blocks: on the 288-expert
+    layer T <= 4 stays within 2 x 304 tiles, and T = 8 (up to 74 x 16) claims whole tiles with no
+    contraction split and needs no slots. On the 128-expert top-4 layer (I = 2048) T = 8 reaches
+    exactly 38 x 16 = 608 tiles and takes equal ranges."""
     slots = 2 * 152 * 2 * 8 * 256 * 4
     for T in (1, 2, 4):
         assert st.strata_moe_workspace_size(layer(st), T) >= slots
     assert st.strata_moe_workspace_size(layer(st), 8) < slots
+    assert st.strata_moe_workspace_size(layer(st, I=2048, E=128, k=4), 8) >= slots
+    assert st.strata_moe_workspace_size(layer(st, I=2048, E=128, k=4), 16) < slots
 
 
 @pytest.mark.parametrize("kw,expect", [(dict(H=1000), 2), (dict(I=100), 2), (dict(k=9, E=8), 1),
