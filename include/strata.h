@@ -259,9 +259,10 @@ strata_status strata_moe_forward(const strata_moe_layer* layer, const void* x_bf
  *           with a copy in stream order before the replay).
  * x_bf16    [T_max, H] bf16 (device); rows T..T_max-1 are never read and may hold anything.
  * out_bf16  [T_max, H] bf16 (device); rows 0..T-1 get exactly what strata_moe_forward gives for
- *           those T tokens up to the order of its split-K sums (the contraction split is chosen
- *           for T_max); rows T..T_max-1 are not written. The padding tokens route to no expert and
- *           cost no weight traffic: every grid is sized for T_max, every loop stops at T.
+ *           those T tokens up to the order of its contraction sums (the GEMMs' schedule, and with
+ *           it how a contraction is split between CTAs, is chosen for T_max); rows T..T_max-1 are
+ *           not written. The padding tokens route to no expert and cost no weight traffic: every
+ *           grid is sized for T_max, every loop stops at T.
  * A count outside [0, T_max] sets STRATA_DEV_BAD_TOKENS in the device status word and the call
  * then runs with no live token (out untouched).
  * T_max: 1..64 (the fused decode router); 4-bit codes; not STRATA_FORCE_TC_PATH. Otherwise
